@@ -1,0 +1,138 @@
+"""Seeded synthetic inputs for the five workloads.
+
+This module draws random numbers with the shapes, sizes and value distributions of the workloads
+and nothing else: it holds no quantisation and no attention arithmetic.  Both the oracle tests and
+the CUDA-path tests / benchmark take their inputs from here.
+
+Generator: numpy's ``default_rng(seed)`` (PCG64), seed = 1000 + workload number.  Normal draws
+are f32; "bf16 queries" are f32 N(0,1) draws rounded to bf16 by torch (round-to-nearest-even).
+
+Workloads (one query position = one decode step of one layer):
+  1 tiny      H=16,  T=256     rows N(0,1)*10^U(-3,2); row 17 all zero (element 0 = -0.0);
+                               row 42 N(0,1)*1e-39 (subnormal amax); q f32 N(0,1)
+  2 dec16k    H=128, T=16384   rows N(0,1)*10^U(-1,1); row T-1 is the fresh f32 row; q bf16
+  3 dec262k   H=128, T=262144  as 2, plus a seeded 1% of rows times 50; q bf16
+  4 dsa       B=8, H=128, T=131072 per sequence, NS=2048 sorted unique indices uniform in [0,T)
+  5 prefill   S=1024, H=128, T=65536, pos0=64512; rows 64512.. are the fresh f32 rows; q bf16
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+D, KL, KR = 576, 512, 64
+SM_SCALE = float(np.float32(1.0 / np.sqrt(192.0)))
+
+
+@dataclass(frozen=True)
+class Workload:
+    key: str
+    number: int
+    H: int
+    T: int
+    B: int = 1
+    NS: int = 0
+    S: int = 1
+    pos0: int = 0
+    mag_lo: float = 0.1
+    mag_hi: float = 10.0
+    heavy_frac: float = 0.0
+    heavy_mult: float = 1.0
+    q_f32: bool = False
+
+    @property
+    def seed(self) -> int:
+        return 1000 + self.number
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", 1, H=16, T=256, mag_lo=1e-3, mag_hi=1e2, q_f32=True),
+    "dec16k": Workload("dec16k", 2, H=128, T=16384),
+    "dec262k": Workload("dec262k", 3, H=128, T=262144, heavy_frac=0.01, heavy_mult=50.0),
+    "dsa": Workload("dsa", 4, H=128, T=131072, B=8, NS=2048),
+    "prefill": Workload("prefill", 5, H=128, T=65536, S=1024, pos0=64512),
+}
+
+DESCRIPTIONS = {
+    "tiny": "tiny decode: 1 query, H=16, T=256, f32 queries",
+    "dec16k": "single-sequence decode: H=128, T=16384, bf16 queries, 1 fresh row quantized per step",
+    "dec262k": "long-context split-T decode: H=128, T=262144 (152 MB fp8 rows + scales), bf16 queries, "
+               "1 fresh row quantized per step, 1% of rows x50",
+    "dsa": "DSA sparse decode: B=8 sequences x T=131072 rows, NS=2048 selected rows each, H=128, bf16 queries",
+    "prefill": "causal prefill chunk: S=1024 queries at 64512..65535 over T=65536 rows, H=128, bf16 queries",
+}
+
+
+def rng_for(w: Workload, stream: int = 0) -> np.random.Generator:
+    return np.random.default_rng([w.seed, stream])
+
+
+def latent_rows(rng: np.random.Generator, n: int, mag_lo: float, mag_hi: float,
+                heavy_frac: float = 0.0, heavy_mult: float = 1.0) -> np.ndarray:
+    """f32 [n][576]: N(0,1) per element times a per-row magnitude log-uniform in [mag_lo, mag_hi];
+    a Bernoulli(heavy_frac) subset of rows is further multiplied by heavy_mult."""
+    x = rng.standard_normal((n, D), dtype=np.float32)
+    mag = 10.0 ** rng.uniform(np.log10(mag_lo), np.log10(mag_hi), size=n)
+    if heavy_frac > 0.0:
+        heavy = rng.random(n) < heavy_frac
+        mag = np.where(heavy, mag * heavy_mult, mag)
+    x *= mag.astype(np.float32)[:, None]
+    return x
+
+
+def normal_f32(rng: np.random.Generator, shape) -> np.ndarray:
+    return rng.standard_normal(shape, dtype=np.float32)
+
+
+def to_bf16_values(x: np.ndarray) -> np.ndarray:
+    """Round f32 -> bf16 (RNE, by torch) and return the bf16 values as f32 (exact)."""
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).to(torch.float32).numpy()
+
+
+def rows_for(w: Workload, seq: int = 0, start: int = 0, count: int | None = None) -> np.ndarray:
+    """f32 latent rows [count][576] of sequence `seq`, rows start..start+count-1.  Rows are drawn in
+    fixed blocks of 4096 so any sub-range reproduces the same values."""
+    if count is None:
+        count = w.T - start
+    blk = 4096
+    out = np.empty((count, D), dtype=np.float32)
+    b0, b1 = start // blk, (start + count - 1) // blk if count > 0 else start // blk - 1
+    for b in range(b0, b1 + 1):
+        rng = np.random.default_rng([w.seed, 1, seq, b])
+        n_b = min(blk, w.T - b * blk)
+        rows = latent_rows(rng, n_b, w.mag_lo, w.mag_hi, w.heavy_frac, w.heavy_mult)
+        if w.key == "tiny":
+            for t in range(n_b):
+                g = b * blk + t
+                if g == 17:
+                    rows[t, :] = 0.0
+                    rows[t, 0] = -0.0
+                elif g == 42:
+                    rows[t, :] = (rng.standard_normal(D).astype(np.float64) * 1e-39).astype(np.float32)
+        lo = max(start, b * blk)
+        hi = min(start + count, b * blk + n_b)
+        out[lo - start:hi - start] = rows[lo - b * blk:hi - b * blk]
+    return out
+
+
+def queries_for(w: Workload, n_query: int | None = None):
+    """(q_lat, q_rope) as f32 arrays holding the query values ([nq][H][512], [nq][H][64]).
+    For bf16 workloads the values are bf16-representable."""
+    if n_query is None:
+        n_query = w.S if w.key == "prefill" else w.B
+    rng = rng_for(w, 2)
+    q = normal_f32(rng, (n_query, w.H, D))
+    if not w.q_f32:
+        q = to_bf16_values(q)
+    return np.ascontiguousarray(q[..., :KL]), np.ascontiguousarray(q[..., KL:])
+
+
+def selection_for(w: Workload) -> np.ndarray:
+    """idx [B][NS] int32: per sequence, NS unique indices drawn uniformly from [0, T), sorted."""
+    rng = rng_for(w, 3)
+    out = np.empty((w.B, w.NS), dtype=np.int32)
+    for b in range(w.B):
+        out[b] = np.sort(rng.choice(w.T, size=w.NS, replace=False)).astype(np.int32)
+    return out

@@ -1,0 +1,418 @@
+"""Pins for the oracle: checks against things other than the oracle itself.
+
+Each test fixes the oracle to a closed form, an invariant, a hand-derived value (tests/golden/,
+each file citing its source), brute force, or an independent library routine (torch's
+float8_e4m3fn conversion).  Chosen so that a dropped term, a wrong sign or index, or a transposed
+operand in the oracle fails at least one of them.  CPU only.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+D, KL, KR = 576, 512, 64
+
+
+def f32_from_bits(h):
+    return np.array([h], dtype=np.uint32).view(np.float32)[0]
+
+
+def torch_e4m3(y: np.ndarray) -> np.ndarray:
+    """torch's f32 -> float8_e4m3fn conversion (round to nearest even), as bytes."""
+    return torch.from_numpy(np.ascontiguousarray(y, dtype=np.float32)).to(torch.float8_e4m3fn).view(
+        torch.uint8).numpy()
+
+
+# ------------------------------------------------------------------------------------------------
+# e4m3 decode table
+# ------------------------------------------------------------------------------------------------
+def test_decode_table_matches_torch_float8(oracle):
+    tab = oracle.e4m3_table()
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert list(np.nonzero(nan)[0]) == [0x7F, 0xFF]
+    assert np.all(np.isnan(tab[nan]))
+    assert np.array_equal(tab[~nan], ref[~nan])
+    # signed zero
+    assert math.copysign(1.0, tab[0x80]) == -1.0 and math.copysign(1.0, tab[0x00]) == 1.0
+
+
+def test_decode_closed_form_points(oracle):
+    assert oracle.e4m3_decode(0x7E) == 448.0
+    assert oracle.e4m3_decode(0x08) == 2.0 ** -6
+    assert oracle.e4m3_decode(0x01) == 2.0 ** -9
+    assert oracle.e4m3_decode(0x07) == 7 * 2.0 ** -9
+    assert oracle.e4m3_decode(0x38) == 1.0
+    assert oracle.e4m3_decode(0xFE) == -448.0
+    # the table is strictly increasing over 0x00..0x7E
+    tab = oracle.e4m3_table()
+    assert np.all(np.diff(tab[:0x7F]) > 0)
+
+
+# ------------------------------------------------------------------------------------------------
+# e4m3 encode
+# ------------------------------------------------------------------------------------------------
+def _golden_encode_cases():
+    cases = []
+    with open(os.path.join(GOLDEN, "e4m3_encode_cases.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            bits, code, *_ = line.split()
+            cases.append((int(bits, 16), int(code, 16), line))
+    return cases
+
+
+def test_encode_golden_cases(oracle):
+    cases = _golden_encode_cases()
+    assert len(cases) >= 25
+    for bits, code, line in cases:
+        y = f32_from_bits(bits)
+        assert oracle.e4m3_encode(y) == code, line
+        assert oracle.e4m3_encode_scan(y) == code, line
+
+
+def _interesting_values(oracle, rng):
+    tab = oracle.e4m3_table()[:0x7F]
+    mids = (tab[:-1] + tab[1:]) / 2
+    pts = np.concatenate([tab, mids, [464.0, 447.99, 0.0]]).astype(np.float32)
+    bits = pts.view(np.uint32).astype(np.int64)
+    near = (bits[:, None] + np.arange(-3, 4)[None, :]).reshape(-1)
+    near = near[(near >= 0) & (near < 0x7F800000)].astype(np.uint32).view(np.float32)
+    rand = (rng.standard_normal(200_000) * 10.0 ** rng.uniform(-6, 3, 200_000)).astype(np.float32)
+    vals = np.concatenate([near, -near, rand])
+    return vals[np.abs(vals) <= 464.0]
+
+
+def test_encode_matches_torch_rne_in_range(oracle):
+    """Inside |y| <= 464, where no saturation or NaN rule applies, the encoder is plain RNE and
+    must equal torch's conversion (an independent implementation)."""
+    rng = np.random.default_rng(7)
+    vals = _interesting_values(oracle, rng)
+    got = oracle.encode_array(vals)
+    ref = torch_e4m3(vals)
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, [(float(vals[i]), hex(got[i]), hex(ref[i])) for i in bad[:10]]
+
+
+def test_encode_bisection_equals_scan(oracle):
+    rng = np.random.default_rng(8)
+    vals = _interesting_values(oracle, rng)[::37]
+    vals = np.concatenate([vals, [np.inf, -np.inf, np.nan, 1e30, -1e30]]).astype(np.float32)
+    for v in vals:
+        assert oracle.e4m3_encode(v) == oracle.e4m3_encode_scan(v), v
+
+
+def test_encode_saturation_and_nan(oracle):
+    for v in [448.0, 449.0, 464.0, 465.0, 480.0, 1e6, 3.4e38, np.inf]:
+        assert oracle.e4m3_encode(v) == 0x7E
+        assert oracle.e4m3_encode(-v) == 0xFE
+    for bits in [0x7FC00000, 0xFFC00000, 0x7F800001, 0xFFFFFFFF, 0x7FFFFFFF]:
+        assert oracle.e4m3_encode(f32_from_bits(bits)) == 0x00
+
+
+def test_encode_roundtrip_all_codes(oracle):
+    """encode(decode(b)) == b for the 254 non-NaN codes (page: exhaustive e4m3 roundtrip)."""
+    tab = oracle.e4m3_table()
+    for b in range(256):
+        if b in (0x7F, 0xFF):
+            continue
+        assert oracle.e4m3_encode(np.float32(tab[b])) == b, hex(b)
+
+
+def test_encode_change_points_structure(oracle):
+    """The change-point list the exhaustive GPU test compares against: 126 steps per sign, codes
+    rising by exactly one at each, every step agreeing with torch at p and p-1."""
+    cp = oracle.encode_change_points()
+    assert len(cp) == 126 + 2 + 126 + 1
+    assert np.all(np.diff(cp.astype(np.int64)) > 0)
+    pos = cp[:126]
+    neg = cp[128:254]
+    assert list(cp[126:128]) == [0x7F800001, 0x80000000] and cp[-1] == 0xFF800001
+    for group, sign in ((pos, 0), (neg, 0x80)):
+        for k, p in enumerate(group):
+            a = oracle.e4m3_encode(f32_from_bits(int(p)))
+            b = oracle.e4m3_encode(f32_from_bits(int(p) - 1))
+            assert a == sign | (k + 1) and b == sign | k
+            ya = np.array([f32_from_bits(int(p)), f32_from_bits(int(p) - 1)], dtype=np.float32)
+            if np.all(np.abs(ya) <= 464.0):
+                assert list(torch_e4m3(ya)) == [a, b]
+
+
+# ------------------------------------------------------------------------------------------------
+# row quantizer
+# ------------------------------------------------------------------------------------------------
+def _golden_quant_cases():
+    out = []
+    with open(os.path.join(GOLDEN, "quant_rows_cases.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            elems, scale, codes = [p.strip() for p in line.split("|")]
+            x = np.zeros(D, dtype=np.float32)
+            e = [np.float32(v) for v in elems.split()]
+            x[:len(e)] = e
+            c = np.zeros(D, dtype=np.uint8)
+            cc = [int(v, 16) for v in codes.split()]
+            c[:len(cc)] = cc
+            out.append((x, int(scale, 16), c, line))
+    return out
+
+
+def test_quant_golden_rows(oracle):
+    for x, scale_bits, codes, line in _golden_quant_cases():
+        q, s = oracle.quant_rows(x[None, :])
+        assert s.view(np.uint32)[0] == scale_bits, line
+        assert np.array_equal(q[0], codes), line
+
+
+def test_quant_matches_torch_on_normal_rows(oracle):
+    """scale = amax/448 and y = x*(448/amax) in f32, then RNE: torch does the same steps with its
+    own f32 ops and its own fp8 conversion (|y| <= 448 here, so no saturation rule applies)."""
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal((300, D)) * 10.0 ** rng.uniform(-20, 20, (300, 1))).astype(np.float32)
+    q, s = oracle.quant_rows(x)
+    xt = torch.from_numpy(x)
+    amax = xt.abs().amax(dim=1)
+    st = amax / 448.0
+    inv = torch.tensor(448.0, dtype=torch.float32) / amax
+    y = xt * inv[:, None]
+    qt = y.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(s.view(np.uint32), st.numpy().view(np.uint32))
+    assert np.array_equal(q, qt)
+
+
+def test_quant_amax_element_and_zero_row(oracle):
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((50, D)).astype(np.float32)
+    q, s = oracle.quant_rows(x)
+    i = np.abs(x).argmax(axis=1)
+    for r in range(50):
+        assert q[r, i[r]] == (0xFE if x[r, i[r]] < 0 else 0x7E)
+    z = np.zeros((1, D), dtype=np.float32)
+    z[0, 5] = -0.0
+    qz, sz = oracle.quant_rows(z)
+    assert sz[0] == 0.0 and qz[0, 5] == 0x80 and np.count_nonzero(qz) == 1
+
+
+def test_quant_scale_invariance_and_subnormal_guard(oracle):
+    """Scaling a row by 2^k changes its scale by 2^k and not its bytes; a subnormal-amax row (where
+    448/amax overflows) gives the bytes of the same row scaled into the normal range."""
+    rng = np.random.default_rng(13)
+    base = rng.standard_normal((20, D)).astype(np.float32)
+    q0, s0 = oracle.quant_rows(base)
+    for k in (-40, -5, 7, 60):
+        qk, sk = oracle.quant_rows((base.astype(np.float64) * 2.0 ** k).astype(np.float32))
+        assert np.array_equal(qk, q0)
+        assert np.array_equal(sk, (s0.astype(np.float64) * 2.0 ** k).astype(np.float32))
+    # subnormal amax: build rows whose values are exactly base * 2^-140 (representable only with
+    # fewer bits, so compare against the same reduced-precision values scaled by 2^64).
+    sub = (base.astype(np.float64) * 2.0 ** -140).astype(np.float32)
+    assert np.all(np.abs(sub).max(axis=1) < 448.0 / np.finfo(np.float32).max)
+    qs, ss = oracle.quant_rows(sub)
+    up = (sub.astype(np.float64) * 2.0 ** 64).astype(np.float32)
+    qu, su = oracle.quant_rows(up)
+    assert np.array_equal(qs, qu)
+    assert np.all(ss >= 0.0) and np.all(np.isfinite(ss))
+
+
+def test_quant_error_bound(oracle):
+    """|dequant - x| <= half an e4m3 step of y, times the scale (plus the f32 rounding of y)."""
+    rng = np.random.default_rng(14)
+    x = (rng.standard_normal((200, D)) * 10.0 ** rng.uniform(-3, 3, (200, 1))).astype(np.float32)
+    q, s = oracle.quant_rows(x)
+    deq = oracle.dequant_rows(q, s)
+    y = np.abs(x.astype(np.float64)) * (448.0 / np.abs(x).max(axis=1, keepdims=True).astype(np.float64))
+    e = np.floor(np.log2(np.maximum(y, 2.0 ** -6)))
+    half_step = 0.5 * 2.0 ** (e - 3)
+    bound = (half_step * (1 + 1e-6) + 448.0 * 2.0 ** -23) * s[:, None].astype(np.float64) * (1 + 1e-6)
+    assert np.all(np.abs(deq - x) <= bound)
+
+
+# ------------------------------------------------------------------------------------------------
+# attention (decode / split / select / prefill)
+# ------------------------------------------------------------------------------------------------
+def _rand_cache(rng, T, mag=1.0):
+    codes = rng.integers(0, 256, size=(T, D), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3C  # no NaN codes
+    scale = (rng.uniform(0.5, 2.0, T) * mag).astype(np.float32)
+    return codes, scale
+
+
+def test_attn_single_row_returns_dequantized_row(oracle):
+    rng = np.random.default_rng(20)
+    kv, sc = _rand_cache(rng, 1)
+    ql = rng.standard_normal((3, KL)).astype(np.float32)
+    qr = rng.standard_normal((3, KR)).astype(np.float32)
+    out = oracle.attn_decode(ql, qr, kv, sc, 0.07)
+    tab = oracle.e4m3_table()
+    want = (tab[kv[0, :KL]] * np.float64(sc[0])).astype(np.float32)
+    for h in range(3):
+        assert np.array_equal(out[h], want)
+
+
+def test_attn_zero_query_is_mean_of_rows(oracle):
+    rng = np.random.default_rng(21)
+    kv, sc = _rand_cache(rng, 37)
+    out = oracle.attn_decode(np.zeros((2, KL)), np.zeros((2, KR)), kv, sc, 0.3)
+    tab = oracle.e4m3_table()
+    deq = tab[kv[:, :KL]] * sc.astype(np.float64)[:, None]
+    np.testing.assert_allclose(out[0], deq.mean(axis=0), rtol=1e-6, atol=1e-30)
+
+
+def _two_row_case(which):
+    """Two rows that differ only in one coordinate of Lc (index 511) or Rc (index 63)."""
+    kv = np.full((2, D), 0x38, dtype=np.uint8)  # every element 1.0
+    kv[1, :KL] = 0x40  # row 1's latent is 2.0 everywhere
+    sc = np.array([1.0, 1.0], dtype=np.float32)
+    ql = np.zeros((1, KL), dtype=np.float32)
+    qr = np.zeros((1, KR), dtype=np.float32)
+    if which == "rope":
+        kv[0, KL + 63] = 0x38   # 1.0
+        kv[1, KL + 63] = 0xC0   # -2.0
+        qr[0, 63] = 1.5
+        s = np.array([1.5 * 1.0, 1.5 * -2.0])
+    else:
+        # Lc row 1 is 2.0 at index 511 as well; q_lat picks index 511 only
+        ql[0, 511] = -0.75
+        s = np.array([-0.75 * 1.0, -0.75 * 2.0])
+    return kv, sc, ql, qr, s
+
+
+@pytest.mark.parametrize("which", ["rope", "latent"])
+def test_attn_two_rows_closed_form(oracle, which):
+    kv, sc, ql, qr, s = _two_row_case(which)
+    sm = 0.625
+    out = oracle.attn_decode(ql, qr, kv, sc, sm)
+    w1 = 1.0 / (1.0 + math.exp(sm * (s[0] - s[1])))
+    w0 = 1.0 - w1
+    want = w0 * 1.0 + w1 * 2.0
+    np.testing.assert_allclose(out[0], np.full(KL, want), rtol=1e-7)
+
+
+def test_attn_row_scale_enters_score_and_value(oracle):
+    """Doubling a row's scale doubles its score and its value (s_t multiplies both)."""
+    kv = np.full((2, D), 0x38, dtype=np.uint8)
+    sc = np.array([1.0, 2.0], dtype=np.float32)
+    ql = np.zeros((1, KL), dtype=np.float32)
+    ql[0, 0] = 1.0
+    sm = 0.5
+    out = oracle.attn_decode(ql, np.zeros((1, KR)), kv, sc, sm)
+    s0, s1 = sm * 1.0 * 1.0, sm * 2.0 * 1.0
+    w1 = 1.0 / (1.0 + math.exp(s0 - s1))
+    want = (1 - w1) * 1.0 + w1 * 2.0
+    np.testing.assert_allclose(out[0], np.full(KL, want), rtol=1e-7)
+
+
+def test_attn_sharp_softmax_selects_argmax_row(oracle):
+    rng = np.random.default_rng(22)
+    kv, sc = _rand_cache(rng, 64)
+    ql = rng.standard_normal((4, KL)).astype(np.float32)
+    qr = rng.standard_normal((4, KR)).astype(np.float32)
+    tab = oracle.e4m3_table()
+    deq = tab[kv] * sc.astype(np.float64)[:, None]
+    scores = ql.astype(np.float64) @ deq[:, :KL].T + qr.astype(np.float64) @ deq[:, KL:].T
+    out = oracle.attn_decode(ql, qr, kv, sc, 1e4)
+    for h in range(4):
+        top = np.argsort(scores[h])[-2:]
+        assert (scores[h, top[1]] - scores[h, top[0]]) * 1e4 > 50  # a clear winner
+        np.testing.assert_allclose(out[h], deq[top[1], :KL], rtol=1e-6)
+
+
+def test_attn_permutation_invariance(oracle):
+    rng = np.random.default_rng(23)
+    kv, sc = _rand_cache(rng, 200)
+    ql = rng.standard_normal((3, KL)).astype(np.float32)
+    qr = rng.standard_normal((3, KR)).astype(np.float32)
+    perm = rng.permutation(200)
+    a = oracle.attn_decode(ql, qr, kv, sc, 0.05)
+    b = oracle.attn_decode(ql, qr, kv[perm], sc[perm], 0.05)
+    np.testing.assert_allclose(a, b, rtol=1e-6, atol=1e-12)
+
+
+@pytest.mark.parametrize("P", [1, 2, 7, 64, 300])
+def test_split_merge_equals_unsplit(oracle, P):
+    rng = np.random.default_rng(24)
+    T = 300
+    kv, sc = _rand_cache(rng, T)
+    ql = rng.standard_normal((5, KL)).astype(np.float32)
+    qr = rng.standard_normal((5, KR)).astype(np.float32)
+    ref = oracle.attn_decode(ql, qr, kv, sc, 0.08)
+    out, cl, m, z = oracle.attn_decode_split(ql, qr, kv, sc, 0.08, P)
+    np.testing.assert_allclose(out, ref, rtol=2e-6, atol=1e-30)
+    # each partial normalised on its own equals the dense result over its rows
+    for p in sorted({0, P // 2, P - 1}):
+        t0, t1 = T * p // P, T * (p + 1) // P
+        if t1 > t0:
+            np.testing.assert_allclose(cl[p] / z[p][:, None], oracle.attn_decode(ql, qr, kv[t0:t1], sc[t0:t1], 0.08),
+                                       rtol=2e-6, atol=1e-30)
+
+
+def test_split_with_empty_partitions(oracle):
+    rng = np.random.default_rng(25)
+    kv, sc = _rand_cache(rng, 3)
+    ql = rng.standard_normal((2, KL)).astype(np.float32)
+    qr = rng.standard_normal((2, KR)).astype(np.float32)
+    out, cl, m, z = oracle.attn_decode_split(ql, qr, kv, sc, 0.1, 8)  # 5 of 8 partitions empty
+    assert np.sum(np.isinf(m)) == 2 * 5 and np.all(z[np.isinf(m)] == 0)
+    np.testing.assert_allclose(out, oracle.attn_decode(ql, qr, kv, sc, 0.1), rtol=2e-6)
+
+
+def test_select_full_index_equals_dense_and_subset_equals_gathered(oracle):
+    rng = np.random.default_rng(26)
+    B, T, H = 3, 120, 2
+    kv, sc = _rand_cache(rng, B * T)
+    ql = rng.standard_normal((B, H, KL)).astype(np.float32)
+    qr = rng.standard_normal((B, H, KR)).astype(np.float32)
+    full = np.tile(np.arange(T, dtype=np.int32), (B, 1))
+    out, bad = oracle.attn_select(ql, qr, kv, sc, T, T, full, 0.07)
+    assert bad == 0
+    for b in range(B):
+        np.testing.assert_allclose(out[b], oracle.attn_decode(ql[b], qr[b], kv[b * T:(b + 1) * T],
+                                                              sc[b * T:(b + 1) * T], 0.07), rtol=1e-6)
+    sel = np.stack([np.sort(rng.choice(T, 17, replace=False)) for _ in range(B)]).astype(np.int32)
+    out, _ = oracle.attn_select(ql, qr, kv, sc, T, T, sel, 0.07)
+    for b in range(B):
+        rows = b * T + sel[b]
+        np.testing.assert_allclose(out[b], oracle.attn_decode(ql[b], qr[b], kv[rows], sc[rows], 0.07), rtol=1e-6)
+    one = sel[:, :1].copy()
+    out, _ = oracle.attn_select(ql, qr, kv, sc, T, T, one, 0.07)
+    tab = oracle.e4m3_table()
+    for b in range(B):
+        r = b * T + one[b, 0]
+        np.testing.assert_array_equal(out[b, 0], (tab[kv[r, :KL]] * np.float64(sc[r])).astype(np.float32))
+
+
+def test_select_skips_out_of_range(oracle):
+    rng = np.random.default_rng(27)
+    T = 50
+    kv, sc = _rand_cache(rng, 2 * T)
+    ql = rng.standard_normal((2, 1, KL)).astype(np.float32)
+    qr = rng.standard_normal((2, 1, KR)).astype(np.float32)
+    idx = np.array([[3, 60, 7, -1], [0, 1, 2, 49]], dtype=np.int32)
+    out, bad = oracle.attn_select(ql, qr, kv, sc, T, T, idx, 0.1)
+    assert bad == 2
+    np.testing.assert_allclose(out[0], oracle.attn_decode(ql[0], qr[0], kv[[3, 7]], sc[[3, 7]], 0.1), rtol=1e-6)
+
+
+def test_prefill_query_equals_decode_over_prefix(oracle):
+    rng = np.random.default_rng(28)
+    T, pos0, S, H = 90, 80, 10, 2
+    kv, sc = _rand_cache(rng, T)
+    ql = rng.standard_normal((S, H, KL)).astype(np.float32)
+    qr = rng.standard_normal((S, H, KR)).astype(np.float32)
+    pos = pos0 + np.arange(S)
+    out = oracle.attn_prefill(ql, qr, pos, kv, sc, 0.09)
+    for i in range(S):
+        ref = oracle.attn_decode(ql[i], qr[i], kv[:pos[i] + 1], sc[:pos[i] + 1], 0.09)
+        np.testing.assert_array_equal(out[i], ref)
+    # the first query cannot see the second query's row
+    kv2 = kv.copy()
+    kv2[pos0 + 1:] = 0x7E
+    out2 = oracle.attn_prefill(ql[:1], qr[:1], pos[:1], kv2, sc, 0.09)
+    np.testing.assert_array_equal(out2[0], out[0])
