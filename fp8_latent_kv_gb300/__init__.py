@@ -1,0 +1,163 @@
+"""Python binding of libkv8mla.so: fp8 latent-KV absorbed MLA attention for GB300 (sm_103a).
+
+Argument marshalling only: every step runs in the library's CUDA kernels.  Functions carry the C ABI
+names (include/kv8mla.h) and take torch CUDA tensors; the stream defaults to torch's current stream.
+A nonzero return code raises Kv8Error.  There is no fallback: if the library is missing or fails to
+load, `load()` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libkv8mla.so")
+
+KV8_ROW_BYTES, KV8_KL, KV8_KR = 576, 512, 64
+KV8_MAX_HEADS, KV8_MAX_ROWS, KV8_MAX_SELECT = 128, 1 << 20, 4096
+KV8_OK, KV8_EINVAL, KV8_EWORKSPACE, KV8_ECUDA, KV8_EUNSUPPORTED = 0, -1, -2, -3, -4
+KV8_ERR_INDEX, KV8_ERR_TIMEOUT = 1, 2
+KV8_F32, KV8_BF16 = 0, 1
+
+# (restype, argtypes) for every exported symbol of include/kv8mla.h
+_P, _I, _I64, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "kv8_encode_e4m3": (_I, [_P, _I64, _P, _P]),
+    "kv8_quant_rows": (_I, [_P, _I64, _P, _P, _P]),
+    "mla_decode8_partitions": (_I, [_I, _I64, _I, _P]),
+    "mla_decode8_workspace_bytes": (_I, [_I, _I64, _I, _P]),
+    "mla_decode8_partial": (_I, [_P, _P, _I, _I, _P, _P, _I64, _F, _I, _P, _SZ, _P, _P]),
+    "mla_lse_merge8": (_I, [_P, _I, _I, _I, _P, _P]),
+    "mla_absorb_decode8": (_I, [_P, _P, _I, _I, _P, _P, _I64, _F, _I, _P, _SZ, _P, _P, _P]),
+    "mla_sel8_workspace_bytes": (_I, [_I, _I, _I, _P]),
+    "mla_absorb_sel8": (_I, [_P, _P, _I, _I, _I, _P, _P, _I64, _I64, _P, _I, _F, _P, _SZ, _P, _P, _P]),
+    "mla_absorb_prefill8": (_I, [_P, _P, _I, _I, _I, _I64, _P, _P, _I64, _F, _P, _P, _P]),
+    "kv8_strerror": (ctypes.c_char_p, [_I]),
+}
+
+_lib = None
+
+
+class Kv8Error(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        msg = _lib.kv8_strerror(code).decode() if _lib is not None else str(code)
+        super().__init__(f"{fn} returned {code}: {msg}")
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libkv8mla.so (build it first with fp8_latent_kv_gb300.build / __graft_entry__.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build the CUDA library first (python -m fp8_latent_kv_gb300.build)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != KV8_OK:
+        raise Kv8Error(fn, rc)
+
+
+def _qdtype(q) -> int:
+    import torch
+    if q.dtype == torch.bfloat16:
+        return KV8_BF16
+    if q.dtype == torch.float32:
+        return KV8_F32
+    raise TypeError(f"queries must be float32 or bfloat16, got {q.dtype}")
+
+
+def kv8_encode_e4m3(y, out, stream=None) -> None:
+    _check("kv8_encode_e4m3", load().kv8_encode_e4m3(_ptr(y), y.numel(), _ptr(out), _stream(stream)))
+
+
+def kv8_quant_rows(x, kv8, kv_scale, n: int | None = None, stream=None) -> None:
+    """x [n][576] f32 -> kv8 [n][576] u8 (or a view starting at the first row to write), kv_scale [n]."""
+    n = x.shape[0] if n is None else n
+    _check("kv8_quant_rows", load().kv8_quant_rows(_ptr(x), n, _ptr(kv8), _ptr(kv_scale), _stream(stream)))
+
+
+def mla_decode8_partitions(H: int, T: int, P_req: int = 0) -> int:
+    out = ctypes.c_int(0)
+    _check("mla_decode8_partitions", load().mla_decode8_partitions(H, T, P_req, ctypes.addressof(out)))
+    return out.value
+
+
+def mla_decode8_workspace_bytes(H: int, T: int, P_req: int = 0) -> int:
+    out = ctypes.c_size_t(0)
+    _check("mla_decode8_workspace_bytes", load().mla_decode8_workspace_bytes(H, T, P_req, ctypes.addressof(out)))
+    return out.value
+
+
+def mla_decode8_partial(q_lat, q_rope, kv8, kv_scale, T: int, sm_scale: float, workspace, P_req: int = 0,
+                        err_word=None, stream=None) -> None:
+    H = q_lat.shape[-2]
+    _check("mla_decode8_partial", load().mla_decode8_partial(
+        _ptr(q_lat), _ptr(q_rope), _qdtype(q_lat), H, _ptr(kv8), _ptr(kv_scale), T, sm_scale, P_req,
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err_word), _stream(stream)))
+
+
+def mla_lse_merge8(workspace, B: int, P: int, H: int, out, stream=None) -> None:
+    _check("mla_lse_merge8", load().mla_lse_merge8(_ptr(workspace), B, P, H, _ptr(out), _stream(stream)))
+
+
+def mla_absorb_decode8(q_lat, q_rope, kv8, kv_scale, T: int, sm_scale: float, workspace, out, P_req: int = 0,
+                       err_word=None, stream=None) -> None:
+    H = q_lat.shape[-2]
+    _check("mla_absorb_decode8", load().mla_absorb_decode8(
+        _ptr(q_lat), _ptr(q_rope), _qdtype(q_lat), H, _ptr(kv8), _ptr(kv_scale), T, sm_scale, P_req,
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err_word), _ptr(out), _stream(stream)))
+
+
+def mla_sel8_workspace_bytes(B: int, H: int, NS: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check("mla_sel8_workspace_bytes", load().mla_sel8_workspace_bytes(B, H, NS, ctypes.addressof(out)))
+    return out.value
+
+
+def mla_absorb_sel8(q_lat, q_rope, kv8, kv_scale, T: int, seq_stride_rows: int, idx, sm_scale: float, workspace,
+                    out, err_word=None, stream=None) -> None:
+    B, NS = idx.shape
+    H = q_lat.shape[-2]
+    _check("mla_absorb_sel8", load().mla_absorb_sel8(
+        _ptr(q_lat), _ptr(q_rope), _qdtype(q_lat), B, H, _ptr(kv8), _ptr(kv_scale), T, seq_stride_rows, _ptr(idx),
+        NS, sm_scale, _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err_word), _ptr(out),
+        _stream(stream)))
+
+
+def mla_absorb_prefill8(q_lat, q_rope, pos0: int, kv8, kv_scale, T: int, sm_scale: float, out, err_word=None,
+                        stream=None) -> None:
+    S, H = q_lat.shape[0], q_lat.shape[1]
+    _check("mla_absorb_prefill8", load().mla_absorb_prefill8(
+        _ptr(q_lat), _ptr(q_rope), _qdtype(q_lat), S, H, pos0, _ptr(kv8), _ptr(kv_scale), T, sm_scale,
+        _ptr(err_word), _ptr(out), _stream(stream)))
+
+
+def kv8_strerror(code: int) -> str:
+    return load().kv8_strerror(code).decode()

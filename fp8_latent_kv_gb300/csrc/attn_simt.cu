@@ -1,0 +1,266 @@
+// attn_simt.cu -- absorbed MLA attention over e4m3 cache rows on the CUDA cores (sm_103a).
+//
+// Page "KV8 long-context CUDA: fp8 device shadow, split-T kernels, DSA-aware gather":
+//   first commit message  -- the latent is both key and value; the row scale is hoisted out of the
+//                            dot (score = sm_scale * s_t * q.e4m3(row)); context = softmax-weighted
+//                            sum of s_t * e4m3(Lc_t).
+//   second commit message -- split-T: partial online-softmax blocks (cl[K], m, z) plus a log-sum-exp
+//                            merge kernel; DSA gather: attend the selected rows of the device cache
+//                            by absolute index; batch/prefill path tiled over the rows.
+//
+// This is the general kernel: f32 or bf16 queries, any H in [1, 128], dense / selected / causal row
+// lists.  A block owns 32 heads and one partition of the row list; it streams 64-row tiles of the
+// cache through shared memory (16-byte loads), computes the 64x32 score tile, updates the online
+// softmax per head and accumulates the 32x512 context in registers (2 latent columns per thread).
+#include "internal.h"
+
+#include <math.h>
+
+namespace kv8 {
+namespace {
+
+constexpr int kHB = 32;        // heads per block
+constexpr int kTR = 64;        // rows per tile
+constexpr int kThreads = 256;  // 8 warps
+constexpr int kTileStride = kRow + 4;  // 580 bytes = 145 words: odd, so row-per-lane reads are conflict-free
+constexpr int kSStride = kHB + 1;
+
+struct Smem {
+    float q[kHB][kRow];               // queries of this block's heads (f32)
+    uint8_t tile[kTR][kTileStride];   // current cache tile
+    float s[kTR][kSStride];           // scores (log2 domain)
+    float p[kTR][kHB];                // weights p * s_t, row-major for broadcast reads
+    float rscale[kTR];                // row scale, 0 for an invalid row
+    int rvalid[kTR];
+    const uint8_t *rowptr[kTR];
+    float m_run[kHB], z_run[kHB], corr[kHB];
+};
+
+__device__ __forceinline__ float load_q(const void *base, int64_t i, int bf16) {
+    if (bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[i]);
+    return reinterpret_cast<const float *>(base)[i];
+}
+
+__global__ void __launch_bounds__(kThreads, 1) attn_simt_kernel(AttnArgs a) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int part = blockIdx.x, hb0 = blockIdx.y * kHB, b = blockIdx.z;
+    const int nh = min(kHB, a.H - hb0);
+
+    // ---- row list of this batch item and this partition
+    int64_t n_list;
+    if (a.idx) n_list = a.NS;
+    else if (a.pos0 >= 0) n_list = (a.pos0 + b + 1 < a.T) ? a.pos0 + b + 1 : a.T;
+    else n_list = a.T;
+    const int64_t j0 = n_list * part / a.P, j1 = n_list * (part + 1) / a.P;
+    const uint8_t *kv_b = a.kv8 + (int64_t)b * a.seq_stride_rows * kRow;
+    const float *sc_b = a.kv_scale + (int64_t)b * a.seq_stride_rows;
+    const int32_t *idx_b = a.idx ? a.idx + (int64_t)b * a.NS : nullptr;
+
+    // ---- queries -> shared (f32, exact)
+    for (int i = tid; i < kHB * kRow; i += kThreads) {
+        const int h = i / kRow, k = i - h * kRow;
+        float v = 0.f;
+        if (h < nh) {
+            const int64_t qh = (int64_t)b * a.H + hb0 + h;
+            v = (k < kKL) ? load_q(a.q_lat, qh * kKL + k, a.q_bf16) : load_q(a.q_rope, qh * kKR + (k - kKL), a.q_bf16);
+        }
+        sm.q[h][k] = v;
+    }
+    if (tid < kHB) {
+        sm.m_run[tid] = -INFINITY;
+        sm.z_run[tid] = 0.f;
+    }
+
+    float acc[kHB][2];
+#pragma unroll
+    for (int h = 0; h < kHB; ++h) acc[h][0] = acc[h][1] = 0.f;
+    bool bad_index = false;
+
+    for (int64_t jt = j0; jt < j1; jt += kTR) {
+        __syncthreads();  // previous tile fully consumed
+        // ---- row pointers and scales for this tile
+        if (tid < kTR) {
+            const int64_t j = jt + tid;
+            int valid = 0;
+            int64_t t = 0;
+            if (j < j1) {
+                t = idx_b ? (int64_t)idx_b[j] : j;
+                if (t >= 0 && t < a.T) valid = 1;
+                else bad_index = true;
+            }
+            sm.rvalid[tid] = valid;
+            sm.rowptr[tid] = valid ? kv_b + t * kRow : nullptr;
+            sm.rscale[tid] = valid ? sc_b[t] : 0.f;
+        }
+        __syncthreads();
+        // ---- tile load: 64 rows x 36 uint4
+        for (int c = tid; c < kTR * (kRow / 16); c += kThreads) {
+            const int r = c / (kRow / 16), col = c - r * (kRow / 16);
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            const uint8_t *rp = sm.rowptr[r];
+            if (rp) v = __ldg(reinterpret_cast<const uint4 *>(rp) + col);
+            uint32_t *dst = reinterpret_cast<uint32_t *>(&sm.tile[r][col * 16]);
+            dst[0] = v.x;
+            dst[1] = v.y;
+            dst[2] = v.z;
+            dst[3] = v.w;
+        }
+        __syncthreads();
+        // ---- scores: warp w -> heads (w&3)*8..+7, rows (w>>2)*32 + lane
+        {
+            const int g = warp & 3, r = (warp >> 2) * 32 + lane;
+            float s8[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) s8[j] = 0.f;
+            const uint32_t *rw = reinterpret_cast<const uint32_t *>(&sm.tile[r][0]);
+#pragma unroll 4
+            for (int k4 = 0; k4 < kRow / 4; ++k4) {
+                float e0, e1, e2, e3;
+                e4m3x4_to_f32(rw[k4], e0, e1, e2, e3);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 q4 = *reinterpret_cast<const float4 *>(&sm.q[g * 8 + j][k4 * 4]);
+                    s8[j] = fmaf(q4.x, e0, s8[j]);
+                    s8[j] = fmaf(q4.y, e1, s8[j]);
+                    s8[j] = fmaf(q4.z, e2, s8[j]);
+                    s8[j] = fmaf(q4.w, e3, s8[j]);
+                }
+            }
+            const float f = sm.rscale[r] * a.sm_scale_log2;
+            const bool ok = sm.rvalid[r] != 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) sm.s[r][g * 8 + j] = ok ? s8[j] * f : -INFINITY;
+        }
+        __syncthreads();
+        // ---- online softmax: thread -> head tid/8, rows (tid%8)*8..+7
+        {
+            const int h = tid >> 3, sub = tid & 7;
+            float mloc = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mloc = fmaxf(mloc, sm.s[sub * 8 + i][h]);
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
+            const float m_old = sm.m_run[h];
+            const float m_new = fmaxf(m_old, mloc);
+            float corr = 1.f, zloc = 0.f;
+            if (m_new == -INFINITY) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) sm.p[sub * 8 + i][h] = 0.f;
+            } else {
+                corr = exp2f(m_old - m_new);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int r = sub * 8 + i;
+                    const float pr = exp2f(sm.s[r][h] - m_new);
+                    zloc += pr;
+                    sm.p[r][h] = pr * sm.rscale[r];
+                }
+            }
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) zloc += __shfl_xor_sync(0xffffffffu, zloc, o);
+            __syncwarp();
+            if (sub == 0) {
+                sm.m_run[h] = m_new;
+                sm.z_run[h] = sm.z_run[h] * corr + zloc;
+                sm.corr[h] = corr;
+            }
+        }
+        __syncthreads();
+        // ---- context: thread -> latent columns 2*tid, 2*tid+1
+        {
+#pragma unroll
+            for (int h = 0; h < kHB; ++h) {
+                const float c = sm.corr[h];
+                acc[h][0] *= c;
+                acc[h][1] *= c;
+            }
+            const int nr = (j1 - jt) < kTR ? (int)(j1 - jt) : kTR;
+            for (int r = 0; r < nr; ++r) {
+                float v0, v1;
+                e4m3x2_to_f32(*reinterpret_cast<const uint16_t *>(&sm.tile[r][2 * tid]), v0, v1);
+#pragma unroll
+                for (int h4 = 0; h4 < kHB / 4; ++h4) {
+                    const float4 w = *reinterpret_cast<const float4 *>(&sm.p[r][h4 * 4]);
+                    acc[h4 * 4 + 0][0] = fmaf(w.x, v0, acc[h4 * 4 + 0][0]);
+                    acc[h4 * 4 + 0][1] = fmaf(w.x, v1, acc[h4 * 4 + 0][1]);
+                    acc[h4 * 4 + 1][0] = fmaf(w.y, v0, acc[h4 * 4 + 1][0]);
+                    acc[h4 * 4 + 1][1] = fmaf(w.y, v1, acc[h4 * 4 + 1][1]);
+                    acc[h4 * 4 + 2][0] = fmaf(w.z, v0, acc[h4 * 4 + 2][0]);
+                    acc[h4 * 4 + 2][1] = fmaf(w.z, v1, acc[h4 * 4 + 2][1]);
+                    acc[h4 * 4 + 3][0] = fmaf(w.w, v0, acc[h4 * 4 + 3][0]);
+                    acc[h4 * 4 + 3][1] = fmaf(w.w, v1, acc[h4 * 4 + 3][1]);
+                }
+            }
+        }
+    }
+    if (bad_index && a.err_word) atomicOr(a.err_word, (int)KV8_ERR_INDEX);
+    __syncthreads();
+
+    // ---- write the partial set, or the normalised output
+    if (a.ws) {
+        PartialView pv(a.ws, a.B, a.P, a.H);
+        const int64_t base = ((int64_t)b * a.P + part) * a.H + hb0;
+        for (int h = 0; h < nh; ++h)
+            reinterpret_cast<float2 *>(pv.cl + (base + h) * kKL)[tid] = make_float2(acc[h][0], acc[h][1]);
+        if (tid < nh) {
+            pv.m[base + tid] = sm.m_run[tid];
+            pv.z[base + tid] = sm.z_run[tid];
+        }
+    } else {
+        for (int h = 0; h < nh; ++h) {
+            const float z = sm.z_run[h];
+            const float inv = z > 0.f ? 1.f / z : 0.f;
+            reinterpret_cast<float2 *>(a.out + ((int64_t)b * a.H + hb0 + h) * kKL)[tid] =
+                make_float2(acc[h][0] * inv, acc[h][1] * inv);
+        }
+    }
+}
+
+// Log-sum-exp merge: block (h, b), 128 threads x 4 latent columns.
+__global__ void __launch_bounds__(128) lse_merge_kernel(const float *__restrict__ ws, int B, int P, int H,
+                                                        float *__restrict__ out) {
+    const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+    PartialView pv(const_cast<float *>(ws), B, P, H);
+    const int64_t base = (int64_t)b * P * H + h;
+    float M = -INFINITY;
+    for (int p = 0; p < P; ++p) M = fmaxf(M, pv.m[base + (int64_t)p * H]);
+    float Z = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+        for (int p = 0; p < P; ++p) {
+            const float mp = pv.m[base + (int64_t)p * H];
+            if (mp == -INFINITY) continue;
+            const float w = exp2f(mp - M);
+            Z = fmaf(w, pv.z[base + (int64_t)p * H], Z);
+            const float4 c = reinterpret_cast<const float4 *>(pv.cl + (base + (int64_t)p * H) * kKL)[tid];
+            acc.x = fmaf(w, c.x, acc.x);
+            acc.y = fmaf(w, c.y, acc.y);
+            acc.z = fmaf(w, c.z, acc.z);
+            acc.w = fmaf(w, c.w, acc.w);
+        }
+    }
+    const float inv = Z > 0.f ? 1.f / Z : 0.f;
+    reinterpret_cast<float4 *>(out + ((int64_t)b * H + h) * kKL)[tid] =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t st) {
+    const size_t smem = sizeof(Smem);
+    cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)a.P, (unsigned)((a.H + kHB - 1) / kHB), (unsigned)a.B);
+    attn_simt_kernel<<<grid, kThreads, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_lse_merge(const float *ws, int B, int P, int H, float *out, cudaStream_t st) {
+    dim3 grid((unsigned)H, (unsigned)B);
+    lse_merge_kernel<<<grid, 128, 0, st>>>(ws, B, P, H, out);
+    return cudaGetLastError();
+}
+
+}  // namespace kv8

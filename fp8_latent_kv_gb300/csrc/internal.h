@@ -1,0 +1,38 @@
+// internal.h -- host-side launchers behind the C ABI (not exported).
+#pragma once
+
+#include "common.cuh"
+
+namespace kv8 {
+
+// One attention problem set: B batch items (decode: 1; selection: B sequences; prefill: S queries),
+// each with H heads, attending a list of rows of a cache, split into P partitions.
+struct AttnArgs {
+    const void *q_lat;        // [B][H][512]
+    const void *q_rope;       // [B][H][64]
+    int q_bf16;               // 1: bf16 queries, 0: f32
+    int B, H;
+    const uint8_t *kv8;       // cache rows [*][576]
+    const float *kv_scale;    // [*]
+    int64_t T;                // rows in each batch item's cache
+    int64_t seq_stride_rows;  // rows between consecutive batch items' caches (selection), else 0
+    const int32_t *idx;       // selection lists [B][NS], or nullptr for a dense row range
+    int NS;                   // selection length
+    int64_t pos0;             // causal prefill: item i attends rows [0, pos0 + i]; -1 = not causal
+    float sm_scale_log2;      // sm_scale * log2(e)
+    int P;                    // partitions per batch item
+    float *ws;                // partial sets (PartialView layout), or nullptr when `out` is written directly
+    float *out;               // [B][H][512] normalised output (used when ws == nullptr; requires P == 1)
+    int *err_word;            // optional device error word
+};
+
+cudaError_t launch_quant_rows(const float *x, int64_t n, uint8_t *q, float *scale, cudaStream_t st);
+cudaError_t launch_encode(const float *y, int64_t n, uint8_t *out, cudaStream_t st);
+cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t st);
+cudaError_t launch_lse_merge(const float *ws, int B, int P, int H, float *out, cudaStream_t st);
+
+// Partition policy shared by the workspace queries and the launchers.
+int decode_partitions(int H, int64_t T, int P_req);
+int select_partitions(int B, int H, int NS);
+
+}  // namespace kv8

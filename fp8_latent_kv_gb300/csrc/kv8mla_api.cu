@@ -1,0 +1,207 @@
+// kv8mla_api.cu -- the C ABI (include/kv8mla.h): host-side validation and launches.
+//
+// Every entry point validates its scalars and pointers before enqueuing anything, returns a
+// KV8_E* code instead of falling back, allocates nothing and never synchronises (page "B1 Mixed
+// FP8/BF16 FMHA first pass", "Intentional first-pass limits": unsupported shapes are a hard error).
+#include "internal.h"
+
+#include <math.h>
+
+namespace kv8 {
+namespace {
+
+inline bool aligned(const void *p, uintptr_t a) { return p && (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline int status(cudaError_t e) { return e == cudaSuccess ? KV8_OK : KV8_ECUDA; }
+
+inline bool valid_q(const void *q_lat, const void *q_rope, int q_dtype) {
+    return aligned(q_lat, 16) && aligned(q_rope, 16) && (q_dtype == KV8_F32 || q_dtype == KV8_BF16);
+}
+
+inline bool valid_cache(const uint8_t *kv8, const float *kv_scale, int64_t T) {
+    return aligned(kv8, 16) && aligned(kv_scale, 4) && T >= 1 && T <= KV8_MAX_ROWS;
+}
+
+}  // namespace
+
+int decode_partitions(int H, int64_t T, int P_req) {
+    (void)H;
+    if (T < 1) return 1;
+    if (P_req > 0) {
+        int64_t p = P_req < T ? P_req : T;
+        return (int)(p > 65535 ? 65535 : p);
+    }
+    // automatic: about one partition per pair of SMs, at least 128 rows each
+    int64_t p = (T + 127) / 128;
+    return (int)(p < 76 ? p : 76);
+}
+
+int select_partitions(int B, int H, int NS) {
+    (void)B;
+    (void)H;
+    int p = (NS + 127) / 128;
+    return p < 1 ? 1 : (p > 16 ? 16 : p);
+}
+
+}  // namespace kv8
+
+using namespace kv8;
+
+extern "C" {
+
+const char *kv8_strerror(int code) {
+    switch (code) {
+        case KV8_OK: return "ok";
+        case KV8_EINVAL: return "invalid argument (null pointer, size, alignment or limit)";
+        case KV8_EWORKSPACE: return "workspace too small";
+        case KV8_ECUDA: return "CUDA launch failed";
+        case KV8_EUNSUPPORTED: return "unsupported device or shape";
+        default: return "unknown kv8 error code";
+    }
+}
+
+int kv8_encode_e4m3(const float *y, int64_t n, uint8_t *out, void *stream) {
+    if (n < 0) return KV8_EINVAL;
+    if (n == 0) return KV8_OK;
+    if (!aligned(y, 16) || !aligned(out, 4)) return KV8_EINVAL;
+    return status(launch_encode(y, n, out, (cudaStream_t)stream));
+}
+
+int kv8_quant_rows(const float *x, int64_t n, uint8_t *kv8, float *kv_scale, void *stream) {
+    if (n < 0) return KV8_EINVAL;
+    if (n == 0) return KV8_OK;
+    if (!aligned(x, 16) || !aligned(kv8, 16) || !aligned(kv_scale, 4)) return KV8_EINVAL;
+    return status(launch_quant_rows(x, n, kv8, kv_scale, (cudaStream_t)stream));
+}
+
+int mla_decode8_partitions(int H, int64_t T, int P_req, int *P_out) {
+    if (!P_out || H < 1 || H > KV8_MAX_HEADS || T < 1 || T > KV8_MAX_ROWS || P_req < 0) return KV8_EINVAL;
+    *P_out = decode_partitions(H, T, P_req);
+    return KV8_OK;
+}
+
+int mla_decode8_workspace_bytes(int H, int64_t T, int P_req, size_t *bytes) {
+    int P = 0;
+    int rc = mla_decode8_partitions(H, T, P_req, &P);
+    if (rc != KV8_OK || !bytes) return rc != KV8_OK ? rc : KV8_EINVAL;
+    *bytes = PartialView::floats(1, P, H) * sizeof(float);
+    return KV8_OK;
+}
+
+int mla_decode8_partial(const void *q_lat, const void *q_rope, int q_dtype, int H, const uint8_t *kv8,
+                        const float *kv_scale, int64_t T, float sm_scale, int P_req, void *workspace,
+                        size_t ws_bytes, int *err_word, void *stream) {
+    size_t need = 0;
+    int rc = mla_decode8_workspace_bytes(H, T, P_req, &need);
+    if (rc != KV8_OK) return rc;
+    if (!valid_q(q_lat, q_rope, q_dtype) || !valid_cache(kv8, kv_scale, T) || !isfinite(sm_scale) ||
+        !aligned(workspace, 16))
+        return KV8_EINVAL;
+    if (ws_bytes < need) return KV8_EWORKSPACE;
+    AttnArgs a{};
+    a.q_lat = q_lat;
+    a.q_rope = q_rope;
+    a.q_bf16 = q_dtype == KV8_BF16;
+    a.B = 1;
+    a.H = H;
+    a.kv8 = kv8;
+    a.kv_scale = kv_scale;
+    a.T = T;
+    a.seq_stride_rows = 0;
+    a.idx = nullptr;
+    a.NS = 0;
+    a.pos0 = -1;
+    a.sm_scale_log2 = sm_scale * kLog2e;
+    a.P = decode_partitions(H, T, P_req);
+    a.ws = static_cast<float *>(workspace);
+    a.out = nullptr;
+    a.err_word = err_word;
+    return status(launch_attn_simt(a, (cudaStream_t)stream));
+}
+
+int mla_lse_merge8(const void *workspace, int B, int P, int H, float *out, void *stream) {
+    if (!aligned(workspace, 16) || !aligned(out, 16) || B < 1 || B > 65535 || P < 1 || P > 65535 || H < 1 ||
+        H > KV8_MAX_HEADS)
+        return KV8_EINVAL;
+    return status(launch_lse_merge(static_cast<const float *>(workspace), B, P, H, out, (cudaStream_t)stream));
+}
+
+int mla_absorb_decode8(const void *q_lat, const void *q_rope, int q_dtype, int H, const uint8_t *kv8,
+                       const float *kv_scale, int64_t T, float sm_scale, int P_req, void *workspace,
+                       size_t ws_bytes, int *err_word, float *out, void *stream) {
+    if (!aligned(out, 16)) return KV8_EINVAL;
+    int rc = mla_decode8_partial(q_lat, q_rope, q_dtype, H, kv8, kv_scale, T, sm_scale, P_req, workspace, ws_bytes,
+                                 err_word, stream);
+    if (rc != KV8_OK) return rc;
+    return mla_lse_merge8(workspace, 1, decode_partitions(H, T, P_req), H, out, stream);
+}
+
+int mla_sel8_workspace_bytes(int B, int H, int NS, size_t *bytes) {
+    if (!bytes || B < 1 || B > 65535 || H < 1 || H > KV8_MAX_HEADS || NS < 1 || NS > KV8_MAX_SELECT)
+        return KV8_EINVAL;
+    *bytes = PartialView::floats(B, select_partitions(B, H, NS), H) * sizeof(float);
+    return KV8_OK;
+}
+
+int mla_absorb_sel8(const void *q_lat, const void *q_rope, int q_dtype, int B, int H, const uint8_t *kv8,
+                    const float *kv_scale, int64_t T, int64_t seq_stride_rows, const int32_t *idx, int NS,
+                    float sm_scale, void *workspace, size_t ws_bytes, int *err_word, float *out, void *stream) {
+    size_t need = 0;
+    int rc = mla_sel8_workspace_bytes(B, H, NS, &need);
+    if (rc != KV8_OK) return rc;
+    if (!valid_q(q_lat, q_rope, q_dtype) || !valid_cache(kv8, kv_scale, T) || !aligned(idx, 4) ||
+        !isfinite(sm_scale) || !aligned(workspace, 16) || !aligned(out, 16) || seq_stride_rows < 0 ||
+        (B > 1 && seq_stride_rows < T))
+        return KV8_EINVAL;
+    if (ws_bytes < need) return KV8_EWORKSPACE;
+    AttnArgs a{};
+    a.q_lat = q_lat;
+    a.q_rope = q_rope;
+    a.q_bf16 = q_dtype == KV8_BF16;
+    a.B = B;
+    a.H = H;
+    a.kv8 = kv8;
+    a.kv_scale = kv_scale;
+    a.T = T;
+    a.seq_stride_rows = B > 1 ? seq_stride_rows : 0;
+    a.idx = idx;
+    a.NS = NS;
+    a.pos0 = -1;
+    a.sm_scale_log2 = sm_scale * kLog2e;
+    a.P = select_partitions(B, H, NS);
+    a.ws = static_cast<float *>(workspace);
+    a.out = nullptr;
+    a.err_word = err_word;
+    rc = status(launch_attn_simt(a, (cudaStream_t)stream));
+    if (rc != KV8_OK) return rc;
+    return mla_lse_merge8(workspace, B, a.P, H, out, stream);
+}
+
+int mla_absorb_prefill8(const void *q_lat, const void *q_rope, int q_dtype, int S, int H, int64_t pos0,
+                        const uint8_t *kv8, const float *kv_scale, int64_t T, float sm_scale, int *err_word,
+                        float *out, void *stream) {
+    if (!valid_q(q_lat, q_rope, q_dtype) || !valid_cache(kv8, kv_scale, T) || !aligned(out, 16) ||
+        !isfinite(sm_scale) || S < 1 || S > 65535 || H < 1 || H > KV8_MAX_HEADS || pos0 < 0 || pos0 + S > T)
+        return KV8_EINVAL;
+    AttnArgs a{};
+    a.q_lat = q_lat;
+    a.q_rope = q_rope;
+    a.q_bf16 = q_dtype == KV8_BF16;
+    a.B = S;
+    a.H = H;
+    a.kv8 = kv8;
+    a.kv_scale = kv_scale;
+    a.T = T;
+    a.seq_stride_rows = 0;
+    a.idx = nullptr;
+    a.NS = 0;
+    a.pos0 = pos0;
+    a.sm_scale_log2 = sm_scale * kLog2e;
+    a.P = 1;
+    a.ws = nullptr;
+    a.out = out;
+    a.err_word = err_word;
+    return status(launch_attn_simt(a, (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,170 @@
+/*
+ * kv8mla.h -- C ABI of the fp8 latent-KV absorbed MLA attention library (libkv8mla.so, sm_103a).
+ *
+ * The operations follow two web pages:
+ *   [KV8]  "KV8 long-context CUDA: fp8 device shadow, split-T kernels, DSA-aware gather"
+ *          (colibri pull request #300): first commit message (fp8 row format, c/kv_fp8.h codec,
+ *          absorb attention, CUDA wrappers coli_cuda_attention_absorb8 / _absorb_batch8) and second
+ *          commit message (device-resident shadow, split-T partial blocks + log-sum-exp merge,
+ *          DSA gather attention_absorb_sel_kernel8 with NS <= 4096, batch cap lifted to 1M rows).
+ *   [B1]   "B1 Mixed FP8/BF16 FMHA first pass", sections "New files" (C ABI launcher driven from
+ *          Python through ctypes) and "Intentional first-pass limits" (unsupported shapes are a
+ *          hard error, not a fallback).
+ *
+ * Cache layout (one layer).  Row t of the latent cache is KV8_ROW_BYTES = 576 e4m3 bytes:
+ * bytes 0..511 are Lc (kv_lora latent), bytes 512..575 are Rc (qk_rope key), followed in a separate
+ * array by one f32 scale s_t = amax_t / 448 covering the whole row.  kv8 is [T][576] u8 row-major,
+ * kv_scale is [T] f32.  The attended value of row t, head h:
+ *     score[h,t] = sm_scale * s_t * ( q_lat[h].e4m3(Lc8_t) + q_rope[h].e4m3(Rc8_t) )
+ *     cl[h]      = sum_t softmax_t(score[h,:]) * s_t * e4m3(Lc8_t)            (512 f32 per head)
+ * ("the latent is both key and value"; the row scale is hoisted out of the dot: [KV8] first commit.)
+ *
+ * Conventions for every call:
+ *   - Pointers are DEVICE pointers owned by the caller (unless stated).  The library allocates no
+ *     memory, keeps no state between calls, never synchronises the device, and has no CPU
+ *     fallback: an unsupported argument is an error code.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are asynchronous:
+ *     a return of KV8_OK means the kernels were enqueued; results are valid once the stream has
+ *     reached that point.
+ *   - Validation happens on the host before any launch: on any error nothing is enqueued.
+ *   - Device buffers must be 16-byte aligned (TMA and vector loads).  Inputs and outputs must not
+ *     overlap, except where stated.
+ *   - Return values: KV8_OK (0) or a negative KV8_E* code.  kv8_strerror() names it.
+ *   - Device-side conditions (a selected index out of range, a wait that timed out) are OR-ed
+ *     into *err_word (a device int, optional: may be NULL) as KV8_ERR_* bits; the caller clears it
+ *     beforehand and reads it after synchronising.
+ */
+#ifndef KV8MLA_H
+#define KV8MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define KV8_API __attribute__((visibility("default")))
+#else
+#define KV8_API
+#endif
+
+#define KV8_ROW_BYTES 576      /* e4m3 bytes per cache row: Lc then Rc */
+#define KV8_KL 512             /* kv_lora rank: latent width, also the context width */
+#define KV8_KR 64              /* qk_rope width */
+#define KV8_MAX_HEADS 128      /* query heads per call */
+#define KV8_MAX_ROWS (1 << 20) /* rows per cache: the 1M cap of [KV8] second commit */
+#define KV8_MAX_SELECT 4096    /* selected rows per sequence: NS <= 4096 ([KV8] second commit) */
+
+/* return codes */
+#define KV8_OK 0
+#define KV8_EINVAL (-1)       /* null pointer, bad size, misalignment, or value outside the limits */
+#define KV8_EWORKSPACE (-2)   /* workspace smaller than the matching *_workspace_bytes() */
+#define KV8_ECUDA (-3)        /* a CUDA launch or attribute call failed */
+#define KV8_EUNSUPPORTED (-4) /* the device is not sm_103 (or the shape has no kernel) */
+
+/* bits OR-ed into *err_word by the device */
+#define KV8_ERR_INDEX 1u    /* a selected row index was outside [0, T): that entry was skipped */
+#define KV8_ERR_TIMEOUT 2u  /* a bounded wait in a kernel gave up: that output is not valid */
+
+/* query element types */
+#define KV8_F32 0
+#define KV8_BF16 1
+
+/* -----------------------------------------------------------------------------------------------
+ * kv8_encode_e4m3 -- the element encoder of the row quantizer, without scaling.
+ * [KV8] first commit, c/kv_fp8.h item: round to nearest, ties to even; saturate at +-448 (inf
+ * included); keep the sign of zero (so -0.0 and negative values that round to zero give 0x80);
+ * store NaN as 0x00.
+ *   y   [n] f32 in, out [n] u8 out (byte i encodes y[i]).  n >= 0 (n == 0 enqueues nothing).
+ *   Alignment: y 16-byte aligned, out 4-byte aligned.
+ * --------------------------------------------------------------------------------------------- */
+KV8_API int kv8_encode_e4m3(const float *y, int64_t n, uint8_t *out, void *stream);
+
+/* -----------------------------------------------------------------------------------------------
+ * kv8_quant_rows -- quantize n f32 rows into cache rows ([KV8] first commit: the producer
+ * quantizes the fresh normed/roped row; per-row quantizer with a subnormal-amax guard).
+ *   x        [n][576] f32 in (Lc then Rc for each row)
+ *   kv8      [n][576] u8 out: pass the cache base + 576*t to write rows t..t+n-1
+ *   kv_scale [n] f32 out:     pass the scale base + t
+ * Per row, in f32 with IEEE round-to-nearest: amax = max |x_i| over finite x_i; scale = amax/448;
+ * y_i = x_i * (448/amax), or, when 448/amax overflows (subnormal amax), (x_i*2^64)*(448/(amax*2^64));
+ * when amax == 0, y_i = x_i.  byte_i = kv8_encode_e4m3(y_i).  Bit-exact with the oracle.
+ *   n >= 0.  x and kv8 16-byte aligned, kv_scale 4-byte aligned.
+ * --------------------------------------------------------------------------------------------- */
+KV8_API int kv8_quant_rows(const float *x, int64_t n, uint8_t *kv8, float *kv_scale, void *stream);
+
+/* -----------------------------------------------------------------------------------------------
+ * Split-T decode ([KV8] second commit: flash-decoding style partial online-softmax blocks
+ * (cl[K], m, z) plus a log-sum-exp merge kernel; the cache is device-resident, only new rows are
+ * uploaded).  One query of H heads over rows 0..T-1.
+ *
+ * Partition p of P covers rows [floor(T*p/P), floor(T*(p+1)/P)).  Workspace layout (f32), for
+ * B batch items (B = 1 for decode):
+ *     cl [B][P][H][512]   unnormalised context of each partition, relative to its own max
+ *     m  [B][P][H]        partition max of score * log2(e)  (-inf for an empty partition)
+ *     z  [B][P][H]        sum over the partition of 2^(score*log2(e) - m)
+ * mla_decode8_partitions:      the partition count P the library uses for (H, T, P_req):
+ *                              P_req = 0 picks automatically, P_req > 0 is clamped to [1, T].
+ * mla_decode8_workspace_bytes: workspace bytes for (H, T, P_req).
+ * --------------------------------------------------------------------------------------------- */
+KV8_API int mla_decode8_partitions(int H, int64_t T, int P_req, int *P_out);
+KV8_API int mla_decode8_workspace_bytes(int H, int64_t T, int P_req, size_t *bytes);
+
+/* mla_decode8_partial -- the partial kernel alone (fills the workspace for P partitions).
+ *   q_lat [H][512], q_rope [H][64] of type q_dtype (KV8_F32 or KV8_BF16), 16-byte aligned.
+ *   H in [1, 128]; T in [1, KV8_MAX_ROWS]; kv8 [T][576], kv_scale [T].
+ *   sm_scale: finite.  err_word: optional (KV8_ERR_TIMEOUT).
+ *   workspace: >= mla_decode8_workspace_bytes(H, T, P_req) bytes. */
+KV8_API int mla_decode8_partial(const void *q_lat, const void *q_rope, int q_dtype, int H, const uint8_t *kv8,
+                        const float *kv_scale, int64_t T, float sm_scale, int P_req, void *workspace,
+                        size_t ws_bytes, int *err_word, void *stream);
+
+/* mla_lse_merge8 -- the log-sum-exp merge of B*H partial sets into out [B][H][512] f32:
+ *   M = max_p m_p;  w_p = 2^(m_p - M) (0 when m_p = -inf);  Z = sum_p w_p z_p;
+ *   out = sum_p w_p cl_p / Z   (0 when Z == 0, i.e. no row was attended).
+ * workspace as written by the partial kernels; P in [1, 65535]. */
+KV8_API int mla_lse_merge8(const void *workspace, int B, int P, int H, float *out, void *stream);
+
+/* mla_absorb_decode8 -- partial + merge on one stream: out [H][512] f32 = cl for each head. */
+KV8_API int mla_absorb_decode8(const void *q_lat, const void *q_rope, int q_dtype, int H, const uint8_t *kv8,
+                       const float *kv_scale, int64_t T, float sm_scale, int P_req, void *workspace,
+                       size_t ws_bytes, int *err_word, float *out, void *stream);
+
+/* -----------------------------------------------------------------------------------------------
+ * mla_absorb_sel8 -- DSA gather decode ([KV8] second commit: attention_absorb_sel_kernel8 attends
+ * the selected rows straight from the device cache by absolute index, NS <= 4096; when a
+ * selection is active decode attends exactly the selection).
+ *   B sequences; sequence b's cache is rows [b*seq_stride_rows, b*seq_stride_rows + T) of
+ *   kv8 / kv_scale (seq_stride_rows >= T, or 0 when B == 1).
+ *   q_lat [B][H][512], q_rope [B][H][64] (q_dtype); idx [B][NS] int32 absolute row indices into
+ *   the sequence's own cache (any order; duplicates attend twice).  An index outside [0, T) is
+ *   skipped and sets KV8_ERR_INDEX in *err_word.  out [B][H][512] f32.
+ *   NS in [1, KV8_MAX_SELECT]; T in [1, KV8_MAX_ROWS]; H in [1, 128]; B >= 1.
+ *   workspace >= mla_sel8_workspace_bytes(B, H, NS).
+ * --------------------------------------------------------------------------------------------- */
+KV8_API int mla_sel8_workspace_bytes(int B, int H, int NS, size_t *bytes);
+KV8_API int mla_absorb_sel8(const void *q_lat, const void *q_rope, int q_dtype, int B, int H, const uint8_t *kv8,
+                    const float *kv_scale, int64_t T, int64_t seq_stride_rows, const int32_t *idx, int NS,
+                    float sm_scale, void *workspace, size_t ws_bytes, int *err_word, float *out, void *stream);
+
+/* -----------------------------------------------------------------------------------------------
+ * mla_absorb_prefill8 -- causal prefill of S new queries ([KV8] first and second commits: the
+ * batch/prefill absorb path, coli_cuda_attention_absorb_batch8, tiled streaming, cap 1M rows).
+ * Query i sits at position pos0 + i and attends rows 0..pos0+i (row index = position); its own
+ * fresh row must already be quantized into the cache (kv8_quant_rows).
+ *   q_lat [S][H][512], q_rope [S][H][64] (q_dtype); out [S][H][512] f32.
+ *   S >= 1; pos0 >= 0; pos0 + S <= T <= KV8_MAX_ROWS; H in [1, 128].
+ * --------------------------------------------------------------------------------------------- */
+KV8_API int mla_absorb_prefill8(const void *q_lat, const void *q_rope, int q_dtype, int S, int H, int64_t pos0,
+                        const uint8_t *kv8, const float *kv_scale, int64_t T, float sm_scale, int *err_word,
+                        float *out, void *stream);
+
+/* Name of a return code (static string). */
+KV8_API const char *kv8_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KV8MLA_H */
