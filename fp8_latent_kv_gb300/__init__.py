@@ -32,6 +32,7 @@ SIGNATURES = {
     "mla_sel8_workspace_bytes": (_I, [_I, _I, _I, _P]),
     "mla_absorb_sel8": (_I, [_P, _P, _I, _I, _I, _P, _P, _I64, _I64, _P, _I, _F, _P, _SZ, _P, _P, _P]),
     "mla_absorb_prefill8": (_I, [_P, _P, _I, _I, _I, _I64, _P, _P, _I64, _F, _P, _P, _P]),
+    "mla_absorb_decode8_noalloc": (_I, [_P, _P, _I, _I, _P, _P, _I64, _F, _I, _P, _P, _P]),
     "kv8_strerror": (ctypes.c_char_p, [_I]),
 }
 
@@ -156,6 +157,15 @@ def mla_absorb_prefill8(q_lat, q_rope, pos0: int, kv8, kv_scale, T: int, sm_scal
     S, H = q_lat.shape[0], q_lat.shape[1]
     _check("mla_absorb_prefill8", load().mla_absorb_prefill8(
         _ptr(q_lat), _ptr(q_rope), _qdtype(q_lat), S, H, pos0, _ptr(kv8), _ptr(kv_scale), T, sm_scale,
+        _ptr(err_word), _ptr(out), _stream(stream)))
+
+
+def mla_absorb_decode8_noalloc(q_lat, q_rope, kv8, kv_scale, T: int, sm_scale: float, out, P_req: int = 0,
+                               err_word=None, stream=None) -> None:
+    """Decode without a workspace argument: the partials live in the library's fixed device array."""
+    H = q_lat.shape[-2]
+    _check("mla_absorb_decode8_noalloc", load().mla_absorb_decode8_noalloc(
+        _ptr(q_lat), _ptr(q_rope), _qdtype(q_lat), H, _ptr(kv8), _ptr(kv_scale), T, sm_scale, P_req,
         _ptr(err_word), _ptr(out), _stream(stream)))
 
 

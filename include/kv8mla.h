@@ -161,6 +161,32 @@ KV8_API int mla_absorb_prefill8(const void *q_lat, const void *q_rope, int q_dty
                         const uint8_t *kv8, const float *kv_scale, int64_t T, float sm_scale, int *err_word,
                         float *out, void *stream);
 
+/* -----------------------------------------------------------------------------------------------
+ * mla_absorb_decode8_noalloc -- mla_absorb_decode8 for callers that cannot allocate device memory.
+ * The pages have no counterpart to this call; it exists for users of this library.
+ *
+ * Some callers cannot call cudaMalloc or reach an allocator for the workspace that the split-T
+ * partials need: a plugin loaded into a host program whose memory pool already owns the GPU's
+ * memory, a caller from another language runtime with no handle on the host's caching allocator,
+ * or a latency-critical loop that must not take cudaMalloc's implicit device synchronisation.
+ * This entry point keeps the partials in a fixed array of KV8_NOALLOC_SCRATCH_BYTES that is part of
+ * the library's device image: every GPU that loads the library holds it until the process exits.
+ * Neither this call nor anything it calls allocates memory.
+ *
+ * Arguments as mla_absorb_decode8, without workspace / ws_bytes.  P_req == 0 picks the automatic
+ * partition count, lowered if needed until the partials fit the array; an explicit P_req whose
+ * partials do not fit returns KV8_EWORKSPACE (nothing is enqueued).
+ * The first call on each device (with that device current) looks up the array's device address;
+ * make that first call before any stream capture.  All calls share the one array and it keeps the
+ * last call's contents (each call writes every partial it reads, so nothing needs clearing):
+ * calls whose kernels overlap on the GPU (two streams, or two host threads) race on it and must be
+ * ordered by the caller.
+ * --------------------------------------------------------------------------------------------- */
+#define KV8_NOALLOC_SCRATCH_BYTES (16u << 20) /* 16 MiB per device */
+KV8_API int mla_absorb_decode8_noalloc(const void *q_lat, const void *q_rope, int q_dtype, int H,
+                                       const uint8_t *kv8, const float *kv_scale, int64_t T, float sm_scale,
+                                       int P_req, int *err_word, float *out, void *stream);
+
 /* Name of a return code (static string). */
 KV8_API const char *kv8_strerror(int code);
 
