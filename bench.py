@@ -373,7 +373,7 @@ def run_ours(args, rank, world, local_rank):
     roof["hbm_gbs"] = hbm_gbs
     roof["hbm_frac"] = hbm_gbs / peaks["hbm_gbs"]
 
-    base = cpu_baseline(rows, w) if world == 1 else None
+    base = cpu_baseline(rows, w) if (world == 1 and not args.no_cpu_baseline) else None
     value = whole_job_us_per_step(ms_per_step, world)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -403,6 +403,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     args = ap.parse_args(argv)
     rank, world, local_rank = dist_env()
     if world > 1:
