@@ -29,6 +29,8 @@ struct AttnArgs {
 cudaError_t launch_quant_rows(const float *x, int64_t n, uint8_t *q, float *scale, cudaStream_t st);
 cudaError_t launch_encode(const float *y, int64_t n, uint8_t *out, cudaStream_t st);
 cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t st);
+// tcgen05 kernel for bf16 queries over a dense (optionally causal) row range; a.idx must be null.
+cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st);
 cudaError_t launch_lse_merge(const float *ws, int B, int P, int H, float *out, cudaStream_t st);
 
 // Partition policy shared by the workspace queries and the launchers.

@@ -116,7 +116,8 @@ int mla_decode8_partial(const void *q_lat, const void *q_rope, int q_dtype, int 
     a.ws = static_cast<float *>(workspace);
     a.out = nullptr;
     a.err_word = err_word;
-    return status(launch_attn_simt(a, (cudaStream_t)stream));
+    // bf16 queries: tensor cores; f32 queries keep full f32 precision on the CUDA cores
+    return status(a.q_bf16 ? launch_attn_tc(a, (cudaStream_t)stream) : launch_attn_simt(a, (cudaStream_t)stream));
 }
 
 int mla_lse_merge8(const void *workspace, int B, int P, int H, float *out, void *stream) {
@@ -201,7 +202,7 @@ int mla_absorb_prefill8(const void *q_lat, const void *q_rope, int q_dtype, int 
     a.ws = nullptr;
     a.out = out;
     a.err_word = err_word;
-    return status(launch_attn_simt(a, (cudaStream_t)stream));
+    return status(a.q_bf16 ? launch_attn_tc(a, (cudaStream_t)stream) : launch_attn_simt(a, (cudaStream_t)stream));
 }
 
 }  // extern "C"
