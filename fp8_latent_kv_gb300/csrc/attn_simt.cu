@@ -218,32 +218,66 @@ __global__ void __launch_bounds__(kThreads, 1) attn_simt_kernel(AttnArgs a) {
     }
 }
 
-// Log-sum-exp merge: block (h, b), 128 threads x 4 latent columns.
+// Log-sum-exp merge: block (h, quarter, b) -- 128 threads, one latent column each.  Warp 0 turns
+// the P partition maxima into weights 2^(m_p - M) in shared memory; then every thread sums its column
+// over the partitions with independent loads in flight.
+constexpr int kMergeMaxP = 1024;  // weights kept in shared memory; larger P loops over slices
+
 __global__ void __launch_bounds__(128) lse_merge_kernel(const float *__restrict__ ws, int B, int P, int H,
                                                         float *__restrict__ out) {
-    const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+    __shared__ float wsh[kMergeMaxP];
+    __shared__ float zsh;
+    // launched as a programmatic dependent of the partial kernel: wait until its partials are written
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int h = blockIdx.x, quarter = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
     PartialView pv(const_cast<float *>(ws), B, P, H);
     const int64_t base = (int64_t)b * P * H + h;
+    // global max over partitions (every thread; P is small and the values are L2-resident)
     float M = -INFINITY;
-    for (int p = 0; p < P; ++p) M = fmaxf(M, pv.m[base + (int64_t)p * H]);
-    float Z = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -INFINITY) {
-        for (int p = 0; p < P; ++p) {
+    if (tid < 32) {
+        for (int p = tid; p < P; p += 32) M = fmaxf(M, pv.m[base + (int64_t)p * H]);
+        M = warp_max(M);
+        float Z = 0.f;
+        for (int p = tid; p < P; p += 32) {
             const float mp = pv.m[base + (int64_t)p * H];
-            if (mp == -INFINITY) continue;
-            const float w = exp2f(mp - M);
+            const float w = (mp == -INFINITY || M == -INFINITY) ? 0.f : exp2f(mp - M);
+            if (p < kMergeMaxP) wsh[p] = w;
             Z = fmaf(w, pv.z[base + (int64_t)p * H], Z);
-            const float4 c = reinterpret_cast<const float4 *>(pv.cl + (base + (int64_t)p * H) * kKL)[tid];
-            acc.x = fmaf(w, c.x, acc.x);
-            acc.y = fmaf(w, c.y, acc.y);
-            acc.z = fmaf(w, c.z, acc.z);
-            acc.w = fmaf(w, c.w, acc.w);
+        }
+        Z = warp_sum(Z);
+        if (tid == 0) zsh = Z;
+    }
+    __syncthreads();
+    const int d = quarter * 128 + tid;
+    const float *cl = pv.cl + base * kKL + d;
+    const int64_t pstride = (int64_t)H * kKL;
+    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+    const int pw = P < kMergeMaxP ? P : kMergeMaxP;
+    int p = 0;
+    for (; p + 4 <= pw; p += 4) {
+        const float c0 = cl[(int64_t)(p + 0) * pstride], c1 = cl[(int64_t)(p + 1) * pstride];
+        const float c2 = cl[(int64_t)(p + 2) * pstride], c3 = cl[(int64_t)(p + 3) * pstride];
+        // a partition with weight 0 may hold anything (it attended no row): do not touch its values
+        if (wsh[p + 0] != 0.f) acc0 = fmaf(wsh[p + 0], c0, acc0);
+        if (wsh[p + 1] != 0.f) acc1 = fmaf(wsh[p + 1], c1, acc1);
+        if (wsh[p + 2] != 0.f) acc2 = fmaf(wsh[p + 2], c2, acc2);
+        if (wsh[p + 3] != 0.f) acc3 = fmaf(wsh[p + 3], c3, acc3);
+    }
+    for (; p < pw; ++p)
+        if (wsh[p] != 0.f) acc0 = fmaf(wsh[p], cl[(int64_t)p * pstride], acc0);
+    // partitions beyond the shared-memory slice (P > kMergeMaxP): weights recomputed on the fly
+    if (P > kMergeMaxP) {
+        float Mx = -INFINITY;
+        for (int q = 0; q < P; ++q) Mx = fmaxf(Mx, pv.m[base + (int64_t)q * H]);
+        for (int q = kMergeMaxP; q < P; ++q) {
+            const float mp = pv.m[base + (int64_t)q * H];
+            if (mp == -INFINITY) continue;
+            acc1 = fmaf(exp2f(mp - Mx), cl[(int64_t)q * pstride], acc1);
         }
     }
+    const float Z = zsh;
     const float inv = Z > 0.f ? 1.f / Z : 0.f;
-    reinterpret_cast<float4 *>(out + ((int64_t)b * H + h) * kKL)[tid] =
-        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    out[((int64_t)b * H + h) * kKL + d] = ((acc0 + acc1) + (acc2 + acc3)) * inv;
 }
 
 }  // namespace
@@ -258,8 +292,17 @@ cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t st) {
 }
 
 cudaError_t launch_lse_merge(const float *ws, int B, int P, int H, float *out, cudaStream_t st) {
-    dim3 grid((unsigned)H, (unsigned)B);
-    lse_merge_kernel<<<grid, 128, 0, st>>>(ws, B, P, H, out);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)H, 4u, (unsigned)B);
+    cfg.blockDim = dim3(128);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, lse_merge_kernel, ws, B, P, H, out);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

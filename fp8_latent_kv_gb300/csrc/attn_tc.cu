@@ -53,21 +53,29 @@ constexpr float kTau = 2.0f;           // lazy-rescale threshold (log2 units): p
 constexpr float kWScale = 64.0f;       // 2^(8 - kTau): keeps w <= 256 < 448 (e4m3 max)
 
 struct Misc {
-    // per-head arrays first: m_run is read with 16-byte vector loads
-    alignas(16) float m_run[kHeadsPerCta];
-    alignas(16) float red[4][kHeadsPerCta];
-    alignas(16) float alpha[kHeadsPerCta];
-    alignas(16) float zsum[kHeadsPerCta];
-    alignas(16) float wred[2][16];
-    uint64_t kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, pv_done, sync_bar, final_bar;
+    // per-head arrays first: they are read with 16-byte vector loads
+    alignas(16) float m_run[2][kHeadsPerCta];  // running max per head; which copy is current flips on a rescale
+    alignas(16) float c_head[kHeadsPerCta];    // sm_scale * log2(e) * 2^-e_h per head (0 for padding heads)
+    alignas(16) float red[4][kHeadsPerCta];    // per-quadrant tile maxima / row sums
+    union alignas(16) Phase {                  // storage that is never live in two phases at once
+        struct {
+            int qmax_bits[kHeadsPerCta];       // prologue: per-head max |q| (bits of a non-negative float)
+            float wred[2][16];                 // prologue: per-warp maxima
+        } pro;
+        float alpha[8][32];                    // tile loop: per softmax warp, rescale factors of its heads
+        float zsum[kHeadsPerCta];              // epilogue: row sums per head
+    } ph;
+    uint64_t kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, pv_done, sync_bar, final_bar, q_full;
+    uint64_t kv_blk[2][4];  // latent block kb of a stage has been read by the context product
     uint32_t tmem_base;
     int abort_flag;
     int vote[2];
-    float c_score;   // sm_scale * log2(e) * 2^-e
     float w_mul;     // kWScale / s_ref
     float out_mul;   // s_ref / kWScale
 };
-static_assert(OFF_MISC % 16 == 0 && offsetof(Misc, m_run) % 16 == 0, "vector loads of m_run need 16-byte alignment");
+static_assert(OFF_MISC % 16 == 0 && offsetof(Misc, m_run) % 16 == 0 && offsetof(Misc, red) % 16 == 0 &&
+                  offsetof(Misc, ph) % 16 == 0 && offsetof(Misc, c_head) % 16 == 0,
+              "vector accesses need 16-byte alignment");
 static_assert(offsetof(Misc, kv_full) % 8 == 0, "mbarriers need 8-byte alignment");
 constexpr uint32_t kSmemBytes = OFF_MISC + sizeof(Misc);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -83,7 +91,15 @@ struct TcArgs {
     float *ws;                   // partial sets, or nullptr
     float *out;                  // direct normalised output when ws == nullptr
     int *err_word;
+    // written by tc_prep_kernel (decode): query images [n_half][kImg], per-head factors [n_half*64],
+    // per-partition row-scale maxima [P].  Null: the kernel prepares its own queries (prefill).
+    const uint8_t *qimg;
+    const float *c_head;
+    const float *smax;
 };
+
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ void named_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -107,6 +123,20 @@ __device__ __forceinline__ void split_pair(float a, float b, uint32_t &hi, uint3
     hi = enc_pair(a, b);
     const float2 h = dec_pair(hi);
     lo = enc_pair(a - h.x, b - h.y);
+}
+
+// The same split through f16x2 (5 instructions per pair): w is first rounded to f16 (11 bits, finer
+// than the 8 bits hi + lo keep), then hi = e4m3(w), lo = e4m3(w - hi) with the residual exact in f16.
+__device__ __forceinline__ void split_pair_h(float a, float b, uint32_t &hi, uint32_t &lo) {
+    uint32_t w16, h16, r16;
+    uint16_t h8, l8;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(w16) : "f"(b), "f"(a));
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(h8) : "r"(w16));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h16) : "h"(h8));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r16) : "r"(w16), "r"(h16));
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l8) : "r"(r16));
+    hi = h8;
+    lo = l8;
 }
 
 // Bounded barrier among the 256 softmax threads (an mbarrier, so a missing thread cannot hang it).
@@ -144,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < 2; ++s) {
             mbar_init(&ms.kv_full[s], 1);
             mbar_init(&ms.kv_empty[s], 1);
+            for (int kb = 0; kb < 4; ++kb) mbar_init(&ms.kv_blk[s][kb], 1);
             mbar_init(&ms.s_full[s], 1);
             mbar_init(&ms.s_free[s], kSoftmaxThreads);
             ms.vote[s] = 0;
@@ -152,6 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&ms.pv_done, 1);
         mbar_init(&ms.sync_bar, kSoftmaxThreads);
         mbar_init(&ms.final_bar, 1);
+        mbar_init(&ms.q_full, 1);
         ms.abort_flag = 0;
         fence_barrier_init();
     }
@@ -159,6 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(&ms.tmem_base, 512);
         tmem_relinquish();
     }
+    if (tid < kHeadsPerCta) ms.ph.pro.qmax_bits[tid] = 0;
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -170,97 +203,158 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && n_tiles > 0) {
             prefetch_tensormap(&map_lc);
             prefetch_tensormap(&map_rc);
-            int issued = 0;
+            // tiles beyond the two stages are pulled into L2 ahead of their loads
+            auto prefetch = [&](int i) {
+                if (i >= n_tiles) return;
+                const int y = (int)(t0 + (int64_t)i * kTile);
+                for (int kb = 0; kb < 4; ++kb) tma_prefetch_l2_2d(&map_lc, kb * 128, y);
+                tma_prefetch_l2_2d(&map_rc, 512, y);
+            };
+            int issued = 0, armed = 0;
             for (int i = 0; i < n_tiles; ++i) {
                 const int s = i & 1;
-                if (i >= 2 && !mbar_wait(&ms.kv_empty[s], ((i >> 1) - 1) & 1, &ms.abort_flag, a.err_word)) break;
+                if (i == 2 || (i == n_tiles - 1 && i < 2)) {
+                    // the rows do not depend on the query prep; the query image does
+                    if (a.qimg) {
+                        grid_dependency_wait();
+                        mbar_arrive_expect_tx(&ms.q_full, kImg);
+                        const uint8_t *src = a.qimg + (size_t)half * kImg;
+                        for (int kb = 0; kb < 4; ++kb) bulk_load(smem + OFF_Q + kb * 16384, src + kb * 16384, 16384, &ms.q_full);
+                        bulk_load(smem + OFF_Q + kRcOff, src + kRcOff, 8192, &ms.q_full);
+                    }
+                }
                 uint8_t *st = smem + (s ? OFF_ST1 : OFF_ST0);
-                mbar_arrive_expect_tx(&ms.kv_full[s], kImg);
                 const int y = (int)(t0 + (int64_t)i * kTile);
-                for (int kb = 0; kb < 4; ++kb) tma_load_2d(st + kb * 16384, &map_lc, kb * 128, y, &ms.kv_full[s]);
+                const uint32_t ph = ((i >> 1) - 1) & 1;  // phase of tile i-2's release
+                // each latent block is refilled as soon as the context product of tile i-2 has read it;
+                // the rope block also holds tile i-2's weights and is refilled after the whole product.
+                // The stage's full barrier is re-armed only after the first release: that implies tile
+                // i-2's phase of it has completed (one arrival per phase).
+                bool ok_p = true;
+                for (int kb = 0; kb < 4 && ok_p; ++kb) {
+                    if (i >= 2 && !(ok_p = mbar_wait(&ms.kv_blk[s][kb], ph, &ms.abort_flag, a.err_word))) break;
+                    if (kb == 0) {
+                        mbar_arrive_expect_tx(&ms.kv_full[s], kImg);
+                        armed = i + 1;
+                    }
+                    tma_load_2d(st + kb * 16384, &map_lc, kb * 128, y, &ms.kv_full[s]);
+                }
+                if (ok_p && i >= 2) ok_p = mbar_wait(&ms.kv_empty[s], ph, &ms.abort_flag, a.err_word);
+                if (!ok_p) break;
                 tma_load_2d(st + kRcOff, &map_rc, 512, y, &ms.kv_full[s]);
                 issued = i + 1;
+                if (i == 1) {
+                    prefetch(2);
+                    prefetch(3);
+                }
+                if (i >= 1) prefetch(i + 3);
             }
-            // every issued load must land before the CTA ends
-            for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i)
-                mbar_wait(&ms.kv_full[i & 1], (i >> 1) & 1, nullptr, a.err_word, 200000000ull);
+            // every issued load must land before the CTA ends (a partly issued tile times out quickly,
+            // after its issued blocks have landed)
+            for (int i = (armed > 2 ? armed - 2 : 0); i < armed; ++i)
+                mbar_wait(&ms.kv_full[i & 1], (i >> 1) & 1, nullptr, a.err_word, i < issued ? 200000000ull : 20000000ull);
+            if (a.qimg && issued > 0) mbar_wait(&ms.q_full, 0, nullptr, a.err_word, 200000000ull);
         }
         __syncwarp();
     } else {
         // ======================= prologue: query image, row-scale max =======================
         const int pt = tid - 32;  // 0..287
-        float qmax = 0.f, smax = 0.f;
-        for (int it = pt; it < kHeadsPerCta * 36; it += kPrepThreads) {
-            const int h = it / 36, ch = it - h * 36;
-            const int hg = half * kHeadsPerCta + h;
-            if (hg < a.H) {
-                const __nv_bfloat16 *src = ch < 32 ? a.q_lat + ((int64_t)b * a.H + hg) * kKL + ch * 16
-                                                   : a.q_rope + ((int64_t)b * a.H + hg) * kKR + (ch - 32) * 16;
-                const uint4 u0 = *reinterpret_cast<const uint4 *>(src), u1 = *reinterpret_cast<const uint4 *>(src + 8);
-                const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+        float smax = 0.f;
+        if (a.qimg) {
+            // decode: the prep kernel wrote the query image (loaded by the producer) and the factors
+            grid_dependency_wait();
+            if (pt < kHeadsPerCta) ms.c_head[pt] = a.c_head[half * kHeadsPerCta + pt];
+            smax = a.smax[part];
+        } else {
+            // prefill: each CTA prepares its own 64 heads (the image is reused for all its tiles)
+            constexpr int kItems = kHeadsPerCta * 36 / kPrepThreads;  // 8 chunks of 16 query elements
+            static_assert(kHeadsPerCta * 36 == kItems * kPrepThreads, "query chunks split evenly");
+            uint4 qv[kItems][2];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[k]));
-                    qmax = fmaxf(qmax, fmaxf(fabsf(f.x), fabsf(f.y)));
+            for (int k = 0; k < kItems; ++k) {
+                const int it = pt + k * kPrepThreads, h = it / 36, ch = it - h * 36;
+                const int hg = half * kHeadsPerCta + h;
+                qv[k][0] = qv[k][1] = make_uint4(0u, 0u, 0u, 0u);
+                if (hg < a.H) {
+                    const __nv_bfloat16 *src = ch < 32 ? a.q_lat + ((int64_t)b * a.H + hg) * kKL + ch * 16
+                                                       : a.q_rope + ((int64_t)b * a.H + hg) * kKR + (ch - 32) * 16;
+                    qv[k][0] = __ldg(reinterpret_cast<const uint4 *>(src));
+                    qv[k][1] = __ldg(reinterpret_cast<const uint4 *>(src) + 1);
                 }
             }
-        }
-        for (int64_t t = t0 + pt; t < t1; t += kPrepThreads) smax = fmaxf(smax, fabsf(__ldg(a.kv_scale + t)));
-        qmax = warp_max(qmax);
-        smax = warp_max(smax);
-        if (lane == 0) {
-            ms.wred[0][warp - 1] = qmax;
-            ms.wred[1][warp - 1] = smax;
-        }
-        named_sync(1, kPrepThreads);
-        qmax = 0.f;
-        smax = 0.f;
-        for (int k = 0; k < 9; ++k) {
-            qmax = fmaxf(qmax, ms.wred[0][k]);
-            smax = fmaxf(smax, ms.wred[1][k]);
-        }
-        // q * 2^e lies in [128, 256): every bf16 value splits exactly into e4m3 hi + lo (down to the
-        // e4m3 subnormal step); the score is rescaled by 2^-e.
-        int E = 0;
-        if (qmax > 0.f) frexpf(qmax, &E);
-        const int e = qmax > 0.f ? 8 - E : 0;
-        const float qmul = ldexpf(1.f, e);
-        for (int it = pt; it < kHeadsPerCta * 36; it += kPrepThreads) {
-            const int h = it / 36, ch = it - h * 36;
-            const int hg = half * kHeadsPerCta + h;
-            uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
-            if (hg < a.H) {
-                const __nv_bfloat16 *src = ch < 32 ? a.q_lat + ((int64_t)b * a.H + hg) * kKL + ch * 16
-                                                   : a.q_rope + ((int64_t)b * a.H + hg) * kKR + (ch - 32) * 16;
-                const uint4 u0 = *reinterpret_cast<const uint4 *>(src), u1 = *reinterpret_cast<const uint4 *>(src + 8);
-                const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            for (int64_t t = t0 + pt; t < t1; t += 8 * kPrepThreads) {
+                float v[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[k]));
+                for (int u = 0; u < 8; ++u) {
+                    const int64_t tu = t + (int64_t)u * kPrepThreads;
+                    v[u] = tu < t1 ? __ldg(a.kv_scale + tu) : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) smax = fmaxf(smax, fabsf(v[u]));
+            }
+#pragma unroll
+            for (int k = 0; k < kItems; ++k) {
+                const int it = pt + k * kPrepThreads, h = it / 36;
+                const uint32_t w[8] = {qv[k][0].x, qv[k][0].y, qv[k][0].z, qv[k][0].w,
+                                       qv[k][1].x, qv[k][1].y, qv[k][1].z, qv[k][1].w};
+                float mx = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
+                    mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+                }
+                atomicMax(&ms.ph.pro.qmax_bits[h], __float_as_int(mx));  // non-negative floats order like ints
+            }
+            smax = warp_max(smax);
+            if (lane == 0) ms.ph.pro.wred[1][warp - 1] = smax;
+            named_sync(1, kPrepThreads);
+            smax = 0.f;
+            for (int k = 0; k < 9; ++k) smax = fmaxf(smax, ms.ph.pro.wred[1][k]);
+            // q_h * 2^e_h lies in [128, 256): every bf16 value splits exactly into e4m3 hi + lo (down to
+            // the e4m3 subnormal step); the score is rescaled by 2^-e_h.
+#pragma unroll
+            for (int k = 0; k < kItems; ++k) {
+                const int it = pt + k * kPrepThreads, h = it / 36, ch = it - h * 36;
+                const float qmax = __int_as_float(ms.ph.pro.qmax_bits[h]);
+                int E = 0;
+                if (qmax > 0.f) frexpf(qmax, &E);
+                const float qmul = qmax > 0.f ? ldexpf(1.f, 8 - E) : 1.f;
+                const uint32_t w[8] = {qv[k][0].x, qv[k][0].y, qv[k][0].z, qv[k][0].w,
+                                       qv[k][1].x, qv[k][1].y, qv[k][1].z, qv[k][1].w};
+                uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                for (int e2 = 0; e2 < 8; ++e2) {
+                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e2]));
                     uint32_t ph, pl;
                     split_pair(f.x * qmul, f.y * qmul, ph, pl);
-                    hi[k >> 1] |= ph << ((k & 1) * 16);
-                    lo[k >> 1] |= pl << ((k & 1) * 16);
+                    hi[e2 >> 1] |= ph << ((e2 & 1) * 16);
+                    lo[e2 >> 1] |= pl << ((e2 & 1) * 16);
                 }
+                uint8_t *img = smem + OFF_Q;
+                uint32_t off_hi, off_lo;
+                if (ch < 32) {
+                    const uint32_t kb = ch >> 3, byte = (ch & 7) * 16;
+                    off_hi = kb * 16384 + sw128_offset(h, byte);
+                    off_lo = kb * 16384 + sw128_offset(h + 64, byte);
+                } else {
+                    const uint32_t byte = (ch - 32) * 16;
+                    off_hi = kRcOff + sw64_offset(h, byte);
+                    off_lo = kRcOff + sw64_offset(h + 64, byte);
+                }
+                *reinterpret_cast<uint4 *>(img + off_hi) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4 *>(img + off_lo) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
-            uint8_t *img = smem + OFF_Q;
-            uint32_t off_hi, off_lo;
-            if (ch < 32) {
-                const uint32_t kb = ch >> 3, byte = (ch & 7) * 16;
-                off_hi = kb * 16384 + sw128_offset(h, byte);
-                off_lo = kb * 16384 + sw128_offset(h + 64, byte);
-            } else {
-                const uint32_t byte = (ch - 32) * 16;
-                off_hi = kRcOff + sw64_offset(h, byte);
-                off_lo = kRcOff + sw64_offset(h + 64, byte);
+            if (pt < kHeadsPerCta) {
+                const int hg = half * kHeadsPerCta + pt;
+                const float qmax = __int_as_float(ms.ph.pro.qmax_bits[pt]);
+                int E = 0;
+                if (qmax > 0.f) frexpf(qmax, &E);
+                ms.c_head[pt] = hg < a.H ? a.sm_scale_log2 * (qmax > 0.f ? ldexpf(1.f, E - 8) : 1.f) : 0.f;
             }
-            *reinterpret_cast<uint4 *>(img + off_hi) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4 *>(img + off_lo) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
-        if (pt < kHeadsPerCta) ms.m_run[pt] = -INFINITY;
+        if (pt < kHeadsPerCta) ms.m_run[0][pt] = ms.m_run[1][pt] = -INFINITY;
         if (pt == 0) {
             const float s_ref = fmaxf(smax, 1e-30f);
-            ms.c_score = a.sm_scale_log2 * ldexpf(1.f, -e);
             ms.w_mul = kWScale / s_ref;
             ms.out_mul = s_ref / kWScale;
         }
@@ -273,47 +367,75 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t id_s = idesc_e4m3_f32(128, 128, false, false);
                 const uint32_t id_pv = idesc_e4m3_f32(128, 64, true, true);
                 const uint32_t qb = sbase + OFF_Q;
-                for (int i = 0; i <= n_tiles; ++i) {
-                    if (i < n_tiles) {
-                        const int s = i & 1;
-                        if (!mbar_wait(&ms.kv_full[s], (i >> 1) & 1, &ms.abort_flag, a.err_word)) break;
-                        if (i >= 2 && !mbar_wait(&ms.s_free[s], ((i >> 1) - 1) & 1, &ms.abort_flag, a.err_word)) break;
-                        tc_fence_after_sync();
-                        const uint32_t st = sbase + (s ? OFF_ST1 : OFF_ST0);
-                        const uint32_t d = tmem + (uint32_t)s * 128u;
+                auto issue_score = [&](int i) {
+                    const int s = i & 1;
+                    const uint32_t st = sbase + (s ? OFF_ST1 : OFF_ST0);
+                    const uint32_t d = tmem + (uint32_t)s * 128u;
 #pragma unroll
-                        for (int kb = 0; kb < 4; ++kb)
+                    for (int kb = 0; kb < 4; ++kb)
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                mma_f8f6f4(d, smem_desc(st + kb * 16384 + kk * 32, 0, 1024, kSw128),
-                                           smem_desc(qb + kb * 16384 + kk * 32, 0, 1024, kSw128), id_s,
-                                           (kb | kk) != 0);
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_f8f6f4(d, smem_desc(st + kb * 16384 + kk * 32, 0, 1024, kSw128),
+                                       smem_desc(qb + kb * 16384 + kk * 32, 0, 1024, kSw128), id_s, (kb | kk) != 0);
 #pragma unroll
-                        for (int kk = 0; kk < 2; ++kk)
-                            mma_f8f6f4(d, smem_desc(st + kRcOff + kk * 32, 0, 512, kSw64),
-                                       smem_desc(qb + kRcOff + kk * 32, 0, 512, kSw64), id_s, 1);
-                        mma_commit(&ms.s_full[s]);
-                    }
-                    if (i >= 1) {
-                        const int j = i - 1, s = j & 1;
-                        if (!mbar_wait(&ms.p_full, j & 1, &ms.abort_flag, a.err_word)) break;
-                        tc_fence_after_sync();
-                        const uint32_t st = sbase + (s ? OFF_ST1 : OFF_ST0);
-                        const uint32_t phi = st + kRcOff, plo = sbase + OFF_PLO;
+                    for (int kk = 0; kk < 2; ++kk)
+                        mma_f8f6f4(d, smem_desc(st + kRcOff + kk * 32, 0, 512, kSw64),
+                                   smem_desc(qb + kRcOff + kk * 32, 0, 512, kSw64), id_s, 1);
+                    mma_commit(&ms.s_full[s]);
+                };
+                auto issue_pv = [&](int j) {
+                    const int s = j & 1;
+                    const uint32_t st = sbase + (s ? OFF_ST1 : OFF_ST0);
+                    const uint32_t phi = st + kRcOff, plo = sbase + OFF_PLO;
 #pragma unroll
-                        for (int ch = 0; ch < 4; ++ch) {
-                            const uint32_t d = tmem + 256u + (uint32_t)ch * 64u;
+                    for (int ch = 0; ch < 4; ++ch) {
+                        const uint32_t d = tmem + 256u + (uint32_t)ch * 64u;
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk) {
-                                const uint64_t ad = smem_desc(st + ch * 16384 + kk * 4096, 0, 1024, kSw128);
-                                mma_f8f6f4(d, ad, smem_desc(phi + kk * 2048, 0, 512, kSw64), id_pv, (j | kk) != 0);
-                                mma_f8f6f4(d, ad, smem_desc(plo + kk * 2048, 0, 512, kSw64), id_pv, 1);
-                            }
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t ad = smem_desc(st + ch * 16384 + kk * 4096, 0, 1024, kSw128);
+                            mma_f8f6f4(d, ad, smem_desc(phi + kk * 2048, 0, 512, kSw64), id_pv, (j | kk) != 0);
+                            mma_f8f6f4(d, ad, smem_desc(plo + kk * 2048, 0, 512, kSw64), id_pv, 1);
                         }
-                        mma_commit(&ms.kv_empty[s]);
-                        mma_commit(&ms.pv_done);
+                        mma_commit(&ms.kv_blk[s][ch]);  // latent block ch may be refilled
+                    }
+                    mma_commit(&ms.kv_empty[s]);
+                    mma_commit(&ms.pv_done);
+                };
+                // Issue whichever is ready, the context product first: it releases the row stage for
+                // the next load.  Score i needs tile i loaded and score buffer i%2 read by the softmax
+                // (tile i-2); PV j needs the weights of tile j.
+                int ns = 0, np = 0;
+                if (a.qimg && n_tiles > 0 && !mbar_wait(&ms.q_full, 0, &ms.abort_flag, a.err_word)) np = n_tiles;
+                const uint64_t t_start = globaltimer_ns();
+                uint64_t t_last = t_start;
+                uint32_t spins = 0;
+                while (np < n_tiles) {
+                    if (np < ns && mbar_try_wait(&ms.p_full, np & 1)) {
+                        tc_fence_after_sync();
+                        issue_pv(np++);
+                        spins = 0;
+                        continue;
+                    }
+                    if (ns < n_tiles && mbar_try_wait(&ms.kv_full[ns & 1], (ns >> 1) & 1) &&
+                        (ns < 2 || mbar_try_wait(&ms.s_free[ns & 1], ((ns >> 1) - 1) & 1))) {
+                        tc_fence_after_sync();
+                        issue_score(ns++);
+                        spins = 0;
+                        continue;
+                    }
+                    if ((++spins & 255u) == 0) {
+                        const uint64_t now = globaltimer_ns();
+                        if (ms.abort_flag) break;
+                        if (spins > 256u && now - t_last > 2000000000ull) {  // no progress for 2 s
+                            ms.abort_flag = 1;
+                            if (a.err_word) atomicOr(a.err_word, (int)KV8_ERR_TIMEOUT);
+                            break;
+                        }
+                    } else if (spins == 1) {
+                        t_last = globaltimer_ns();
                     }
                 }
+                (void)t_start;
                 // all issued MMAs complete before the CTA tears down
                 mma_commit(&ms.final_bar);
                 mbar_wait(&ms.final_bar, 0, nullptr, a.err_word, 200000000ull);
@@ -326,12 +448,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int r = q * 32 + lane;          // row within the tile = TMEM lane
             const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
             SoftSync sync{&ms.sync_bar, &ms.abort_flag, a.err_word};
-            const float c_score = ms.c_score, w_mul = ms.w_mul;
+            const float w_mul = ms.w_mul;
             float z[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) z[j] = 0.f;
             float sc_next = (n_tiles > 0 && t0 + r < t1) ? __ldg(a.kv_scale + t0 + r) : 0.f;
             bool ok = true;
+            int cur = 0;  // which ms.m_run copy is current (uniform across the softmax threads)
             for (int i = 0; i < n_tiles && ok; ++i) {
                 const int bb = i & 1;
                 const int64_t t = t0 + (int64_t)i * kTile + r;
@@ -341,7 +464,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 if (!(ok = mbar_wait(&ms.s_full[bb], (i >> 1) & 1, &ms.abort_flag, a.err_word))) break;
                 tc_fence_after_sync();
-                const float f = sc_t * c_score;
                 float s[32];
 #pragma unroll
                 for (int k2 = 0; k2 < 2; ++k2) {
@@ -350,72 +472,86 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_32x32b_x16(tmem + lane_addr + (uint32_t)bb * 128u + 64u + 32u * hh + 16u * k2, slo);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        s[16 * k2 + j] = valid ? (__uint_as_float(shi[j]) + __uint_as_float(slo[j])) * f : -INFINITY;
+                    for (int j = 0; j < 16; ++j) s[16 * k2 + j] = __uint_as_float(shi[j]) + __uint_as_float(slo[j]);
+                }
+#pragma unroll
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    const float4 c4 = *reinterpret_cast<const float4 *>(&ms.c_head[32 * hh + 4 * j4]);
+                    s[4 * j4 + 0] = valid ? s[4 * j4 + 0] * (c4.x * sc_t) : -INFINITY;
+                    s[4 * j4 + 1] = valid ? s[4 * j4 + 1] * (c4.y * sc_t) : -INFINITY;
+                    s[4 * j4 + 2] = valid ? s[4 * j4 + 2] * (c4.z * sc_t) : -INFINITY;
+                    s[4 * j4 + 3] = valid ? s[4 * j4 + 3] * (c4.w * sc_t) : -INFINITY;
                 }
                 tc_fence_before_sync();
                 mbar_arrive(&ms.s_free[bb]);
 
                 // lazy rescale check: does any score exceed its head's running max by more than kTau?
+                const float *mrow = &ms.m_run[cur][32 * hh];
                 bool need = false;
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
-                    const float4 m4 = *reinterpret_cast<const float4 *>(&ms.m_run[32 * hh + 4 * j4]);
+                    const float4 m4 = *reinterpret_cast<const float4 *>(mrow + 4 * j4);
                     need |= (s[4 * j4 + 0] > m4.x + kTau) | (s[4 * j4 + 1] > m4.y + kTau) |
                             (s[4 * j4 + 2] > m4.z + kTau) | (s[4 * j4 + 3] > m4.w + kTau);
                 }
                 if (need) ms.vote[bb] = i + 1;
                 if (!(ok = sync())) break;
-                if (ms.vote[bb] == i + 1) {
-                    // tile max per head: warp reduce, then across the 4 quadrants
-                    float mine = -INFINITY;
+                const bool slow = ms.vote[bb] == i + 1;
+                bool any_alpha = false;
+                if (slow) {
+                    // tile max per head over this warp's 32 rows (order-preserving integer keys)
+                    int mine = 0;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        const float v = warp_max(s[j]);
+                        const int bits = __float_as_int(s[j]);
+                        const int key = bits >= 0 ? bits : (bits ^ 0x7FFFFFFF);
+                        int v;
+                        asm volatile("redux.sync.max.s32 %0, %1, 0xffffffff;" : "=r"(v) : "r"(key));
                         if (lane == j) mine = v;
                     }
-                    ms.red[q][32 * hh + lane] = mine;
+                    mine = mine >= 0 ? mine : (mine ^ 0x7FFFFFFF);
+                    ms.red[q][32 * hh + lane] = __int_as_float(mine);
                     if (!(ok = sync())) break;
-                    if (q == 0) {
-                        const int h = 32 * hh + lane;
-                        const float tmax = fmaxf(fmaxf(ms.red[0][h], ms.red[1][h]), fmaxf(ms.red[2][h], ms.red[3][h]));
-                        const float mo = ms.m_run[h];
-                        const float mn = (tmax > mo + kTau) ? tmax : mo;
-                        ms.alpha[h] = (mn == mo) ? 1.f : exp2f(mo - mn);
-                        ms.m_run[h] = mn;
-                    }
-                    if (!(ok = sync())) break;
-                    bool any = false;
+                    // every quadrant warp combines the four quadrant maxima of its heads itself
+                    float *mnext = &ms.m_run[cur ^ 1][32 * hh];
+                    float *al = ms.ph.alpha[warp - 2];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float al = ms.alpha[32 * hh + j];
-                        z[j] *= al;
-                        any |= al != 1.f;
-                    }
-                    if (any && i >= 1) {
-                        // rescale this warp's 32 head columns of the context accumulators (after PV(i-1))
-                        if (!(ok = mbar_wait(&ms.pv_done, (i - 1) & 1, &ms.abort_flag, a.err_word))) break;
-                        tc_fence_after_sync();
-#pragma unroll 1
-                        for (int ch = 0; ch < 8; ++ch) {
-                            uint32_t o[16];
-                            const uint32_t ta = tmem + lane_addr + 256u + 64u * (ch >> 1) + 32u * hh + 16u * (ch & 1);
-                            tmem_ld_32x32b_x16(ta, o);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                o[j] = __float_as_uint(__uint_as_float(o[j]) * ms.alpha[32 * hh + 16 * (ch & 1) + j]);
-                            tmem_st_32x32b_x16(ta, o);
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 r0 = *reinterpret_cast<const float4 *>(&ms.red[0][32 * hh + 4 * j4]);
+                        const float4 r1 = *reinterpret_cast<const float4 *>(&ms.red[1][32 * hh + 4 * j4]);
+                        const float4 r2 = *reinterpret_cast<const float4 *>(&ms.red[2][32 * hh + 4 * j4]);
+                        const float4 r3 = *reinterpret_cast<const float4 *>(&ms.red[3][32 * hh + 4 * j4]);
+                        const float4 mo = *reinterpret_cast<const float4 *>(mrow + 4 * j4);
+                        const float t0 = fmaxf(fmaxf(r0.x, r1.x), fmaxf(r2.x, r3.x));
+                        const float t1 = fmaxf(fmaxf(r0.y, r1.y), fmaxf(r2.y, r3.y));
+                        const float t2 = fmaxf(fmaxf(r0.z, r1.z), fmaxf(r2.z, r3.z));
+                        const float t3 = fmaxf(fmaxf(r0.w, r1.w), fmaxf(r2.w, r3.w));
+                        const float4 mn = make_float4(t0 > mo.x + kTau ? t0 : mo.x, t1 > mo.y + kTau ? t1 : mo.y,
+                                                      t2 > mo.z + kTau ? t2 : mo.z, t3 > mo.w + kTau ? t3 : mo.w);
+                        const float4 a4 = make_float4(mn.x == mo.x ? 1.f : exp2f(mo.x - mn.x),
+                                                      mn.y == mo.y ? 1.f : exp2f(mo.y - mn.y),
+                                                      mn.z == mo.z ? 1.f : exp2f(mo.z - mn.z),
+                                                      mn.w == mo.w ? 1.f : exp2f(mo.w - mn.w));
+                        if (lane == 0) {
+                            *reinterpret_cast<float4 *>(mnext + 4 * j4) = mn;  // the same values from all 4 quadrants
+                            *reinterpret_cast<float4 *>(al + 4 * j4) = a4;
                         }
-                        tmem_wait_st();
+                        z[4 * j4 + 0] *= a4.x;
+                        z[4 * j4 + 1] *= a4.y;
+                        z[4 * j4 + 2] *= a4.z;
+                        z[4 * j4 + 3] *= a4.w;
+                        any_alpha |= (a4.x != 1.f) | (a4.y != 1.f) | (a4.z != 1.f) | (a4.w != 1.f);
                     }
+                    __syncwarp();
+                    cur ^= 1;
+                    mrow = &ms.m_run[cur][32 * hh];
                 }
                 // weights: p = 2^(s - m) (row sum z), w = p * s_t * kWScale / s_ref, split e4m3 hi + lo
                 const float g = sc_t * w_mul;
                 uint32_t whi[8], wlo[8];
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
-                    const float4 m4 = *reinterpret_cast<const float4 *>(&ms.m_run[32 * hh + 4 * j4]);
+                    const float4 m4 = *reinterpret_cast<const float4 *>(mrow + 4 * j4);
                     const float p0 = exp2f(s[4 * j4 + 0] - m4.x), p1 = exp2f(s[4 * j4 + 1] - m4.y);
                     const float p2 = exp2f(s[4 * j4 + 2] - m4.z), p3 = exp2f(s[4 * j4 + 3] - m4.w);
                     z[4 * j4 + 0] += p0;
@@ -423,8 +559,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     z[4 * j4 + 2] += p2;
                     z[4 * j4 + 3] += p3;
                     uint32_t h01, l01, h23, l23;
-                    split_pair(p0 * g, p1 * g, h01, l01);
-                    split_pair(p2 * g, p3 * g, h23, l23);
+                    split_pair_h(p0 * g, p1 * g, h01, l01);
+                    split_pair_h(p2 * g, p3 * g, h23, l23);
                     whi[j4] = h01 | (h23 << 16);
                     wlo[j4] = l01 | (l23 << 16);
                 }
@@ -432,7 +568,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4 *>(phi + sw64_offset(r, 32 * hh)) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
                 *reinterpret_cast<uint4 *>(phi + sw64_offset(r, 32 * hh + 16)) =
                     make_uint4(whi[4], whi[5], whi[6], whi[7]);
-                if (i >= 1 && !(ok = mbar_wait(&ms.pv_done, (i - 1) & 1, &ms.abort_flag, a.err_word))) break;
+                if (i >= 1) {
+                    // the previous context product must be done before its weights' lo buffer is reused
+                    // and before its accumulators are rescaled
+                    if (!(ok = mbar_wait(&ms.pv_done, (i - 1) & 1, &ms.abort_flag, a.err_word))) break;
+                    if (any_alpha) {
+                        tc_fence_after_sync();
+                        const float *al = ms.ph.alpha[warp - 2];
+                        bool chunk_any[2] = {false, false};
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) chunk_any[j >> 4] |= al[j] != 1.f;
+#pragma unroll 1
+                        for (int ch = 0; ch < 4; ++ch) {
+                            const uint32_t ta = tmem + lane_addr + 256u + 64u * ch + 32u * hh;
+                            uint32_t o0[16], o1[16];
+                            if (chunk_any[0]) tmem_ld_32x32b_x16(ta, o0);
+                            if (chunk_any[1]) tmem_ld_32x32b_x16(ta + 16u, o1);
+                            tmem_wait_ld();
+                            if (chunk_any[0]) {
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) o0[j] = __float_as_uint(__uint_as_float(o0[j]) * al[j]);
+                                tmem_st_32x32b_x16(ta, o0);
+                            }
+                            if (chunk_any[1]) {
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) o1[j] = __float_as_uint(__uint_as_float(o1[j]) * al[16 + j]);
+                                tmem_st_32x32b_x16(ta + 16u, o1);
+                            }
+                        }
+                        tmem_wait_st();
+                    }
+                }
                 uint8_t *plo = smem + OFF_PLO;
                 *reinterpret_cast<uint4 *>(plo + sw64_offset(r, 32 * hh)) = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
                 *reinterpret_cast<uint4 *>(plo + sw64_offset(r, 32 * hh + 16)) =
@@ -443,6 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 
             // ================================ epilogue ================================
+            grid_launch_dependents();
             if (ok && n_tiles > 0) ok = mbar_wait(&ms.pv_done, (n_tiles - 1) & 1, &ms.abort_flag, a.err_word);
             tc_fence_after_sync();
             // row sums: over the 32 lanes of the warp, then over the 4 quadrants
@@ -457,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) {
                 if (q == 0) {
                     const int h = 32 * hh + lane;
-                    ms.zsum[h] = ms.red[0][h] + ms.red[1][h] + ms.red[2][h] + ms.red[3][h];
+                    ms.ph.zsum[h] = ms.red[0][h] + ms.red[1][h] + ms.red[2][h] + ms.red[3][h];
                 }
                 ok = sync();
             }
@@ -485,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (a.ws) {
                             pv.cl[(((int64_t)b * a.P + part) * a.H + hg) * kKL + d] = v;
                         } else {
-                            const float zz = ms.zsum[hl];
+                            const float zz = ms.ph.zsum[hl];
                             a.out[((int64_t)b * a.H + hg) * kKL + d] = zz > 0.f ? v / zz : 0.f;
                         }
                     }
@@ -494,8 +661,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int hg = hbase + lane;
                     if (hg < a.H) {
                         const int64_t idx = ((int64_t)b * a.P + part) * a.H + hg;
-                        pv.m[idx] = n_tiles > 0 ? ms.m_run[32 * hh + lane] : -INFINITY;
-                        pv.z[idx] = ms.zsum[32 * hh + lane];
+                        pv.m[idx] = n_tiles > 0 ? ms.m_run[cur][32 * hh + lane] : -INFINITY;
+                        pv.z[idx] = ms.ph.zsum[32 * hh + lane];
                     }
                 }
             }
@@ -504,6 +671,86 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// Query prep for decode, run once before the partial kernel: block h < n_heads_pad splits head h's
+// query (scaled by 2^e_h so that max|q| * 2^e_h lies in [128, 256)) into e4m3 hi + lo rows of its head
+// group's image and writes its score factor sm_scale*log2(e)*2^-e_h (0 for a padding head); block
+// n_heads_pad + p takes the largest row scale of partition p.
+__global__ void __launch_bounds__(128) tc_prep_kernel(const __nv_bfloat16 *__restrict__ q_lat,
+                                                      const __nv_bfloat16 *__restrict__ q_rope, int H, int n_heads_pad,
+                                                      float sm_scale_log2, const float *__restrict__ kv_scale,
+                                                      int64_t T, int P, uint8_t *__restrict__ img,
+                                                      float *__restrict__ c_head, float *__restrict__ smax) {
+    grid_launch_dependents();  // the partial kernel may start its row loads while this runs
+    __shared__ float red[4];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, bid = blockIdx.x;
+    if (bid < n_heads_pad) {
+        const int h = bid, half = h / kHeadsPerCta, row = h - half * kHeadsPerCta;
+        uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        float mx = 0.f;
+        if (tid < 36 && h < H) {
+            const __nv_bfloat16 *src = tid < 32 ? q_lat + (int64_t)h * kKL + tid * 16 : q_rope + (int64_t)h * kKR + (tid - 32) * 16;
+            const uint4 u0 = __ldg(reinterpret_cast<const uint4 *>(src)), u1 = __ldg(reinterpret_cast<const uint4 *>(src) + 1);
+            w[0] = u0.x; w[1] = u0.y; w[2] = u0.z; w[3] = u0.w;
+            w[4] = u1.x; w[5] = u1.y; w[6] = u1.z; w[7] = u1.w;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
+                mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+        }
+        mx = warp_max(mx);
+        if (lane == 0) red[warp] = mx;
+        __syncthreads();
+        mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+        int E = 0;
+        if (mx > 0.f) frexpf(mx, &E);
+        const float qmul = mx > 0.f ? ldexpf(1.f, 8 - E) : 1.f;
+        if (tid < 36) {
+            uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
+                uint32_t ph, pl;
+                split_pair(f.x * qmul, f.y * qmul, ph, pl);
+                hi[e >> 1] |= ph << ((e & 1) * 16);
+                lo[e >> 1] |= pl << ((e & 1) * 16);
+            }
+            uint8_t *dst = img + (size_t)half * kImg;
+            uint32_t off_hi, off_lo;
+            if (tid < 32) {
+                const uint32_t kb = tid >> 3, byte = (tid & 7) * 16;
+                off_hi = kb * 16384 + sw128_offset(row, byte);
+                off_lo = kb * 16384 + sw128_offset(row + 64, byte);
+            } else {
+                const uint32_t byte = (tid - 32) * 16;
+                off_hi = kRcOff + sw64_offset(row, byte);
+                off_lo = kRcOff + sw64_offset(row + 64, byte);
+            }
+            *reinterpret_cast<uint4 *>(dst + off_hi) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4 *>(dst + off_lo) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+        if (tid == 0) c_head[h] = h < H ? sm_scale_log2 * (mx > 0.f ? ldexpf(1.f, E - 8) : 1.f) : 0.f;
+    } else {
+        const int p = bid - n_heads_pad;
+        const int64_t t0 = T * p / P, t1 = T * (p + 1) / P;
+        float mx = 0.f;
+        for (int64_t t = t0 + tid; t < t1; t += 8 * 128) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int64_t tu = t + (int64_t)u * 128;
+                v[u] = tu < t1 ? __ldg(kv_scale + tu) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) mx = fmaxf(mx, fabsf(v[u]));
+        }
+        mx = warp_max(mx);
+        if (lane == 0) red[warp] = mx;
+        __syncthreads();
+        if (tid == 0) smax[p] = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -556,8 +803,38 @@ cudaError_t launch_attn_tc(const AttnArgs &x, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     const int64_t grid = (int64_t)a.B * a.P * a.n_half;
+    if (x.tc_scratch && x.B == 1) {
+        // decode: prepare the queries once, then start the partial kernel as a programmatic dependent
+        uint8_t *scr = static_cast<uint8_t *>(x.tc_scratch);
+        a.qimg = scr;
+        a.c_head = reinterpret_cast<float *>(scr + 2 * (size_t)kImg);
+        a.smax = a.c_head + 2 * kHeadsPerCta;
+        const int n_heads_pad = a.n_half * kHeadsPerCta;
+        tc_prep_kernel<<<(unsigned)(n_heads_pad + a.P), 128, 0, st>>>(
+            a.q_lat, a.q_rope, a.H, n_heads_pad, a.sm_scale_log2, a.kv_scale, a.T, a.P, const_cast<uint8_t *>(a.qimg),
+            const_cast<float *>(a.c_head), const_cast<float *>(a.smax));
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, attn_tc_kernel, m_lc, m_rc, a);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     attn_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(m_lc, m_rc, a);
     return cudaGetLastError();
+}
+
+size_t tc_scratch_bytes(int P) {
+    // query images (2 head groups), per-head factors, per-partition row-scale maxima
+    return 2 * (size_t)kImg + 2 * kHeadsPerCta * sizeof(float) + (((size_t)P * sizeof(float) + 255) & ~(size_t)255);
 }
 
 }  // namespace kv8

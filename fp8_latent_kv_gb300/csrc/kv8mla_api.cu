@@ -24,6 +24,10 @@ inline bool valid_cache(const uint8_t *kv8, const float *kv_scale, int64_t T) {
 
 }  // namespace
 
+size_t decode_partial_bytes(int P, int H) {
+    return ((PartialView::floats(1, P, H) * sizeof(float)) + 255) & ~(size_t)255;
+}
+
 int decode_partitions(int H, int64_t T, int P_req) {
     (void)H;
     if (T < 1) return 1;
@@ -84,7 +88,8 @@ int mla_decode8_workspace_bytes(int H, int64_t T, int P_req, size_t *bytes) {
     int P = 0;
     int rc = mla_decode8_partitions(H, T, P_req, &P);
     if (rc != KV8_OK || !bytes) return rc != KV8_OK ? rc : KV8_EINVAL;
-    *bytes = PartialView::floats(1, P, H) * sizeof(float);
+    // partial sets first (the documented layout), then staging for the tensor-core path
+    *bytes = decode_partial_bytes(P, H) + tc_scratch_bytes(P);
     return KV8_OK;
 }
 
@@ -116,6 +121,7 @@ int mla_decode8_partial(const void *q_lat, const void *q_rope, int q_dtype, int 
     a.ws = static_cast<float *>(workspace);
     a.out = nullptr;
     a.err_word = err_word;
+    a.tc_scratch = static_cast<uint8_t *>(workspace) + decode_partial_bytes(a.P, H);
     // bf16 queries: tensor cores; f32 queries keep full f32 precision on the CUDA cores
     return status(a.q_bf16 ? launch_attn_tc(a, (cudaStream_t)stream) : launch_attn_simt(a, (cudaStream_t)stream));
 }

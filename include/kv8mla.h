@@ -100,11 +100,13 @@ KV8_API int kv8_quant_rows(const float *x, int64_t n, uint8_t *kv8, float *kv_sc
  * (cl[K], m, z) plus a log-sum-exp merge kernel; the cache is device-resident, only new rows are
  * uploaded).  One query of H heads over rows 0..T-1.
  *
- * Partition p of P covers rows [floor(T*p/P), floor(T*(p+1)/P)).  Workspace layout (f32), for
- * B batch items (B = 1 for decode):
+ * Partition p of P covers rows [floor(T*p/P), floor(T*(p+1)/P)).  The workspace begins with the
+ * partial sets (f32), for B batch items (B = 1 for decode):
  *     cl [B][P][H][512]   unnormalised context of each partition, relative to its own max
  *     m  [B][P][H]        partition max of score * log2(e)  (-inf for an empty partition)
  *     z  [B][P][H]        sum over the partition of 2^(score*log2(e) - m)
+ * The decode workspace continues with the library's own staging (the prepared queries); its size
+ * is included in mla_decode8_workspace_bytes.
  * mla_decode8_partitions:      the partition count P the library uses for (H, T, P_req):
  *                              P_req = 0 picks automatically, P_req > 0 is clamped to [1, T].
  * mla_decode8_workspace_bytes: workspace bytes for (H, T, P_req).

@@ -50,7 +50,9 @@ def test_partitions_and_workspace_sizes(lib):
     assert kv.mla_decode8_partitions(128, 5, P_req=9) == 5
     assert kv.mla_decode8_partitions(128, 1000, P_req=7) == 7
     P = kv.mla_decode8_partitions(128, 262144)
-    assert kv.mla_decode8_workspace_bytes(128, 262144) == P * 128 * 514 * 4
+    ws = kv.mla_decode8_workspace_bytes(128, 262144)
+    assert ws >= P * 128 * 514 * 4                      # the partial sets come first
+    assert ws - P * 128 * 514 * 4 < 256 * 1024          # plus a small staging area
     assert kv.mla_sel8_workspace_bytes(8, 128, 2048) == 8 * 16 * 128 * 514 * 4
 
 
