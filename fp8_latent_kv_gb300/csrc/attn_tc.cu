@@ -65,11 +65,11 @@ struct Misc {
         float alpha[8][32];                    // tile loop: per softmax warp, rescale factors of its heads
         float zsum[kHeadsPerCta];              // epilogue: row sums per head
     } ph;
-    uint64_t kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, pv_done, sync_bar, final_bar, q_full;
+    uint64_t kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, pv_done, sync_bar[2], final_bar, q_full;
     uint64_t kv_blk[2][4];  // latent block kb of a stage has been read by the context product
     uint32_t tmem_base;
     int abort_flag;
-    int vote[2];
+    int vote[2][2];  // [head half][tile parity]
     float w_mul;     // kWScale / s_ref
     float out_mul;   // s_ref / kWScale
 };
@@ -177,11 +177,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kb = 0; kb < 4; ++kb) mbar_init(&ms.kv_blk[s][kb], 1);
             mbar_init(&ms.s_full[s], 1);
             mbar_init(&ms.s_free[s], kSoftmaxThreads);
-            ms.vote[s] = 0;
+            ms.vote[0][s] = ms.vote[1][s] = 0;
         }
         mbar_init(&ms.p_full, kSoftmaxThreads);
         mbar_init(&ms.pv_done, 1);
-        mbar_init(&ms.sync_bar, kSoftmaxThreads);
+        mbar_init(&ms.sync_bar[0], kSoftmaxThreads / 2);
+        mbar_init(&ms.sync_bar[1], kSoftmaxThreads / 2);
         mbar_init(&ms.final_bar, 1);
         mbar_init(&ms.q_full, 1);
         ms.abort_flag = 0;
@@ -203,13 +204,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && n_tiles > 0) {
             prefetch_tensormap(&map_lc);
             prefetch_tensormap(&map_rc);
-            // tiles beyond the two stages are pulled into L2 ahead of their loads
-            auto prefetch = [&](int i) {
-                if (i >= n_tiles) return;
-                const int y = (int)(t0 + (int64_t)i * kTile);
-                for (int kb = 0; kb < 4; ++kb) tma_prefetch_l2_2d(&map_lc, kb * 128, y);
-                tma_prefetch_l2_2d(&map_rc, 512, y);
-            };
             int issued = 0, armed = 0;
             for (int i = 0; i < n_tiles; ++i) {
                 const int s = i & 1;
@@ -243,11 +237,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok_p) break;
                 tma_load_2d(st + kRcOff, &map_rc, 512, y, &ms.kv_full[s]);
                 issued = i + 1;
-                if (i == 1) {
-                    prefetch(2);
-                    prefetch(3);
-                }
-                if (i >= 1) prefetch(i + 3);
             }
             // every issued load must land before the CTA ends (a partly issued tile times out quickly,
             // after its issued blocks have landed)
@@ -447,7 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int hh = (warp - 2) >> 2;       // which 32 of the CTA's 64 heads
             const int r = q * 32 + lane;          // row within the tile = TMEM lane
             const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-            SoftSync sync{&ms.sync_bar, &ms.abort_flag, a.err_word};
+            // the two head halves (4 warps each) decide and rescale independently
+            SoftSync sync{&ms.sync_bar[hh], &ms.abort_flag, a.err_word};
             const float w_mul = ms.w_mul;
             float z[32];
 #pragma unroll
@@ -494,23 +484,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     need |= (s[4 * j4 + 0] > m4.x + kTau) | (s[4 * j4 + 1] > m4.y + kTau) |
                             (s[4 * j4 + 2] > m4.z + kTau) | (s[4 * j4 + 3] > m4.w + kTau);
                 }
-                if (need) ms.vote[bb] = i + 1;
+                if (need) ms.vote[hh][bb] = i + 1;
                 if (!(ok = sync())) break;
-                const bool slow = ms.vote[bb] == i + 1;
+                const bool slow = ms.vote[hh][bb] == i + 1;
                 bool any_alpha = false;
                 if (slow) {
-                    // tile max per head over this warp's 32 rows (order-preserving integer keys)
-                    int mine = 0;
+                    // tile max per head over this warp's 32 rows: butterfly transpose-reduction.  At
+                    // step k each lane keeps the half of its heads selected by lane bit k and takes the
+                    // max with the other half from lane ^ k; after 5 steps lane l holds head l's max.
+                    float v[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int bits = __float_as_int(s[j]);
-                        const int key = bits >= 0 ? bits : (bits ^ 0x7FFFFFFF);
-                        int v;
-                        asm volatile("redux.sync.max.s32 %0, %1, 0xffffffff;" : "=r"(v) : "r"(key));
-                        if (lane == j) mine = v;
+                    for (int j = 0; j < 32; ++j) v[j] = s[j];
+#pragma unroll
+                    for (int k = 16; k >= 1; k >>= 1) {
+                        const bool upper = (lane & k) != 0;
+#pragma unroll
+                        for (int j = 0; j < k; ++j) {
+                            const float send = upper ? v[j] : v[j + k];
+                            const float keep = upper ? v[j + k] : v[j];
+                            v[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, k));
+                        }
                     }
-                    mine = mine >= 0 ? mine : (mine ^ 0x7FFFFFFF);
-                    ms.red[q][32 * hh + lane] = __int_as_float(mine);
+                    ms.red[q][32 * hh + lane] = v[0];
                     if (!(ok = sync())) break;
                     // every quadrant warp combines the four quadrant maxima of its heads itself
                     float *mnext = &ms.m_run[cur ^ 1][32 * hh];
@@ -573,28 +568,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // and before its accumulators are rescaled
                     if (!(ok = mbar_wait(&ms.pv_done, (i - 1) & 1, &ms.abort_flag, a.err_word))) break;
                     if (any_alpha) {
+                        // rescale only the changed heads' columns of the four context accumulators
                         tc_fence_after_sync();
                         const float *al = ms.ph.alpha[warp - 2];
-                        bool chunk_any[2] = {false, false};
+                        uint32_t changed = 0;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) chunk_any[j >> 4] |= al[j] != 1.f;
-#pragma unroll 1
-                        for (int ch = 0; ch < 4; ++ch) {
-                            const uint32_t ta = tmem + lane_addr + 256u + 64u * ch + 32u * hh;
-                            uint32_t o0[16], o1[16];
-                            if (chunk_any[0]) tmem_ld_32x32b_x16(ta, o0);
-                            if (chunk_any[1]) tmem_ld_32x32b_x16(ta + 16u, o1);
+                        for (int j = 0; j < 32; ++j) changed |= (al[j] != 1.f ? 1u : 0u) << j;
+                        while (changed) {
+                            const int j = __ffs(changed) - 1;
+                            changed &= changed - 1;
+                            const float aj = al[j];
+                            const uint32_t ta = tmem + lane_addr + 256u + 32u * hh + (uint32_t)j;
+                            const uint32_t v0 = tmem_ld_32x32b_x1(ta), v1 = tmem_ld_32x32b_x1(ta + 64u);
+                            const uint32_t v2 = tmem_ld_32x32b_x1(ta + 128u), v3 = tmem_ld_32x32b_x1(ta + 192u);
                             tmem_wait_ld();
-                            if (chunk_any[0]) {
-#pragma unroll
-                                for (int j = 0; j < 16; ++j) o0[j] = __float_as_uint(__uint_as_float(o0[j]) * al[j]);
-                                tmem_st_32x32b_x16(ta, o0);
-                            }
-                            if (chunk_any[1]) {
-#pragma unroll
-                                for (int j = 0; j < 16; ++j) o1[j] = __float_as_uint(__uint_as_float(o1[j]) * al[16 + j]);
-                                tmem_st_32x32b_x16(ta + 16u, o1);
-                            }
+                            tmem_st_32x32b_x1(ta, __float_as_uint(__uint_as_float(v0) * aj));
+                            tmem_st_32x32b_x1(ta + 64u, __float_as_uint(__uint_as_float(v1) * aj));
+                            tmem_st_32x32b_x1(ta + 128u, __float_as_uint(__uint_as_float(v2) * aj));
+                            tmem_st_32x32b_x1(ta + 192u, __float_as_uint(__uint_as_float(v3) * aj));
                         }
                         tmem_wait_st();
                     }
