@@ -51,6 +51,7 @@ constexpr uint32_t kRcOff = 65536;     // rope block inside an image / stage
 constexpr uint32_t OFF_Q = 0, OFF_ST0 = kImg, OFF_ST1 = 2 * kImg, OFF_PLO = 3 * kImg, OFF_MISC = 3 * kImg + 8192;
 constexpr float kTau = 2.0f;           // lazy-rescale threshold (log2 units): p <= 2^kTau
 constexpr float kWScale = 64.0f;       // 2^(8 - kTau): keeps w <= 256 < 448 (e4m3 max)
+constexpr float kMStart = -1e30f;      // running max before any valid row (log2 units)
 
 struct Misc {
     // per-head arrays first: they are read with 16-byte vector loads
@@ -87,6 +88,9 @@ struct TcArgs {
     const float *kv_scale;
     int64_t T;
     int64_t pos0;                // causal: item b attends rows [0, pos0 + b]; -1: rows [0, T)
+    const int32_t *idx;          // selection: item b attends rows idx[b][0..NS) of its own cache (else null)
+    int NS;
+    int64_t seq_stride_rows;     // selection: rows between consecutive items' caches
     float sm_scale_log2;
     float *ws;                   // partial sets, or nullptr
     float *out;                  // direct normalised output when ws == nullptr
@@ -166,7 +170,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int per_item = a.P * a.n_half;
     const int b = blockIdx.x / per_item, rem = blockIdx.x - b * per_item;
     const int part = rem / a.n_half, half = rem - part * a.n_half;
-    const int64_t n_rows = a.pos0 >= 0 ? ((a.pos0 + b + 1 < a.T) ? a.pos0 + b + 1 : a.T) : a.T;
+    // the list this CTA walks: positions [t0, t1) of rows 0..n_rows-1 (dense / causal) or of idx[b] (selection)
+    const int64_t n_rows = a.idx ? (int64_t)a.NS : a.pos0 >= 0 ? ((a.pos0 + b + 1 < a.T) ? a.pos0 + b + 1 : a.T) : a.T;
+    const int32_t *idx_b = a.idx ? a.idx + (int64_t)b * a.NS : nullptr;
+    const int64_t seq_base = a.idx ? (int64_t)b * a.seq_stride_rows : 0;
     const int64_t t0 = n_rows * part / a.P, t1 = n_rows * (part + 1) / a.P;
     const int n_tiles = (int)((t1 - t0 + kTile - 1) / kTile);
 
@@ -201,48 +208,86 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ================================ TMA producer ================================
-        if (lane == 0 && n_tiles > 0) {
-            prefetch_tensormap(&map_lc);
-            prefetch_tensormap(&map_rc);
+        // Lane 0 issues the copies and does the waits; in selection mode the whole warp reads the
+        // tile's 128 row indices (4 per lane) and lane 0 gathers them 4 rows at a time.
+        if (n_tiles > 0) {
+            if (lane == 0) {
+                prefetch_tensormap(&map_lc);
+                prefetch_tensormap(&map_rc);
+            }
             int issued = 0, armed = 0;
             for (int i = 0; i < n_tiles; ++i) {
                 const int s = i & 1;
-                if (i == 2 || (i == n_tiles - 1 && i < 2)) {
+                if (lane == 0 && (i == 2 || (i == n_tiles - 1 && i < 2)) && a.qimg) {
                     // the rows do not depend on the query prep; the query image does
-                    if (a.qimg) {
-                        grid_dependency_wait();
-                        mbar_arrive_expect_tx(&ms.q_full, kImg);
-                        const uint8_t *src = a.qimg + (size_t)half * kImg;
-                        for (int kb = 0; kb < 4; ++kb) bulk_load(smem + OFF_Q + kb * 16384, src + kb * 16384, 16384, &ms.q_full);
-                        bulk_load(smem + OFF_Q + kRcOff, src + kRcOff, 8192, &ms.q_full);
-                    }
+                    grid_dependency_wait();
+                    mbar_arrive_expect_tx(&ms.q_full, kImg);
+                    const uint8_t *src = a.qimg + ((size_t)b * a.n_half + half) * kImg;
+                    for (int kb = 0; kb < 4; ++kb) bulk_load(smem + OFF_Q + kb * 16384, src + kb * 16384, 16384, &ms.q_full);
+                    bulk_load(smem + OFF_Q + kRcOff, src + kRcOff, 8192, &ms.q_full);
                 }
                 uint8_t *st = smem + (s ? OFF_ST1 : OFF_ST0);
-                const int y = (int)(t0 + (int64_t)i * kTile);
+                const int64_t p0 = t0 + (int64_t)i * kTile;
                 const uint32_t ph = ((i >> 1) - 1) & 1;  // phase of tile i-2's release
-                // each latent block is refilled as soon as the context product of tile i-2 has read it;
-                // the rope block also holds tile i-2's weights and is refilled after the whole product.
-                // The stage's full barrier is re-armed only after the first release: that implies tile
-                // i-2's phase of it has completed (one arrival per phase).
                 bool ok_p = true;
-                for (int kb = 0; kb < 4 && ok_p; ++kb) {
-                    if (i >= 2 && !(ok_p = mbar_wait(&ms.kv_blk[s][kb], ph, &ms.abort_flag, a.err_word))) break;
-                    if (kb == 0) {
-                        mbar_arrive_expect_tx(&ms.kv_full[s], kImg);
-                        armed = i + 1;
+                if (!idx_b) {
+                    // each latent block is refilled as soon as the context product of tile i-2 has read
+                    // it; the rope block also holds tile i-2's weights and is refilled after the whole
+                    // product.  The stage's full barrier is re-armed only after the first release: that
+                    // implies tile i-2's phase of it has completed (one arrival per phase).
+                    if (lane == 0) {
+                        const int y = (int)p0;
+                        for (int kb = 0; kb < 4 && ok_p; ++kb) {
+                            if (i >= 2 && !(ok_p = mbar_wait(&ms.kv_blk[s][kb], ph, &ms.abort_flag, a.err_word))) break;
+                            if (kb == 0) {
+                                mbar_arrive_expect_tx(&ms.kv_full[s], kImg);
+                                armed = i + 1;
+                            }
+                            tma_load_2d(st + kb * 16384, &map_lc, kb * 128, y, &ms.kv_full[s]);
+                        }
+                        if (ok_p && i >= 2) ok_p = mbar_wait(&ms.kv_empty[s], ph, &ms.abort_flag, a.err_word);
+                        if (ok_p) tma_load_2d(st + kRcOff, &map_rc, 512, y, &ms.kv_full[s]);
                     }
-                    tma_load_2d(st + kb * 16384, &map_lc, kb * 128, y, &ms.kv_full[s]);
+                } else {
+                    // rows of this tile: invalid or past-the-end entries fetch row 0 of the item's cache
+                    // (the softmax masks them).  The stage is refilled once tile i-2's context product is done.
+                    int rows[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int64_t pos = p0 + 4 * lane + k;
+                        int r = pos < t1 ? __ldg(idx_b + pos) : 0;
+                        if (r < 0 || (int64_t)r >= a.T) r = 0;
+                        rows[k] = (int)(seq_base + r);
+                    }
+                    if (lane == 0 && i >= 2) ok_p = mbar_wait(&ms.kv_empty[s], ph, &ms.abort_flag, a.err_word);
+                    ok_p = __shfl_sync(0xffffffffu, ok_p, 0);
+                    if (ok_p) {
+                        if (lane == 0) {
+                            mbar_arrive_expect_tx(&ms.kv_full[s], kImg);
+                            armed = i + 1;
+                        }
+                        __syncwarp();
+                        // lane l fetches tile rows 4l..4l+3: 512 bytes of each latent block, 256 of the rope block
+#pragma unroll
+                        for (int kb = 0; kb < 4; ++kb)
+                            tma_gather4(st + kb * 16384 + lane * 512, &map_lc, kb * 128, rows[0], rows[1], rows[2],
+                                        rows[3], &ms.kv_full[s]);
+                        tma_gather4(st + kRcOff + lane * 256, &map_rc, 512, rows[0], rows[1], rows[2], rows[3],
+                                    &ms.kv_full[s]);
+                    }
                 }
-                if (ok_p && i >= 2) ok_p = mbar_wait(&ms.kv_empty[s], ph, &ms.abort_flag, a.err_word);
+                ok_p = __shfl_sync(0xffffffffu, ok_p, 0);
                 if (!ok_p) break;
-                tma_load_2d(st + kRcOff, &map_rc, 512, y, &ms.kv_full[s]);
                 issued = i + 1;
             }
-            // every issued load must land before the CTA ends (a partly issued tile times out quickly,
-            // after its issued blocks have landed)
-            for (int i = (armed > 2 ? armed - 2 : 0); i < armed; ++i)
-                mbar_wait(&ms.kv_full[i & 1], (i >> 1) & 1, nullptr, a.err_word, i < issued ? 200000000ull : 20000000ull);
-            if (a.qimg && issued > 0) mbar_wait(&ms.q_full, 0, nullptr, a.err_word, 200000000ull);
+            if (lane == 0) {
+                // every issued load must land before the CTA ends (a partly issued tile times out
+                // quickly, after its issued blocks have landed)
+                for (int i = (armed > 2 ? armed - 2 : 0); i < armed; ++i)
+                    mbar_wait(&ms.kv_full[i & 1], (i >> 1) & 1, nullptr, a.err_word,
+                              i < issued ? 200000000ull : 20000000ull);
+                if (a.qimg && issued > 0) mbar_wait(&ms.q_full, 0, nullptr, a.err_word, 200000000ull);
+            }
         }
         __syncwarp();
     } else {
@@ -252,8 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (a.qimg) {
             // decode: the prep kernel wrote the query image (loaded by the producer) and the factors
             grid_dependency_wait();
-            if (pt < kHeadsPerCta) ms.c_head[pt] = a.c_head[half * kHeadsPerCta + pt];
-            smax = a.smax[part];
+            if (pt < kHeadsPerCta) ms.c_head[pt] = a.c_head[(b * a.n_half + half) * kHeadsPerCta + pt];
+            smax = a.smax[b * a.P + part];
         } else {
             // prefill: each CTA prepares its own 64 heads (the image is reused for all its tiles)
             constexpr int kItems = kHeadsPerCta * 36 / kPrepThreads;  // 8 chunks of 16 query elements
@@ -341,7 +386,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ms.c_head[pt] = hg < a.H ? a.sm_scale_log2 * (qmax > 0.f ? ldexpf(1.f, E - 8) : 1.f) : 0.f;
             }
         }
-        if (pt < kHeadsPerCta) ms.m_run[0][pt] = ms.m_run[1][pt] = -INFINITY;
+        // a finite start: weights 2^(s - m) of masked rows (s = -inf) are 0, never NaN, even while a
+        // head has seen no valid row
+        if (pt < kHeadsPerCta) ms.m_run[0][pt] = ms.m_run[1][pt] = kMStart;
         if (pt == 0) {
             const float s_ref = fmaxf(smax, 1e-30f);
             ms.w_mul = kWScale / s_ref;
@@ -442,15 +489,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             float z[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) z[j] = 0.f;
-            float sc_next = (n_tiles > 0 && t0 + r < t1) ? __ldg(a.kv_scale + t0 + r) : 0.f;
+            // scale of the row at list position pos, or -1 if that row is masked (past the end, or an
+            // index outside [0, T), which is also reported)
+            bool bad_index = false;
+            auto row_scale = [&](int64_t pos) -> float {
+                if (pos >= t1) return -1.f;
+                if (!idx_b) return __ldg(a.kv_scale + pos);
+                const int ri = __ldg(idx_b + pos);
+                if (ri < 0 || (int64_t)ri >= a.T) {
+                    bad_index = true;
+                    return -1.f;
+                }
+                return __ldg(a.kv_scale + seq_base + ri);
+            };
+            float sc_next = n_tiles > 0 ? row_scale(t0 + r) : -1.f;
             bool ok = true;
             int cur = 0;  // which ms.m_run copy is current (uniform across the softmax threads)
             for (int i = 0; i < n_tiles && ok; ++i) {
                 const int bb = i & 1;
                 const int64_t t = t0 + (int64_t)i * kTile + r;
-                const bool valid = t < t1;
                 const float sc_t = sc_next;
-                sc_next = (i + 1 < n_tiles && t + kTile < t1) ? __ldg(a.kv_scale + t + kTile) : 0.f;
+                const bool valid = sc_t >= 0.f;
+                sc_next = i + 1 < n_tiles ? row_scale(t + kTile) : -1.f;
 
                 if (!(ok = mbar_wait(&ms.s_full[bb], (i >> 1) & 1, &ms.abort_flag, a.err_word))) break;
                 tc_fence_after_sync();
@@ -542,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mrow = &ms.m_run[cur][32 * hh];
                 }
                 // weights: p = 2^(s - m) (row sum z), w = p * s_t * kWScale / s_ref, split e4m3 hi + lo
-                const float g = sc_t * w_mul;
+                const float g = valid ? sc_t * w_mul : 0.f;
                 uint32_t whi[8], wlo[8];
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
@@ -601,6 +661,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // ================================ epilogue ================================
             grid_launch_dependents();
+            if (hh == 0 && __any_sync(0xffffffffu, bad_index) && lane == 0 && a.err_word)
+                atomicOr(a.err_word, (int)KV8_ERR_INDEX);
             if (ok && n_tiles > 0) ok = mbar_wait(&ms.pv_done, (n_tiles - 1) & 1, &ms.abort_flag, a.err_word);
             tc_fence_after_sync();
             // row sums: over the 32 lanes of the warp, then over the 4 quadrants
@@ -652,7 +714,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int hg = hbase + lane;
                     if (hg < a.H) {
                         const int64_t idx = ((int64_t)b * a.P + part) * a.H + hg;
-                        pv.m[idx] = n_tiles > 0 ? ms.m_run[cur][32 * hh + lane] : -INFINITY;
+                        const float mh = ms.m_run[cur][32 * hh + lane];
+                        pv.m[idx] = (n_tiles > 0 && mh > kMStart) ? mh : -INFINITY;  // -inf: no valid row
                         pv.z[idx] = ms.ph.zsum[32 * hh + lane];
                     }
                 }
@@ -664,24 +727,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-// Query prep for decode, run once before the partial kernel: block h < n_heads_pad splits head h's
-// query (scaled by 2^e_h so that max|q| * 2^e_h lies in [128, 256)) into e4m3 hi + lo rows of its head
-// group's image and writes its score factor sm_scale*log2(e)*2^-e_h (0 for a padding head); block
-// n_heads_pad + p takes the largest row scale of partition p.
-__global__ void __launch_bounds__(128) tc_prep_kernel(const __nv_bfloat16 *__restrict__ q_lat,
-                                                      const __nv_bfloat16 *__restrict__ q_rope, int H, int n_heads_pad,
-                                                      float sm_scale_log2, const float *__restrict__ kv_scale,
-                                                      int64_t T, int P, uint8_t *__restrict__ img,
-                                                      float *__restrict__ c_head, float *__restrict__ smax) {
+// Query prep, run once before the partial kernel (decode and selection).  Block b * n_heads_pad + h
+// splits head h of item b (scaled by 2^e_h so that max|q| * 2^e_h lies in [128, 256)) into e4m3 hi +
+// lo rows of that item's head-group image and writes its score factor sm_scale*log2(e)*2^-e_h (0 for
+// a padding head); block B * n_heads_pad + b * P + p takes the largest scale among the rows that
+// partition p of item b attends.
+struct PrepArgs {
+    const __nv_bfloat16 *q_lat, *q_rope;
+    int B, H, n_heads_pad, P;
+    float sm_scale_log2;
+    const float *kv_scale;
+    int64_t T;
+    const int32_t *idx;  // selection lists [B][NS], or null (rows 0..T-1 of one item)
+    int NS;
+    int64_t seq_stride_rows;
+    uint8_t *img;        // [B][n_half][kImg]
+    float *c_head;       // [B][n_heads_pad]
+    float *smax;         // [B][P]
+};
+
+__global__ void __launch_bounds__(128) tc_prep_kernel(PrepArgs a) {
     grid_launch_dependents();  // the partial kernel may start its row loads while this runs
     __shared__ float red[4];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, bid = blockIdx.x;
-    if (bid < n_heads_pad) {
-        const int h = bid, half = h / kHeadsPerCta, row = h - half * kHeadsPerCta;
+    if (bid < a.B * a.n_heads_pad) {
+        const int b = bid / a.n_heads_pad, h = bid - b * a.n_heads_pad;
+        const int half = h / kHeadsPerCta, row = h - half * kHeadsPerCta;
         uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
         float mx = 0.f;
-        if (tid < 36 && h < H) {
-            const __nv_bfloat16 *src = tid < 32 ? q_lat + (int64_t)h * kKL + tid * 16 : q_rope + (int64_t)h * kKR + (tid - 32) * 16;
+        if (tid < 36 && h < a.H) {
+            const int64_t qh = (int64_t)b * a.H + h;
+            const __nv_bfloat16 *src = tid < 32 ? a.q_lat + qh * kKL + tid * 16 : a.q_rope + qh * kKR + (tid - 32) * 16;
             const uint4 u0 = __ldg(reinterpret_cast<const uint4 *>(src)), u1 = __ldg(reinterpret_cast<const uint4 *>(src) + 1);
             w[0] = u0.x; w[1] = u0.y; w[2] = u0.z; w[3] = u0.w;
             w[4] = u1.x; w[5] = u1.y; w[6] = u1.z; w[7] = u1.w;
@@ -708,7 +784,7 @@ __global__ void __launch_bounds__(128) tc_prep_kernel(const __nv_bfloat16 *__res
                 hi[e >> 1] |= ph << ((e & 1) * 16);
                 lo[e >> 1] |= pl << ((e & 1) * 16);
             }
-            uint8_t *dst = img + (size_t)half * kImg;
+            uint8_t *dst = a.img + ((size_t)b * (a.n_heads_pad / kHeadsPerCta) + half) * kImg;
             uint32_t off_hi, off_lo;
             if (tid < 32) {
                 const uint32_t kb = tid >> 3, byte = (tid & 7) * 16;
@@ -722,17 +798,21 @@ __global__ void __launch_bounds__(128) tc_prep_kernel(const __nv_bfloat16 *__res
             *reinterpret_cast<uint4 *>(dst + off_hi) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
             *reinterpret_cast<uint4 *>(dst + off_lo) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
-        if (tid == 0) c_head[h] = h < H ? sm_scale_log2 * (mx > 0.f ? ldexpf(1.f, E - 8) : 1.f) : 0.f;
+        if (tid == 0) a.c_head[bid] = h < a.H ? a.sm_scale_log2 * (mx > 0.f ? ldexpf(1.f, E - 8) : 1.f) : 0.f;
     } else {
-        const int p = bid - n_heads_pad;
-        const int64_t t0 = T * p / P, t1 = T * (p + 1) / P;
+        const int bp = bid - a.B * a.n_heads_pad, b = bp / a.P, p = bp - b * a.P;
+        const int64_t n_list = a.idx ? (int64_t)a.NS : a.T;
+        const int64_t t0 = n_list * p / a.P, t1 = n_list * (p + 1) / a.P;
+        const int32_t *idx_b = a.idx ? a.idx + (int64_t)b * a.NS : nullptr;
+        const float *sc_b = a.kv_scale + (int64_t)b * a.seq_stride_rows;
         float mx = 0.f;
         for (int64_t t = t0 + tid; t < t1; t += 8 * 128) {
             float v[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int64_t tu = t + (int64_t)u * 128;
-                v[u] = tu < t1 ? __ldg(kv_scale + tu) : 0.f;
+                int64_t ri = tu < t1 ? (idx_b ? (int64_t)__ldg(idx_b + tu) : tu) : -1;
+                v[u] = (ri >= 0 && ri < a.T) ? __ldg(sc_b + ri) : 0.f;
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u) mx = fmaxf(mx, fabsf(v[u]));
@@ -740,7 +820,7 @@ __global__ void __launch_bounds__(128) tc_prep_kernel(const __nv_bfloat16 *__res
         mx = warp_max(mx);
         if (lane == 0) red[warp] = mx;
         __syncthreads();
-        if (tid == 0) smax[p] = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+        if (tid == 0) a.smax[bp] = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
     }
 }
 
@@ -760,15 +840,20 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 }  // namespace
 
-// Launch the tensor-core kernel over a cache of T rows.  The grid covers B items x P partitions x
-// the head halves.  Returns cudaErrorNotSupported if the tensor-map encoder is unavailable.
+// Launch the tensor-core kernel.  The grid covers B items x P partitions x the head halves.  Dense
+// rows are loaded as 128-row tiles; selected rows are gathered 4 at a time from a tensor map over all
+// items' caches.  Returns cudaErrorNotSupported if the tensor-map encoder is unavailable.
 cudaError_t launch_attn_tc(const AttnArgs &x, cudaStream_t st) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
+    const bool sel = x.idx != nullptr;
+    const int64_t rows = sel ? (int64_t)(x.B - 1) * x.seq_stride_rows + x.T : x.T;
+    if (rows > 0x7fffffffLL) return cudaErrorInvalidValue;  // tensor-map row coordinates are 32-bit
     CUtensorMap m_lc, m_rc;
-    const cuuint64_t dims[2] = {(cuuint64_t)kRow, (cuuint64_t)x.T};
+    const cuuint64_t dims[2] = {(cuuint64_t)kRow, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)kRow};
-    const cuuint32_t box_lc[2] = {128, kTile}, box_rc[2] = {64, kTile}, es[2] = {1, 1};
+    const cuuint32_t box_h = sel ? 1u : (cuuint32_t)kTile;
+    const cuuint32_t box_lc[2] = {128, box_h}, box_rc[2] = {64, box_h}, es[2] = {1, 1};
     void *base = const_cast<uint8_t *>(x.kv8);
     if (encode(&m_lc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box_lc, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
@@ -787,6 +872,9 @@ cudaError_t launch_attn_tc(const AttnArgs &x, cudaStream_t st) {
     a.kv_scale = x.kv_scale;
     a.T = x.T;
     a.pos0 = x.pos0;
+    a.idx = x.idx;
+    a.NS = x.NS;
+    a.seq_stride_rows = x.seq_stride_rows;
     a.sm_scale_log2 = x.sm_scale_log2;
     a.ws = x.ws;
     a.out = x.out;
@@ -794,16 +882,30 @@ cudaError_t launch_attn_tc(const AttnArgs &x, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     const int64_t grid = (int64_t)a.B * a.P * a.n_half;
-    if (x.tc_scratch && x.B == 1) {
-        // decode: prepare the queries once, then start the partial kernel as a programmatic dependent
-        uint8_t *scr = static_cast<uint8_t *>(x.tc_scratch);
-        a.qimg = scr;
-        a.c_head = reinterpret_cast<float *>(scr + 2 * (size_t)kImg);
-        a.smax = a.c_head + 2 * kHeadsPerCta;
+    if (x.tc_scratch) {
+        // decode / selection: prepare the queries once, then start the partial kernel as a
+        // programmatic dependent
         const int n_heads_pad = a.n_half * kHeadsPerCta;
-        tc_prep_kernel<<<(unsigned)(n_heads_pad + a.P), 128, 0, st>>>(
-            a.q_lat, a.q_rope, a.H, n_heads_pad, a.sm_scale_log2, a.kv_scale, a.T, a.P, const_cast<uint8_t *>(a.qimg),
-            const_cast<float *>(a.c_head), const_cast<float *>(a.smax));
+        PrepArgs pa{};
+        pa.q_lat = a.q_lat;
+        pa.q_rope = a.q_rope;
+        pa.B = a.B;
+        pa.H = a.H;
+        pa.n_heads_pad = n_heads_pad;
+        pa.P = a.P;
+        pa.sm_scale_log2 = a.sm_scale_log2;
+        pa.kv_scale = a.kv_scale;
+        pa.T = a.T;
+        pa.idx = a.idx;
+        pa.NS = a.NS;
+        pa.seq_stride_rows = a.seq_stride_rows;
+        pa.img = static_cast<uint8_t *>(x.tc_scratch);
+        pa.c_head = reinterpret_cast<float *>(pa.img + (size_t)a.B * 2 * kImg);
+        pa.smax = pa.c_head + (size_t)a.B * 2 * kHeadsPerCta;
+        a.qimg = pa.img;
+        a.c_head = pa.c_head;
+        a.smax = pa.smax;
+        tc_prep_kernel<<<(unsigned)((int64_t)a.B * (n_heads_pad + a.P)), 128, 0, st>>>(pa);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)grid);
@@ -819,13 +921,15 @@ cudaError_t launch_attn_tc(const AttnArgs &x, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
+    if (sel) return cudaErrorInvalidValue;  // selection always takes the prepared-query path
     attn_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(m_lc, m_rc, a);
     return cudaGetLastError();
 }
 
-size_t tc_scratch_bytes(int P) {
-    // query images (2 head groups), per-head factors, per-partition row-scale maxima
-    return 2 * (size_t)kImg + 2 * kHeadsPerCta * sizeof(float) + (((size_t)P * sizeof(float) + 255) & ~(size_t)255);
+size_t tc_scratch_bytes(int B, int P) {
+    // query images (2 head groups per item), per-head factors, per-partition row-scale maxima
+    return (size_t)B * (2 * (size_t)kImg + 2 * kHeadsPerCta * sizeof(float)) +
+           (((size_t)B * P * sizeof(float) + 255) & ~(size_t)255);
 }
 
 }  // namespace kv8

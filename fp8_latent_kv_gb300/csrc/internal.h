@@ -24,15 +24,17 @@ struct AttnArgs {
     float *ws;                // partial sets (PartialView layout), or nullptr when `out` is written directly
     float *out;               // [B][H][512] normalised output (used when ws == nullptr; requires P == 1)
     int *err_word;            // optional device error word
-    void *tc_scratch;         // decode on the tensor cores: staging for the prepared queries (tc_scratch_bytes)
+    void *tc_scratch;         // decode / selection on the tensor cores: staging for the prepared queries
+                              // (tc_scratch_bytes(B, P)); null for prefill
 };
 
 cudaError_t launch_quant_rows(const float *x, int64_t n, uint8_t *q, float *scale, cudaStream_t st);
 cudaError_t launch_encode(const float *y, int64_t n, uint8_t *out, cudaStream_t st);
 cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t st);
-// tcgen05 kernel for bf16 queries over a dense (optionally causal) row range; a.idx must be null.
+// tcgen05 kernel for bf16 queries: a dense (optionally causal) row range, or selection lists (which
+// need tc_scratch and (B-1)*seq_stride_rows + T < 2^31).
 cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st);
-size_t tc_scratch_bytes(int P);
+size_t tc_scratch_bytes(int B, int P);
 cudaError_t launch_lse_merge(const float *ws, int B, int P, int H, float *out, cudaStream_t st);
 
 // Partition policy shared by the workspace queries and the launchers.

@@ -28,6 +28,10 @@ size_t decode_partial_bytes(int P, int H) {
     return ((PartialView::floats(1, P, H) * sizeof(float)) + 255) & ~(size_t)255;
 }
 
+size_t sel_partial_bytes(int B, int P, int H) {
+    return ((PartialView::floats(B, P, H) * sizeof(float)) + 255) & ~(size_t)255;
+}
+
 int decode_partitions(int H, int64_t T, int P_req) {
     (void)H;
     if (T < 1) return 1;
@@ -41,10 +45,15 @@ int decode_partitions(int H, int64_t T, int P_req) {
 }
 
 int select_partitions(int B, int H, int NS) {
-    (void)B;
-    (void)H;
-    int p = (NS + 127) / 128;
-    return p < 1 ? 1 : (p > 16 ? 16 : p);
+    // one wave of tensor-core CTAs (one per SM of a 152-SM part): B items x P partitions x head
+    // halves, with the list's 128-row tiles spread evenly over the partitions
+    const int64_t n_half = H > 64 ? 2 : 1;
+    const int64_t tiles = (NS + 127) / 128;
+    int64_t cap = 152 / ((int64_t)B * n_half);
+    if (cap < 1) cap = 1;
+    const int64_t per = (tiles + cap - 1) / cap;
+    const int64_t p = (tiles + per - 1) / per;
+    return (int)(p < 1 ? 1 : p);
 }
 
 }  // namespace kv8
@@ -89,7 +98,7 @@ int mla_decode8_workspace_bytes(int H, int64_t T, int P_req, size_t *bytes) {
     int rc = mla_decode8_partitions(H, T, P_req, &P);
     if (rc != KV8_OK || !bytes) return rc != KV8_OK ? rc : KV8_EINVAL;
     // partial sets first (the documented layout), then staging for the tensor-core path
-    *bytes = decode_partial_bytes(P, H) + tc_scratch_bytes(P);
+    *bytes = decode_partial_bytes(P, H) + tc_scratch_bytes(1, P);
     return KV8_OK;
 }
 
@@ -146,7 +155,9 @@ int mla_absorb_decode8(const void *q_lat, const void *q_rope, int q_dtype, int H
 int mla_sel8_workspace_bytes(int B, int H, int NS, size_t *bytes) {
     if (!bytes || B < 1 || B > 65535 || H < 1 || H > KV8_MAX_HEADS || NS < 1 || NS > KV8_MAX_SELECT)
         return KV8_EINVAL;
-    *bytes = PartialView::floats(B, select_partitions(B, H, NS), H) * sizeof(float);
+    const int P = select_partitions(B, H, NS);
+    // partial sets first, then staging for the tensor-core path
+    *bytes = sel_partial_bytes(B, P, H) + tc_scratch_bytes(B, P);
     return KV8_OK;
 }
 
@@ -179,7 +190,11 @@ int mla_absorb_sel8(const void *q_lat, const void *q_rope, int q_dtype, int B, i
     a.ws = static_cast<float *>(workspace);
     a.out = nullptr;
     a.err_word = err_word;
-    rc = status(launch_attn_simt(a, (cudaStream_t)stream));
+    a.tc_scratch = static_cast<uint8_t *>(workspace) + sel_partial_bytes(B, a.P, H);
+    // bf16 queries: tensor cores (row gathers address all items' caches with 32-bit row coordinates);
+    // f32 queries, or caches spanning 2^31 rows or more: CUDA cores
+    const bool tc = a.q_bf16 && (int64_t)(B - 1) * a.seq_stride_rows + T <= 0x7fffffffLL;
+    rc = status(tc ? launch_attn_tc(a, (cudaStream_t)stream) : launch_attn_simt(a, (cudaStream_t)stream));
     if (rc != KV8_OK) return rc;
     return mla_lse_merge8(workspace, B, a.P, H, out, stream);
 }

@@ -144,7 +144,11 @@ KV8_API int mla_absorb_decode8(const void *q_lat, const void *q_rope, int q_dtyp
  *   the sequence's own cache (any order; duplicates attend twice).  An index outside [0, T) is
  *   skipped and sets KV8_ERR_INDEX in *err_word.  out [B][H][512] f32.
  *   NS in [1, KV8_MAX_SELECT]; T in [1, KV8_MAX_ROWS]; H in [1, 128]; B >= 1.
- *   workspace >= mla_sel8_workspace_bytes(B, H, NS).
+ *   workspace >= mla_sel8_workspace_bytes(B, H, NS): the B x P partial sets, then staging for the
+ *   prepared bf16 queries.  P spreads the list's 128-row tiles over one wave of 152 CTAs (B items x
+ *   P x ceil(H/64)).  bf16 queries run on the tensor cores, which gather the selected rows from all
+ *   items' caches with 32-bit row coordinates; f32 queries, and caches with
+ *   (B-1)*seq_stride_rows + T >= 2^31 rows, run on the CUDA cores.
  * --------------------------------------------------------------------------------------------- */
 KV8_API int mla_sel8_workspace_bytes(int B, int H, int NS, size_t *bytes);
 KV8_API int mla_absorb_sel8(const void *q_lat, const void *q_rope, int q_dtype, int B, int H, const uint8_t *kv8,

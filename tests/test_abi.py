@@ -53,7 +53,11 @@ def test_partitions_and_workspace_sizes(lib):
     ws = kv.mla_decode8_workspace_bytes(128, 262144)
     assert ws >= P * 128 * 514 * 4                      # the partial sets come first
     assert ws - P * 128 * 514 * 4 < 256 * 1024          # plus a small staging area
-    assert kv.mla_sel8_workspace_bytes(8, 128, 2048) == 8 * 16 * 128 * 514 * 4
+    # selection: 8 items x 2 head halves leave 9 CTAs per item -> 16 tiles as 8 partitions of 2;
+    # partial sets, then 2 query images + 128 head factors per item and the row-scale maxima
+    assert kv.mla_sel8_workspace_bytes(8, 128, 2048) == 8 * 8 * 128 * 514 * 4 + 8 * (2 * 73728 + 512) + 256
+    # one item, 64 heads: up to 152 partitions of one tile
+    assert kv.mla_sel8_workspace_bytes(1, 64, 4096) == 1 * 32 * 64 * 514 * 4 + (2 * 73728 + 512) + 256
 
 
 def _rc(fn, *args):

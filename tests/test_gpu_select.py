@@ -116,3 +116,35 @@ def test_select_ragged_ns(lib, oracle):
         heads = [0, 63, 127]
         parity(got[:, heads], oracle.attn_select(ql[:, heads], qr[:, heads], q_o, s_o, T, T, idx,
                                                  synth.SM_SCALE)[0], f"NS={NS}")
+
+
+def test_select_f32_queries(lib, oracle):
+    # f32 queries keep full precision on the CUDA-core kernel
+    B, T, H = 2, 400, 20
+    rng = np.random.default_rng(4)
+    rows = synth.latent_rows(rng, B * T, 0.1, 10.0)
+    q_o, s_o = oracle.quant_rows(rows)
+    q = synth.normal_f32(rng, (B, H, 576))
+    ql, qr = np.ascontiguousarray(q[..., :512]), np.ascontiguousarray(q[..., 512:])
+    idx = rng.integers(0, T, size=(B, 300)).astype(np.int32)
+    got = _sel(lib, torch.from_numpy(ql).to(DEV), torch.from_numpy(qr).to(DEV), torch.from_numpy(q_o).to(DEV),
+               torch.from_numpy(s_o).to(DEV), T, T, torch.from_numpy(idx).to(DEV))
+    parity(got, oracle.attn_select(ql, qr, q_o, s_o, T, T, idx, synth.SM_SCALE)[0], "f32 queries")
+
+
+def test_select_partitions_with_no_valid_row(lib, oracle):
+    # whole partitions whose indices are all out of range, next to partitions with valid rows
+    B, T, H = 2, 3000, 128
+    q_o, s_o, ql, qr, rng = _small(oracle, B, T, H, 5)
+    NS = 1024
+    idx = rng.integers(0, T, size=(B, NS)).astype(np.int32)
+    idx[0, :512] = -5          # the first half of sequence 0's list
+    idx[1, 700:] = T + 3       # the tail of sequence 1's list
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = _sel(lib, _bf(ql), _bf(qr), torch.from_numpy(q_o).to(DEV), torch.from_numpy(s_o).to(DEV), T, T,
+               torch.from_numpy(idx).to(DEV), err)
+    assert err.item() & lib.KV8_ERR_INDEX
+    heads = [1, 64, 100]
+    ref, bad = oracle.attn_select(ql[:, heads], qr[:, heads], q_o, s_o, T, T, idx, synth.SM_SCALE)
+    assert bad == 512 + (NS - 700)
+    parity(got[:, heads], ref, "partitions without valid rows")
