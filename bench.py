@@ -1,18 +1,24 @@
-"""Benchmark: one fp8 MLA decode layer-step at T = 262144 on GB300.
+"""Benchmark of the fp8 MLA hot path on GB300.
 
-A step is the whole decode hot path for one layer and one new token, on one stream:
-  kv8_quant_rows (the fresh f32 row -> cache row T-1)  ->  split-T partial kernel  ->  LSE merge.
-Workload: H = 128 query heads, kv_lora 512 + qk_rope 64, T = 262144 e4m3 rows (152 MB incl. scales),
-bf16 queries, seeded synthetic data (synth.WORKLOADS["dec262k"]).
+Default workload (the headline): one decode layer-step at T = 262144.  A step is the whole decode
+hot path for one layer and one new token, on one stream:
+  kv8_quant_rows (the fresh f32 row -> cache row T-1)  ->  query prep + split-T partial kernel  ->  LSE merge.
+H = 128 query heads, kv_lora 512 + qk_rope 64, T = 262144 e4m3 rows (152 MB incl. scales), bf16
+queries, seeded synthetic data (synth.WORKLOADS["dec262k"]).
 
-Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-For N > 1 launch with torchrun; every rank runs an independent replica (the decode of one layer
-does not need a second GPU), and the timed region is bracketed by a barrier + synchronize.
+Other workloads (--workload), each one step of its own hot path:
+  dec16k   the same decode step at T = 16384
+  dsa      selected-row decode: 8 sequences x 2048 listed rows of a 131072-row cache each
+  prefill  kv8_quant_rows of the chunk's 1024 fresh rows + causal prefill of 1024 queries over T = 65536
 
-Printed (rank 0, one JSON line): metric / value (us per layer-step, whole job) / unit, timing
-details, `e2e` (host-resident inputs copied in and the context copied out every step, through the
-C ABI), `roofline` for the dominant kernel (CUDA-event time on its stream), `cpu_baseline` (the oracle
-on this host's cores, on a bounded sample), `clocks` sampled with nvidia-smi during the timed region.
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload KEY]
+For N > 1 launch with torchrun; every rank runs an independent replica (one layer's attention does
+not need a second GPU), and the timed region is bracketed by a barrier + synchronize.
+
+Printed (rank 0, one JSON line): metric / value (us per step, whole job) / unit, timing details,
+`e2e` (host-resident inputs copied in and the output copied out every step, through the C ABI),
+`roofline` for the dominant kernel (CUDA-event time on its stream), `cpu_baseline` (the oracle on
+this host's cores, on a bounded sample), `clocks` sampled with nvidia-smi during the timed region.
 """
 from __future__ import annotations
 
@@ -32,17 +38,13 @@ if ROOT not in sys.path:
 
 import numpy as np  # noqa: E402
 
-METRIC = "fp8 MLA decode µs/layer-step and HBM GB/s (% of peak) at T=262144"
-UNIT = "us/layer-step"
-KEY = "dec262k"
+HEADLINE_METRIC = "fp8 MLA decode µs/layer-step and HBM GB/s (% of peak) at T=262144"
 ROW_BYTES = 580                 # 576 e4m3 bytes + one f32 scale per cache row
 FLOP_PER_ROW_HEAD = 2 * 1088    # 576-wide score dot + 512-wide context accumulate
 L2_FLUSH_BYTES = 256 << 20      # 2x the 129 MB L2
-DECODE_KERNEL_SOURCES = ["fp8_latent_kv_gb300/csrc/attn_tc.cu", "fp8_latent_kv_gb300/csrc/sm100.cuh"]
-DECODE_KERNEL = "attn_tc_kernel"
-DECODE_BOUND = "tensor"         # e4m3 x e4m3 tensor-core contraction; 479 flop/B is above the HBM ridge
+TC_KERNEL_SOURCES = ["fp8_latent_kv_gb300/csrc/attn_tc.cu", "fp8_latent_kv_gb300/csrc/sm100.cuh"]
+TC_KERNEL = "attn_tc_kernel"
 MMA_PIECES = 2                  # hi + lo e4m3 pieces of the queries and of the weights: 2 MMAs per product
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode262k_traffic.json")
 
 
 # --------------------------------------------------------------------------------------------------
@@ -148,70 +150,319 @@ def sources_digest(paths) -> str:
     return h.hexdigest()[:16]
 
 
-def traffic_per_launch():
-    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, or None when the
-    kernel's sources changed since the counters were taken."""
-    if not os.path.exists(TRAFFIC_FILE):
+def traffic_file(key: str) -> str:
+    return os.path.join(ROOT, "profiles", f"{TC_KERNEL}_{key}_traffic.json")
+
+
+def traffic_per_launch(key: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, or None when there
+    is none for this workload or the kernel's sources changed since the counters were taken."""
+    path = traffic_file(key)
+    if not os.path.exists(path):
         return None
-    with open(TRAFFIC_FILE) as f:
+    with open(path) as f:
         d = json.load(f)
-    if d.get("sources_digest") != sources_digest(DECODE_KERNEL_SOURCES):
+    if d.get("sources_digest") != sources_digest(TC_KERNEL_SOURCES):
         return None
     return d.get("dram_bytes_per_launch")
 
 
-def alu_peak_tflops(sm_max_mhz: float | None) -> float:
-    # f32 FMA: 152 SMs x 128 lanes x 2 flop per clock at the maximum SM clock
-    mhz = sm_max_mhz or 2070.0
-    return 152 * 128 * 2 * mhz * 1e6 / 1e12
+def _bf16(torch, dev, a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev).to(torch.bfloat16)
 
 
-def build_decode_inputs(kv, torch, dev, w):
+class Case:
+    """One workload's step.  Subclasses build the resident inputs and define:
+    step(stream, ev)   enqueue one step; ev = (start, end) events around the dominant kernel call
+    e2e_step(stream)   the same step from pinned host buffers, output copied back
+    and the figures of the JSON line."""
+    key = ""
+    unit = "us/layer-step"
+    launches_per_step = 0
+    kernel_calls = ""       # what the events around the dominant call bracket
+    step_desc = ""
+
+    def config(self) -> dict:
+        raise NotImplementedError
+
+
+class DecodeCase(Case):
+    launches_per_step = 4  # quant + query prep + partial + merge
+    kernel_calls = "mla_decode8_partial: query prep + attn_tc_kernel (programmatic dependent launch)"
+    step_desc = "kv8_quant_rows(1 fresh row) + query prep + split-T partial + log-sum-exp merge"
+
+    def __init__(self, kv, torch, dev, w):
+        import synth
+        self.kv, self.torch, self.w = kv, torch, w
+        H, T = w.H, w.T
+        self.rows = synth.rows_for(w)
+        x = torch.from_numpy(self.rows).to(dev)
+        self.kv8 = torch.empty((T, 576), dtype=torch.uint8, device=dev)
+        self.sc = torch.empty(T, dtype=torch.float32, device=dev)
+        kv.kv8_quant_rows(x[:-1], self.kv8, self.sc)      # the resident cache: rows 0..T-2
+        self.fresh = x[-1:].clone()                       # this step's new row
+        del x
+        ql, qr = synth.queries_for(w, 1)
+        self.q_lat, self.q_rope = _bf16(torch, dev, ql[0]), _bf16(torch, dev, qr[0])
+        self.P = kv.mla_decode8_partitions(H, T)
+        self.ws = torch.empty(kv.mla_decode8_workspace_bytes(H, T) // 4, dtype=torch.float32, device=dev)
+        self.out = torch.empty((H, 512), dtype=torch.float32, device=dev)
+        # e2e host buffers
+        self.h_q_lat = self.q_lat.cpu().pin_memory()
+        self.h_q_rope = self.q_rope.cpu().pin_memory()
+        self.h_fresh = self.fresh.cpu().pin_memory()
+        self.h_out = torch.empty((H, 512), dtype=torch.float32).pin_memory()
+        self.d_fresh = torch.empty_like(self.fresh)
+        self.h2d = self.h_q_lat.numel() * 2 + self.h_q_rope.numel() * 2 + self.h_fresh.numel() * 4
+        self.d2h = self.h_out.numel() * 4
+        self.alg_bytes = T * ROW_BYTES + self.q_lat.numel() * 2 + self.q_rope.numel() * 2
+        self.alg_bytes_step = T * ROW_BYTES + self.h2d + self.d2h
+        self.flops = float(FLOP_PER_ROW_HEAD) * H * T
+
+    def step(self, stream, ev=None):
+        kv, w = self.kv, self.w
+        kv.kv8_quant_rows(self.fresh, self.kv8[w.T - 1:], self.sc[w.T - 1:], stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        kv.mla_decode8_partial(self.q_lat, self.q_rope, self.kv8, self.sc, w.T, SM_SCALE(), self.ws, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        kv.mla_lse_merge8(self.ws, 1, self.P, w.H, self.out, stream=stream)
+
+    def e2e_step(self, stream):
+        kv, w = self.kv, self.w
+        self.q_lat.copy_(self.h_q_lat, non_blocking=True)
+        self.q_rope.copy_(self.h_q_rope, non_blocking=True)
+        self.d_fresh.copy_(self.h_fresh, non_blocking=True)
+        kv.kv8_quant_rows(self.d_fresh, self.kv8[w.T - 1:], self.sc[w.T - 1:], stream=stream)
+        kv.mla_absorb_decode8(self.q_lat, self.q_rope, self.kv8, self.sc, w.T, SM_SCALE(), self.ws, self.out,
+                              stream=stream)
+        self.h_out.copy_(self.out, non_blocking=True)
+
+    def config(self):
+        return {"H": self.w.H, "T": self.w.T, "P": getattr(self, "P", None)}
+
+    # ---- the oracle on a bounded sample: n_heads of the H heads over all T rows
+    def oracle_setup(self, n_heads):
+        import oracle
+        import synth
+        w = self.w
+        q_o, s_o = oracle.quant_rows(self.rows)       # cache bytes from the oracle's own quantizer
+        ql, qr = synth.queries_for(w, 1)
+        heads = np.linspace(0, w.H - 1, n_heads).astype(int)
+        self._o = (q_o, s_o, np.ascontiguousarray(ql[0][heads]), np.ascontiguousarray(qr[0][heads]))
+        self._scale = w.H / n_heads
+        return (f"{n_heads} of {w.H} heads over all T={w.T} rows (+ the fresh-row quantization), "
+                f"scaled x{w.H // n_heads} to one layer-step")
+
+    def oracle_step(self) -> float:
+        import oracle
+        q_o, s_o, ql, qr = self._o
+        t0 = time.perf_counter()
+        oracle.quant_rows(self.rows[-1:])
+        oracle.attn_decode(ql, qr, q_o, s_o, SM_SCALE())
+        return (time.perf_counter() - t0) * self._scale
+
+
+class SelectCase(Case):
+    launches_per_step = 3  # query prep + partial + merge
+    kernel_calls = "mla_absorb_sel8: query prep + attn_tc_kernel (row gather) + log-sum-exp merge"
+    step_desc = "mla_absorb_sel8 over B=8 sequences: query prep + gathered-row partial + log-sum-exp merge"
+
+    def __init__(self, kv, torch, dev, w):
+        import synth
+        self.kv, self.torch, self.w = kv, torch, w
+        B, H, T, NS = w.B, w.H, w.T, w.NS
+        self.kv8 = torch.empty((B * T, 576), dtype=torch.uint8, device=dev)
+        self.sc = torch.empty(B * T, dtype=torch.float32, device=dev)
+        chunk = 65536
+        for b in range(B):
+            for start in range(0, T, chunk):
+                x = torch.from_numpy(synth.rows_for(w, b, start, chunk)).to(dev)
+                r0 = b * T + start
+                kv.kv8_quant_rows(x, self.kv8[r0:r0 + chunk], self.sc[r0:r0 + chunk])
+        torch.cuda.synchronize(dev)
+        self.idx_np = synth.selection_for(w)
+        self.idx = torch.from_numpy(self.idx_np).to(dev)
+        ql, qr = synth.queries_for(w)
+        self.q_lat, self.q_rope = _bf16(torch, dev, ql), _bf16(torch, dev, qr)
+        self.ws = torch.empty(kv.mla_sel8_workspace_bytes(B, H, NS) // 4, dtype=torch.float32, device=dev)
+        self.out = torch.empty((B, H, 512), dtype=torch.float32, device=dev)
+        self.h_q_lat = self.q_lat.cpu().pin_memory()
+        self.h_q_rope = self.q_rope.cpu().pin_memory()
+        self.h_idx = self.idx.cpu().pin_memory()
+        self.h_out = torch.empty((B, H, 512), dtype=torch.float32).pin_memory()
+        self.h2d = self.h_q_lat.numel() * 2 + self.h_q_rope.numel() * 2 + self.h_idx.numel() * 4
+        self.d2h = self.h_out.numel() * 4
+        # listed rows (576 bytes + scale each), the index lists, the queries and the output
+        self.alg_bytes = B * NS * (ROW_BYTES + 4) + self.q_lat.numel() * 2 + self.q_rope.numel() * 2 + \
+            self.out.numel() * 4
+        self.alg_bytes_step = self.alg_bytes
+        self.flops = float(FLOP_PER_ROW_HEAD) * H * B * NS
+
+    def _sel(self, stream):
+        w = self.w
+        self.kv.mla_absorb_sel8(self.q_lat, self.q_rope, self.kv8, self.sc, w.T, w.T, self.idx, SM_SCALE(), self.ws,
+                                self.out, stream=stream)
+
+    def step(self, stream, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        self._sel(stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def e2e_step(self, stream):
+        self.q_lat.copy_(self.h_q_lat, non_blocking=True)
+        self.q_rope.copy_(self.h_q_rope, non_blocking=True)
+        self.idx.copy_(self.h_idx, non_blocking=True)
+        self._sel(stream)
+        self.h_out.copy_(self.out, non_blocking=True)
+
+    def config(self):
+        w = self.w
+        return {"B": w.B, "H": w.H, "T": w.T, "NS": w.NS}
+
+    def oracle_setup(self, n_heads):
+        import oracle
+        import synth
+        w = self.w
+        rows = np.concatenate([synth.rows_for(w, b, 0, w.T)[self.idx_np[b]] for b in range(w.B)])
+        q_o, s_o = oracle.quant_rows(rows)            # only the listed rows: index i of sequence b -> b*NS + i
+        ql, qr = synth.queries_for(w)
+        heads = np.linspace(0, w.H - 1, n_heads).astype(int)
+        idx_local = np.tile(np.arange(w.NS, dtype=np.int32), (w.B, 1))
+        self._o = (q_o, s_o, np.ascontiguousarray(ql[:, heads]), np.ascontiguousarray(qr[:, heads]), idx_local)
+        self._scale = w.H / n_heads
+        return (f"{n_heads} of {w.H} heads of all B={w.B} sequences over their NS={w.NS} listed rows, "
+                f"scaled x{w.H // n_heads} to one step")
+
+    def oracle_step(self) -> float:
+        import oracle
+        q_o, s_o, ql, qr, idx_local = self._o
+        t0 = time.perf_counter()
+        oracle.attn_select(ql, qr, q_o, s_o, self.w.NS, self.w.NS, idx_local, SM_SCALE())
+        return (time.perf_counter() - t0) * self._scale
+
+
+class PrefillCase(Case):
+    unit = "us/chunk"
+    launches_per_step = 2  # quant of the chunk's rows + prefill
+    kernel_calls = "mla_absorb_prefill8: attn_tc_kernel"
+    step_desc = "kv8_quant_rows(1024 fresh rows) + causal prefill of 1024 queries"
+
+    def __init__(self, kv, torch, dev, w):
+        import synth
+        self.kv, self.torch, self.w = kv, torch, w
+        H, T, S, pos0 = w.H, w.T, w.S, w.pos0
+        self.kv8 = torch.empty((T, 576), dtype=torch.uint8, device=dev)
+        self.sc = torch.empty(T, dtype=torch.float32, device=dev)
+        x = torch.from_numpy(synth.rows_for(w)).to(dev)
+        kv.kv8_quant_rows(x[:pos0], self.kv8[:pos0], self.sc[:pos0])   # the resident prefix
+        self.fresh = x[pos0:].clone()                                   # the chunk's rows
+        del x
+        ql, qr = synth.queries_for(w)
+        self.q_lat, self.q_rope = _bf16(torch, dev, ql), _bf16(torch, dev, qr)
+        self.out = torch.empty((S, H, 512), dtype=torch.float32, device=dev)
+        self.h_q_lat = self.q_lat.cpu().pin_memory()
+        self.h_q_rope = self.q_rope.cpu().pin_memory()
+        self.h_fresh = self.fresh.cpu().pin_memory()
+        self.h_out = torch.empty((S, H, 512), dtype=torch.float32).pin_memory()
+        self.d_fresh = torch.empty_like(self.fresh)
+        self.h2d = self.h_q_lat.numel() * 2 + self.h_q_rope.numel() * 2 + self.h_fresh.numel() * 4
+        self.d2h = self.h_out.numel() * 4
+        self.alg_bytes = T * ROW_BYTES + self.q_lat.numel() * 2 + self.q_rope.numel() * 2 + self.out.numel() * 4
+        self.alg_bytes_step = self.alg_bytes + self.fresh.numel() * 4 + S * ROW_BYTES
+        n_pairs = S * pos0 + S * (S + 1) // 2           # (query, row) pairs under the causal mask
+        self.flops = float(FLOP_PER_ROW_HEAD) * H * n_pairs
+
+    def step(self, stream, ev=None):
+        kv, w = self.kv, self.w
+        kv.kv8_quant_rows(self.fresh, self.kv8[w.pos0:], self.sc[w.pos0:], stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        kv.mla_absorb_prefill8(self.q_lat, self.q_rope, w.pos0, self.kv8, self.sc, w.T, SM_SCALE(), self.out,
+                               stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def e2e_step(self, stream):
+        kv, w = self.kv, self.w
+        self.q_lat.copy_(self.h_q_lat, non_blocking=True)
+        self.q_rope.copy_(self.h_q_rope, non_blocking=True)
+        self.d_fresh.copy_(self.h_fresh, non_blocking=True)
+        kv.kv8_quant_rows(self.d_fresh, self.kv8[w.pos0:], self.sc[w.pos0:], stream=stream)
+        kv.mla_absorb_prefill8(self.q_lat, self.q_rope, w.pos0, self.kv8, self.sc, w.T, SM_SCALE(), self.out,
+                               stream=stream)
+        self.h_out.copy_(self.out, non_blocking=True)
+
+    def config(self):
+        w = self.w
+        return {"S": w.S, "H": w.H, "T": w.T, "pos0": w.pos0}
+
+    def oracle_setup(self, n_heads):
+        import oracle
+        import synth
+        w = self.w
+        rows = synth.rows_for(w)
+        q_o, s_o = oracle.quant_rows(rows)
+        ql, qr = synth.queries_for(w)
+        nq = 2
+        qsel = np.array([0, w.S - 1])[:nq]                # the first and last query of the chunk
+        heads = np.linspace(0, w.H - 1, n_heads).astype(int)
+        self._o = (q_o, s_o, [np.ascontiguousarray(ql[i][heads]) for i in qsel],
+                   [np.ascontiguousarray(qr[i][heads]) for i in qsel], [w.pos0 + int(i) + 1 for i in qsel])
+        n_pairs = w.S * w.pos0 + w.S * (w.S + 1) // 2
+        self._scale = (w.H / n_heads) * n_pairs / sum(self._o[4])
+        return (f"{n_heads} of {w.H} heads of the chunk's first and last query ({sum(self._o[4])} causal rows), "
+                f"scaled by (query, row, head) triples to the whole chunk")
+
+    def oracle_step(self) -> float:
+        import oracle
+        q_o, s_o, qls, qrs, lens = self._o
+        t0 = time.perf_counter()
+        for ql, qr, n in zip(qls, qrs, lens):
+            oracle.attn_decode(ql, qr, q_o[:n], s_o[:n], SM_SCALE())
+        return (time.perf_counter() - t0) * self._scale
+
+
+CASES = {"dec262k": DecodeCase, "dec16k": DecodeCase, "dsa": SelectCase, "prefill": PrefillCase}
+ORACLE_HEADS = {"dec262k": 32, "dec16k": 128, "dsa": 128, "prefill": 8}
+REFERENCE_HEADS = {"dec262k": 8, "dec16k": 32, "dsa": 32, "prefill": 4}
+
+
+def SM_SCALE():
     import synth
-    rows = synth.rows_for(w)
-    x = torch.from_numpy(rows).to(dev)
-    kv8 = torch.empty((w.T, 576), dtype=torch.uint8, device=dev)
-    sc = torch.empty(w.T, dtype=torch.float32, device=dev)
-    kv.kv8_quant_rows(x[:-1], kv8, sc)            # the resident cache: rows 0..T-2
-    fresh = x[-1:].clone()                        # this step's new row
-    del x
-    ql, qr = synth.queries_for(w, 1)
-    q_lat = torch.from_numpy(ql[0]).to(dev).to(torch.bfloat16)
-    q_rope = torch.from_numpy(qr[0]).to(dev).to(torch.bfloat16)
-    return rows, kv8, sc, fresh, q_lat, q_rope
+    return synth.SM_SCALE
+
+
+def metric_for(key: str) -> str:
+    if key == "dec262k":
+        return HEADLINE_METRIC
+    import synth
+    return f"fp8 MLA {key} step time ({synth.DESCRIPTIONS[key]})"
 
 
 # --------------------------------------------------------------------------------------------------
 # CPU baseline: the oracle as it stands, on a bounded sample of the workload
 # --------------------------------------------------------------------------------------------------
-def oracle_decode_sample(rows, w, n_heads: int):
+def cpu_baseline(case: Case, n_heads: int) -> dict:
     import oracle
+    sample = case.oracle_setup(n_heads)
+    t_us = case.oracle_step() * 1e6
+    return {"value": t_us, "unit": case.unit, "cores": oracle.num_threads(), "kind": "oracle", "sample": sample}
+
+
+def host_case(key: str):
     import synth
-    q_o, s_o = oracle.quant_rows(rows)            # cache bytes from the oracle's own quantizer
-    ql, qr = synth.queries_for(w, 1)
-    heads = np.linspace(0, w.H - 1, n_heads).astype(int)
-    ql_s, qr_s = np.ascontiguousarray(ql[0][heads]), np.ascontiguousarray(qr[0][heads])
-    return q_o, s_o, ql_s, qr_s
-
-
-def time_oracle_step(q_o, s_o, ql_s, qr_s, fresh_row, w) -> float:
-    import oracle
-    import synth
-    t0 = time.perf_counter()
-    oracle.quant_rows(fresh_row)                  # the step's fresh row
-    oracle.attn_decode(ql_s, qr_s, q_o, s_o, synth.SM_SCALE)
-    return time.perf_counter() - t0
-
-
-def cpu_baseline(rows, w, n_heads: int = 32, repeats: int = 1) -> dict:
-    import oracle
-    q_o, s_o, ql_s, qr_s = oracle_decode_sample(rows, w, n_heads)
-    ts = [time_oracle_step(q_o, s_o, ql_s, qr_s, rows[-1:], w) for _ in range(repeats)]
-    t = min(ts)
-    us = t * 1e6 * w.H / n_heads
-    return {"value": us, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{n_heads} of {w.H} heads over all T={w.T} rows (+ the fresh-row quantization), "
-                      f"timed {t:.2f} s wall, scaled x{w.H // n_heads} to one layer-step"}
+    w = synth.WORKLOADS[key]
+    c = CASES[key].__new__(CASES[key])
+    c.w = w
+    if key in ("dec262k", "dec16k"):
+        c.rows = synth.rows_for(w)
+    elif key == "dsa":
+        c.idx_np = synth.selection_for(w)
+    return c
 
 
 # --------------------------------------------------------------------------------------------------
@@ -224,25 +475,23 @@ def run_reference(args, rank, world):
         return
     import oracle
     oracle.build()
-    w = synth.WORKLOADS[KEY]
-    rows = synth.rows_for(w)
-    n_heads = 8
-    q_o, s_o, ql_s, qr_s = oracle_decode_sample(rows, w, n_heads)
+    key = args.workload
+    case = host_case(key)
+    sample = case.oracle_setup(REFERENCE_HEADS[key])
     for _ in range(args.warmup):
-        time_oracle_step(q_o, s_o, ql_s, qr_s, rows[-1:], w)
+        case.oracle_step()
     t0 = time.perf_counter()
-    ts = [time_oracle_step(q_o, s_o, ql_s, qr_s, rows[-1:], w) for _ in range(args.steps)]
+    ts = [case.oracle_step() for _ in range(args.steps)]
     wall = time.perf_counter() - t0
-    us = statistics.mean(ts) * 1e6 * w.H / n_heads
-    sample = f"{n_heads} of {w.H} heads over all T={w.T} rows per step, scaled x{w.H // n_heads}"
-    line = {"impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": args.gpus,
+    us = statistics.mean(ts) * 1e6
+    cfg = dict({"workload": synth.DESCRIPTIONS[key], "sample": sample}, **case.config())
+    line = {"impl": "reference", "metric": metric_for(key), "value": us, "unit": case.unit, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1000.0, "higher_is_better": False,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": synth.DESCRIPTIONS[KEY], "H": w.H, "T": w.T, "sample": sample},
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
             "wall_s": wall,
-            "cpu_baseline": {"value": us, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "cpu_baseline": {"value": us, "unit": case.unit, "cores": oracle.num_threads(), "kind": "oracle",
                              "sample": sample},
-            "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "e2e": {"value": us, "unit": case.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
     print(json.dumps(line), flush=True)
 
@@ -260,36 +509,22 @@ def run_ours(args, rank, world, local_rank):
     kv.load()
     dev = torch.device(f"cuda:{local_rank}")
     torch.cuda.set_device(dev)
-    w = synth.WORKLOADS[KEY]
-    H, T = w.H, w.T
-    rows, kv8, sc, fresh, q_lat, q_rope = build_decode_inputs(kv, torch, dev, w)
-    P = kv.mla_decode8_partitions(H, T)
-    ws = torch.empty(kv.mla_decode8_workspace_bytes(H, T) // 4, dtype=torch.float32, device=dev)
-    out = torch.empty((H, 512), dtype=torch.float32, device=dev)
+    key = args.workload
+    w = synth.WORKLOADS[key]
+    case = CASES[key](kv, torch, dev, w)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
-    sm_scale = synth.SM_SCALE
-    launches_per_step = 3  # quant + partial + merge
-
-    def step(ev=None):
-        kv.kv8_quant_rows(fresh, kv8[T - 1:], sc[T - 1:], stream=stream)
-        if ev is not None:
-            ev[0].record(stream)
-        kv.mla_decode8_partial(q_lat, q_rope, kv8, sc, T, sm_scale, ws, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-        kv.mla_lse_merge8(ws, 1, P, H, out, stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(max(args.warmup, 3)):
             flush.zero_()
-            step()
+            case.step(stream)
     torch.cuda.synchronize(dev)
 
     # ---- device-timed steps (inputs resident), L2 flushed before each step outside the events
     E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     step_ev = [(E(), E()) for _ in range(args.steps)]
-    part_ev = [(E(), E()) for _ in range(args.steps)]
+    kern_ev = [(E(), E()) for _ in range(args.steps)]
     clocks = ClockSampler(local_rank)
     if rank == 0:
         clocks.start()
@@ -300,38 +535,22 @@ def run_ours(args, rank, world, local_rank):
         for k in range(args.steps):
             flush.zero_()
             step_ev[k][0].record(stream)
-            step(part_ev[k])
+            case.step(stream, kern_ev[k])
             step_ev[k][1].record(stream)
     torch.cuda.synchronize(dev)
     barrier()
     wall_s = time.perf_counter() - t_wall
     clk = clocks.stop() if rank == 0 else {}
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
-    part_ms = [a.elapsed_time(b) for a, b in part_ev]
+    kern_ms = [a.elapsed_time(b) for a, b in kern_ev]
     ms_per_step = reduce_max(statistics.mean(step_ms), dev)
-    part_ms_mean = reduce_max(statistics.mean(part_ms), dev)
+    kern_ms_mean = reduce_max(statistics.mean(kern_ms), dev)
 
-    # ---- end to end through the C ABI with host buffers: q and the fresh row in, context out
-    h_q_lat = q_lat.cpu().pin_memory()
-    h_q_rope = q_rope.cpu().pin_memory()
-    h_fresh = fresh.cpu().pin_memory()
-    h_out = torch.empty((H, 512), dtype=torch.float32).pin_memory()
-    d_fresh = torch.empty_like(fresh)
-    h2d = h_q_lat.numel() * 2 + h_q_rope.numel() * 2 + h_fresh.numel() * 4
-    d2h = h_out.numel() * 4
-
-    def e2e_step():
-        q_lat.copy_(h_q_lat, non_blocking=True)
-        q_rope.copy_(h_q_rope, non_blocking=True)
-        d_fresh.copy_(h_fresh, non_blocking=True)
-        kv.kv8_quant_rows(d_fresh, kv8[T - 1:], sc[T - 1:], stream=stream)
-        kv.mla_absorb_decode8(q_lat, q_rope, kv8, sc, T, sm_scale, ws, out, stream=stream)
-        h_out.copy_(out, non_blocking=True)
-
+    # ---- end to end through the C ABI with host buffers: inputs in, output out, every step
     with torch.cuda.stream(stream):
         for _ in range(3):
             flush.zero_()
-            e2e_step()
+            case.e2e_step(stream)
     torch.cuda.synchronize(dev)
     e2e_ev = [(E(), E()) for _ in range(args.steps)]
     barrier()
@@ -339,7 +558,7 @@ def run_ours(args, rank, world, local_rank):
         for k in range(args.steps):
             flush.zero_()
             e2e_ev[k][0].record(stream)
-            e2e_step()
+            case.e2e_step(stream)
             e2e_ev[k][1].record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = reduce_max(statistics.mean([a.elapsed_time(b) for a, b in e2e_ev]), dev)
@@ -348,51 +567,36 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return
     peaks = measured_peaks()
-    alg_bytes_partial = T * ROW_BYTES + q_lat.numel() * 2 + q_rope.numel() * 2
-    alg_bytes_step = T * ROW_BYTES + h2d + d2h
-    flops = float(FLOP_PER_ROW_HEAD) * H * T
-    part_s = part_ms_mean / 1e3
-    hbm_gbs = alg_bytes_partial / part_s / 1e9
-    if DECODE_BOUND == "alu":
-        peak = alu_peak_tflops(clk.get("sm_max_mhz"))
-        roof = {"bound": "alu", "achieved": flops / part_s / 1e12, "peak": peak, "unit": "TFLOP/s",
-                "peak_source": "derived: 152 SMs x 128 f32 FMA lanes x 2 flop x max SM clock"}
-    elif DECODE_BOUND == "tensor":
-        # the contraction is e4m3 x e4m3: its peak is the measured bf16 burst peak x 2 (nominal fp8/bf16 ratio)
-        peak = peaks["bf16_tflops"] * 2.0
-        roof = {"bound": "tensor", "achieved": flops / part_s / 1e12, "peak": peak, "unit": "TFLOP/s",
-                "peak_source": f"fp8 = 2 x bf16 burst ({peaks['source']})",
-                "mma_tflops_issued": MMA_PIECES * flops / part_s / 1e12,
-                "mma_frac": MMA_PIECES * flops / part_s / 1e12 / peak,
-                "bf16_equiv_frac": flops / part_s / 1e12 / peaks["bf16_tflops"]}
-    else:
-        peak = peaks["hbm_gbs"]
-        roof = {"bound": "hbm", "achieved": hbm_gbs, "peak": peak, "unit": "GB/s",
-                "peak_source": f"HBM copy, {peaks['source']}"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = traffic_per_launch()
-    roof["kernel"] = DECODE_KERNEL
-    roof["algorithmic_bytes"] = alg_bytes_partial
-    roof["algorithmic_flops"] = flops
-    roof["kernel_us"] = part_ms_mean * 1e3
-    roof["hbm_gbs"] = hbm_gbs
-    roof["hbm_frac"] = hbm_gbs / peaks["hbm_gbs"]
+    kern_s = kern_ms_mean / 1e3
+    hbm_gbs = case.alg_bytes / kern_s / 1e9
+    # the contraction is e4m3 x e4m3: its peak is the measured bf16 burst peak x 2 (nominal fp8/bf16 ratio)
+    peak = peaks["bf16_tflops"] * 2.0
+    achieved = case.flops / kern_s / 1e12
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "peak_source": f"fp8 = 2 x bf16 burst ({peaks['source']})",
+            "traffic": traffic_per_launch(key), "kernel": TC_KERNEL, "events_bracket": case.kernel_calls,
+            "mma_tflops_issued": MMA_PIECES * achieved, "mma_frac": MMA_PIECES * achieved / peak,
+            "bf16_equiv_frac": achieved / peaks["bf16_tflops"],
+            "algorithmic_bytes": case.alg_bytes, "algorithmic_flops": case.flops, "kernel_us": kern_ms_mean * 1e3,
+            "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / peaks["hbm_gbs"], "hbm_peak_gbs": peaks["hbm_gbs"]}
 
-    base = cpu_baseline(rows, w) if (world == 1 and not args.no_cpu_baseline) else None
+    n_heads = ORACLE_HEADS[key]
+    base = cpu_baseline(case, n_heads) if (world == 1 and not args.no_cpu_baseline) else None
     value = whole_job_us_per_step(ms_per_step, world)
+    cfg = {"workload": synth.DESCRIPTIONS[key]}
+    cfg.update(case.config())
+    cfg.update({"step": case.step_desc,
+                "l2": f"flushed ({L2_FLUSH_BYTES >> 20} MiB write) before every timed step, outside the events",
+                "parallelism": f"replicas x{world}"})
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": metric_for(key), "value": value, "unit": case.unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": False, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3*e4m3->f32" if DECODE_BOUND == "tensor" else "f32", "data": "synthetic",
-        "config": {"workload": synth.DESCRIPTIONS[KEY], "H": H, "T": T, "P": P,
-                   "step": "kv8_quant_rows(1 fresh row) + split-T partial + log-sum-exp merge",
-                   "l2": f"flushed ({L2_FLUSH_BYTES >> 20} MiB write) before every timed step, outside the events",
-                   "parallelism": f"replicas x{world}"},
-        "step_hbm_gbs": alg_bytes_step / (ms_per_step / 1e3) / 1e9,
-        "step_hbm_frac": alg_bytes_step / (ms_per_step / 1e3) / 1e9 / peaks["hbm_gbs"],
-        "e2e": {"value": whole_job_us_per_step(e2e_ms, world), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches_per_step * args.steps,
+        "vs_baseline": None, "dtype": "e4m3*e4m3->f32", "data": "synthetic", "config": cfg,
+        "step_hbm_gbs": case.alg_bytes_step / (ms_per_step / 1e3) / 1e9,
+        "step_hbm_frac": case.alg_bytes_step / (ms_per_step / 1e3) / 1e9 / peaks["hbm_gbs"],
+        "e2e": {"value": whole_job_us_per_step(e2e_ms, world), "unit": case.unit, "h2d_bytes_per_step": case.h2d,
+                "d2h_bytes_per_step": case.d2h},
+        "gpu_launches": case.launches_per_step * args.steps,
         "roofline": roof,
         "clocks": {k: clk.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples", "power_w_max")},
         "wall_s_timed_region": wall_s,
@@ -409,6 +613,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
+    ap.add_argument("--workload", choices=sorted(CASES), default="dec262k",
+                    help="dec262k (default: the headline decode step), dec16k, dsa or prefill")
     args = ap.parse_args(argv)
     rank, world, local_rank = dist_env()
     if world > 1:
