@@ -51,11 +51,12 @@ constexpr uint32_t kRcOff = 65536;     // rope block inside an image / stage
 constexpr uint32_t OFF_Q = 0, OFF_ST0 = kImg, OFF_ST1 = 2 * kImg, OFF_PLO = 3 * kImg, OFF_MISC = 3 * kImg + 8192;
 constexpr float kTau = 2.0f;           // lazy-rescale threshold (log2 units): p <= 2^kTau
 constexpr float kWScale = 64.0f;       // 2^(8 - kTau): keeps w <= 256 < 448 (e4m3 max)
-constexpr float kMStart = -1e30f;      // running max before any valid row (log2 units)
 
 struct Misc {
-    // per-head arrays first: they are read with 16-byte vector loads
-    alignas(16) float m_run[2][kHeadsPerCta];  // running max per head; which copy is current flips on a rescale
+    // per-head arrays first: they are read with 16-byte vector loads.  m_run / m_ref have two copies;
+    // which one is current flips on a rescale.
+    alignas(16) float m_run[2][kHeadsPerCta];  // running max per head (log2 units), -inf before any valid row
+    alignas(16) float m_ref[2][kHeadsPerCta];  // the weights' reference: m_run, or 0 while that is -inf
     alignas(16) float c_head[kHeadsPerCta];    // sm_scale * log2(e) * 2^-e_h per head (0 for padding heads)
     alignas(16) float red[4][kHeadsPerCta];    // per-quadrant tile maxima / row sums
     union alignas(16) Phase {                  // storage that is never live in two phases at once
@@ -63,19 +64,21 @@ struct Misc {
             int qmax_bits[kHeadsPerCta];       // prologue: per-head max |q| (bits of a non-negative float)
             float wred[2][16];                 // prologue: per-warp maxima
         } pro;
-        float alpha[8][32];                    // tile loop: per softmax warp, rescale factors of its heads
+        struct {
+            float alpha[2][32];                // tile loop, per head half: rescale factors 2^(m_old - m_new)
+            float delta[2][32];                // and the reference shifts m_ref_old - m_ref_new
+        } tile;
         float zsum[kHeadsPerCta];              // epilogue: row sums per head
     } ph;
-    uint64_t kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, pv_done, sync_bar[2], final_bar, q_full;
+    uint64_t kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, pv_done, final_bar, q_full;
     uint64_t kv_blk[2][4];  // latent block kb of a stage has been read by the context product
     uint32_t tmem_base;
     int abort_flag;
-    int vote[2][2];  // [head half][tile parity]
     float w_mul;     // kWScale / s_ref
     float out_mul;   // s_ref / kWScale
 };
-static_assert(OFF_MISC % 16 == 0 && offsetof(Misc, m_run) % 16 == 0 && offsetof(Misc, red) % 16 == 0 &&
-                  offsetof(Misc, ph) % 16 == 0 && offsetof(Misc, c_head) % 16 == 0,
+static_assert(OFF_MISC % 16 == 0 && offsetof(Misc, m_run) % 16 == 0 && offsetof(Misc, m_ref) % 16 == 0 &&
+                  offsetof(Misc, red) % 16 == 0 && offsetof(Misc, ph) % 16 == 0 && offsetof(Misc, c_head) % 16 == 0,
               "vector accesses need 16-byte alignment");
 static_assert(offsetof(Misc, kv_full) % 8 == 0, "mbarriers need 8-byte alignment");
 constexpr uint32_t kSmemBytes = OFF_MISC + sizeof(Misc);
@@ -143,17 +146,26 @@ __device__ __forceinline__ void split_pair_h(float a, float b, uint32_t &hi, uin
     lo = l8;
 }
 
-// Bounded barrier among the 256 softmax threads (an mbarrier, so a missing thread cannot hang it).
-struct SoftSync {
-    uint64_t *bar;
-    volatile int *abort_flag;
-    int *err;
-    uint32_t n = 0;
-    __device__ bool operator()() {
-        mbar_arrive(bar);
-        return mbar_wait(bar, (n++) & 1u, abort_flag, err);
-    }
-};
+// Named barrier over `count` threads that also ORs a predicate across them.
+__device__ __forceinline__ bool bar_red_or(int id, int count, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+// 2^x by the hardware approximation (MUFU.EX2; subnormal results flush to 0, 2^-inf = 0)
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 // 10 warps: a sub-partition holding 3 warps caps a thread at 168 registers (16K registers each).
 __global__ void __launch_bounds__(kThreads, 1)
@@ -184,12 +196,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kb = 0; kb < 4; ++kb) mbar_init(&ms.kv_blk[s][kb], 1);
             mbar_init(&ms.s_full[s], 1);
             mbar_init(&ms.s_free[s], kSoftmaxThreads);
-            ms.vote[0][s] = ms.vote[1][s] = 0;
         }
         mbar_init(&ms.p_full, kSoftmaxThreads);
         mbar_init(&ms.pv_done, 1);
-        mbar_init(&ms.sync_bar[0], kSoftmaxThreads / 2);
-        mbar_init(&ms.sync_bar[1], kSoftmaxThreads / 2);
         mbar_init(&ms.final_bar, 1);
         mbar_init(&ms.q_full, 1);
         ms.abort_flag = 0;
@@ -386,9 +395,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ms.c_head[pt] = hg < a.H ? a.sm_scale_log2 * (qmax > 0.f ? ldexpf(1.f, E - 8) : 1.f) : 0.f;
             }
         }
-        // a finite start: weights 2^(s - m) of masked rows (s = -inf) are 0, never NaN, even while a
-        // head has seen no valid row
-        if (pt < kHeadsPerCta) ms.m_run[0][pt] = ms.m_run[1][pt] = kMStart;
+        if (pt < kHeadsPerCta) {
+            ms.m_run[0][pt] = ms.m_run[1][pt] = -INFINITY;
+            ms.m_ref[0][pt] = ms.m_ref[1][pt] = 0.f;
+        }
         if (pt == 0) {
             const float s_ref = fmaxf(smax, 1e-30f);
             ms.w_mul = kWScale / s_ref;
@@ -400,23 +410,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == 1) {
             // ================================ MMA issuer ================================
             if (lane == 0) {
-                const uint32_t id_s = idesc_e4m3_f32(128, 128, false, false);
+                const uint32_t id_s = idesc_e4m3_f32(128, 64, false, false);
                 const uint32_t id_pv = idesc_e4m3_f32(128, 64, true, true);
                 const uint32_t qb = sbase + OFF_Q;
                 auto issue_score = [&](int i) {
                     const int s = i & 1;
                     const uint32_t st = sbase + (s ? OFF_ST1 : OFF_ST0);
-                    const uint32_t d = tmem + (uint32_t)s * 128u;
+                    // S^T = K8 Q_hi^T + K8 Q_lo^T, both pieces into the same 64 columns (the lo rows of
+                    // the query image start 64 rows = 8 KB into each latent block, 4 KB into the rope block)
+                    const uint32_t d = tmem + (uint32_t)s * 64u;
 #pragma unroll
-                    for (int kb = 0; kb < 4; ++kb)
+                    for (int pc = 0; pc < 2; ++pc) {
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_f8f6f4(d, smem_desc(st + kb * 16384 + kk * 32, 0, 1024, kSw128),
-                                       smem_desc(qb + kb * 16384 + kk * 32, 0, 1024, kSw128), id_s, (kb | kk) != 0);
+                        for (int kb = 0; kb < 4; ++kb)
 #pragma unroll
-                    for (int kk = 0; kk < 2; ++kk)
-                        mma_f8f6f4(d, smem_desc(st + kRcOff + kk * 32, 0, 512, kSw64),
-                                   smem_desc(qb + kRcOff + kk * 32, 0, 512, kSw64), id_s, 1);
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_f8f6f4(d, smem_desc(st + kb * 16384 + kk * 32, 0, 1024, kSw128),
+                                           smem_desc(qb + kb * 16384 + pc * 8192 + kk * 32, 0, 1024, kSw128), id_s,
+                                           (pc | kb | kk) != 0);
+#pragma unroll
+                        for (int kk = 0; kk < 2; ++kk)
+                            mma_f8f6f4(d, smem_desc(st + kRcOff + kk * 32, 0, 512, kSw64),
+                                       smem_desc(qb + kRcOff + pc * 4096 + kk * 32, 0, 512, kSw64), id_s, 1);
+                    }
                     mma_commit(&ms.s_full[s]);
                 };
                 auto issue_pv = [&](int j) {
@@ -446,14 +462,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint64_t t_last = t_start;
                 uint32_t spins = 0;
                 while (np < n_tiles) {
-                    if (np < ns && mbar_try_wait(&ms.p_full, np & 1)) {
+                    if (np < ns && mbar_test_wait(&ms.p_full, np & 1)) {
                         tc_fence_after_sync();
                         issue_pv(np++);
                         spins = 0;
                         continue;
                     }
-                    if (ns < n_tiles && mbar_try_wait(&ms.kv_full[ns & 1], (ns >> 1) & 1) &&
-                        (ns < 2 || mbar_try_wait(&ms.s_free[ns & 1], ((ns >> 1) - 1) & 1))) {
+                    if (ns < n_tiles && mbar_test_wait(&ms.kv_full[ns & 1], (ns >> 1) & 1) &&
+                        (ns < 2 || mbar_test_wait(&ms.s_free[ns & 1], ((ns >> 1) - 1) & 1))) {
                         tc_fence_after_sync();
                         issue_score(ns++);
                         spins = 0;
@@ -479,12 +495,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
         } else {
             // ============================ softmax + epilogue ============================
+            // Each thread owns one tile row (TMEM lane) and the 32 heads of its head half.  The four
+            // warps of a head half decide and rescale together through named barrier 2 + hh.  A wait
+            // that gives up clears `ok`; the thread then skips its remaining waits but still reaches
+            // every named barrier of every tile, so the other warps never wait for it.
             const int q = warp & 3;               // TMEM lane quadrant
             const int hh = (warp - 2) >> 2;       // which 32 of the CTA's 64 heads
             const int r = q * 32 + lane;          // row within the tile = TMEM lane
             const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-            // the two head halves (4 warps each) decide and rescale independently
-            SoftSync sync{&ms.sync_bar[hh], &ms.abort_flag, a.err_word};
+            const int bar_id = 2 + hh;
             const float w_mul = ms.w_mul;
             float z[32];
 #pragma unroll
@@ -504,49 +523,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             float sc_next = n_tiles > 0 ? row_scale(t0 + r) : -1.f;
             bool ok = true;
-            int cur = 0;  // which ms.m_run copy is current (uniform across the softmax threads)
-            for (int i = 0; i < n_tiles && ok; ++i) {
+            bool seen = false;  // some valid row has been scored: every head's running max is finite
+            int cur = 0;        // which copy of ms.m_run / ms.m_ref is current (uniform across the half)
+            for (int i = 0; i < n_tiles; ++i) {
                 const int bb = i & 1;
                 const int64_t t = t0 + (int64_t)i * kTile + r;
                 const float sc_t = sc_next;
                 const bool valid = sc_t >= 0.f;
                 sc_next = i + 1 < n_tiles ? row_scale(t + kTile) : -1.f;
 
-                if (!(ok = mbar_wait(&ms.s_full[bb], (i >> 1) & 1, &ms.abort_flag, a.err_word))) break;
+                if (ok) ok = mbar_wait(&ms.s_full[bb], (i >> 1) & 1, &ms.abort_flag, a.err_word);
                 tc_fence_after_sync();
-                float s[32];
-#pragma unroll
-                for (int k2 = 0; k2 < 2; ++k2) {
-                    uint32_t shi[16], slo[16];
-                    tmem_ld_32x32b_x16(tmem + lane_addr + (uint32_t)bb * 128u + 32u * hh + 16u * k2, shi);
-                    tmem_ld_32x32b_x16(tmem + lane_addr + (uint32_t)bb * 128u + 64u + 32u * hh + 16u * k2, slo);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) s[16 * k2 + j] = __uint_as_float(shi[j]) + __uint_as_float(slo[j]);
-                }
-#pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    const float4 c4 = *reinterpret_cast<const float4 *>(&ms.c_head[32 * hh + 4 * j4]);
-                    s[4 * j4 + 0] = valid ? s[4 * j4 + 0] * (c4.x * sc_t) : -INFINITY;
-                    s[4 * j4 + 1] = valid ? s[4 * j4 + 1] * (c4.y * sc_t) : -INFINITY;
-                    s[4 * j4 + 2] = valid ? s[4 * j4 + 2] * (c4.z * sc_t) : -INFINITY;
-                    s[4 * j4 + 3] = valid ? s[4 * j4 + 3] * (c4.w * sc_t) : -INFINITY;
-                }
+                uint32_t sr[32];
+                tmem_ld_32x32b_x16(tmem + lane_addr + (uint32_t)bb * 64u + 32u * hh, *reinterpret_cast<uint32_t(*)[16]>(sr));
+                tmem_ld_32x32b_x16(tmem + lane_addr + (uint32_t)bb * 64u + 32u * hh + 16u,
+                                   *reinterpret_cast<uint32_t(*)[16]>(sr + 16));
+                tmem_wait_ld();
                 tc_fence_before_sync();
                 mbar_arrive(&ms.s_free[bb]);
 
-                // lazy rescale check: does any score exceed its head's running max by more than kTau?
-                const float *mrow = &ms.m_run[cur][32 * hh];
-                bool need = false;
+                // d = s - ref with s = S * sm_scale*log2(e)*2^-e_h * s_t (one FMA per score); ref is the
+                // running max, or 0 before any valid row
+                float d[32];
+                float dmax = -INFINITY;
+                const float *mref = &ms.m_ref[cur][32 * hh];
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
-                    const float4 m4 = *reinterpret_cast<const float4 *>(mrow + 4 * j4);
-                    need |= (s[4 * j4 + 0] > m4.x + kTau) | (s[4 * j4 + 1] > m4.y + kTau) |
-                            (s[4 * j4 + 2] > m4.z + kTau) | (s[4 * j4 + 3] > m4.w + kTau);
+                    const float4 c4 = *reinterpret_cast<const float4 *>(&ms.c_head[32 * hh + 4 * j4]);
+                    const float4 r4 = *reinterpret_cast<const float4 *>(mref + 4 * j4);
+                    d[4 * j4 + 0] = fmaf(__uint_as_float(sr[4 * j4 + 0]), c4.x * sc_t, -r4.x);
+                    d[4 * j4 + 1] = fmaf(__uint_as_float(sr[4 * j4 + 1]), c4.y * sc_t, -r4.y);
+                    d[4 * j4 + 2] = fmaf(__uint_as_float(sr[4 * j4 + 2]), c4.z * sc_t, -r4.z);
+                    d[4 * j4 + 3] = fmaf(__uint_as_float(sr[4 * j4 + 3]), c4.w * sc_t, -r4.w);
+                    dmax = fmaxf(dmax, fmaxf(fmaxf(d[4 * j4 + 0], d[4 * j4 + 1]), fmaxf(d[4 * j4 + 2], d[4 * j4 + 3])));
                 }
-                if (need) ms.vote[hh][bb] = i + 1;
-                if (!(ok = sync())) break;
-                const bool slow = ms.vote[hh][bb] == i + 1;
+                if (!valid) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) d[j] = -INFINITY;
+                    dmax = -INFINITY;
+                }
+                // lazy rescale: the half takes the slow path when some score exceeds its head's running
+                // max by more than kTau, or while no valid row has been seen
+                const bool slow = bar_red_or(bar_id, 128, dmax > kTau || !seen);
                 bool any_alpha = false;
                 if (slow) {
                     // tile max per head over this warp's 32 rows: butterfly transpose-reduction.  At
@@ -554,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // max with the other half from lane ^ k; after 5 steps lane l holds head l's max.
                     float v[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = s[j];
+                    for (int j = 0; j < 32; ++j) v[j] = d[j];
 #pragma unroll
                     for (int k = 16; k >= 1; k >>= 1) {
                         const bool upper = (lane & k) != 0;
@@ -565,50 +583,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                             v[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, k));
                         }
                     }
-                    ms.red[q][32 * hh + lane] = v[0];
-                    if (!(ok = sync())) break;
-                    // every quadrant warp combines the four quadrant maxima of its heads itself
-                    float *mnext = &ms.m_run[cur ^ 1][32 * hh];
-                    float *al = ms.ph.alpha[warp - 2];
+                    const int hj = 32 * hh + lane;  // lane l now speaks for head l of the half
+                    ms.red[q][hj] = v[0];
+                    named_sync(bar_id, 128);
+                    const float ref_o = ms.m_ref[cur][hj], mo = ms.m_run[cur][hj];
+                    const float tmax = fmaxf(fmaxf(ms.red[0][hj], ms.red[1][hj]), fmaxf(ms.red[2][hj], ms.red[3][hj])) + ref_o;
+                    const float mn = mo == -INFINITY ? tmax : (tmax > mo + kTau ? tmax : mo);
+                    const float al = (mo == -INFINITY || mn == mo) ? 1.f : ex2_approx(mo - mn);
+                    const float ref_n = mn == -INFINITY ? 0.f : mn;
+                    // the four quadrant warps write the same values
+                    ms.m_run[cur ^ 1][hj] = mn;
+                    ms.m_ref[cur ^ 1][hj] = ref_n;
+                    ms.ph.tile.alpha[hh][lane] = al;
+                    ms.ph.tile.delta[hh][lane] = ref_o - ref_n;
+                    seen = __shfl_sync(0xffffffffu, mn, 0) != -INFINITY;  // the same for every head
+                    any_alpha = __any_sync(0xffffffffu, al != 1.f);
+                    __syncwarp();
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4) {
-                        const float4 r0 = *reinterpret_cast<const float4 *>(&ms.red[0][32 * hh + 4 * j4]);
-                        const float4 r1 = *reinterpret_cast<const float4 *>(&ms.red[1][32 * hh + 4 * j4]);
-                        const float4 r2 = *reinterpret_cast<const float4 *>(&ms.red[2][32 * hh + 4 * j4]);
-                        const float4 r3 = *reinterpret_cast<const float4 *>(&ms.red[3][32 * hh + 4 * j4]);
-                        const float4 mo = *reinterpret_cast<const float4 *>(mrow + 4 * j4);
-                        const float t0 = fmaxf(fmaxf(r0.x, r1.x), fmaxf(r2.x, r3.x));
-                        const float t1 = fmaxf(fmaxf(r0.y, r1.y), fmaxf(r2.y, r3.y));
-                        const float t2 = fmaxf(fmaxf(r0.z, r1.z), fmaxf(r2.z, r3.z));
-                        const float t3 = fmaxf(fmaxf(r0.w, r1.w), fmaxf(r2.w, r3.w));
-                        const float4 mn = make_float4(t0 > mo.x + kTau ? t0 : mo.x, t1 > mo.y + kTau ? t1 : mo.y,
-                                                      t2 > mo.z + kTau ? t2 : mo.z, t3 > mo.w + kTau ? t3 : mo.w);
-                        const float4 a4 = make_float4(mn.x == mo.x ? 1.f : exp2f(mo.x - mn.x),
-                                                      mn.y == mo.y ? 1.f : exp2f(mo.y - mn.y),
-                                                      mn.z == mo.z ? 1.f : exp2f(mo.z - mn.z),
-                                                      mn.w == mo.w ? 1.f : exp2f(mo.w - mn.w));
-                        if (lane == 0) {
-                            *reinterpret_cast<float4 *>(mnext + 4 * j4) = mn;  // the same values from all 4 quadrants
-                            *reinterpret_cast<float4 *>(al + 4 * j4) = a4;
-                        }
+                        const float4 a4 = *reinterpret_cast<const float4 *>(&ms.ph.tile.alpha[hh][4 * j4]);
+                        const float4 e4 = *reinterpret_cast<const float4 *>(&ms.ph.tile.delta[hh][4 * j4]);
+                        d[4 * j4 + 0] += e4.x;
+                        d[4 * j4 + 1] += e4.y;
+                        d[4 * j4 + 2] += e4.z;
+                        d[4 * j4 + 3] += e4.w;
                         z[4 * j4 + 0] *= a4.x;
                         z[4 * j4 + 1] *= a4.y;
                         z[4 * j4 + 2] *= a4.z;
                         z[4 * j4 + 3] *= a4.w;
-                        any_alpha |= (a4.x != 1.f) | (a4.y != 1.f) | (a4.z != 1.f) | (a4.w != 1.f);
                     }
-                    __syncwarp();
                     cur ^= 1;
-                    mrow = &ms.m_run[cur][32 * hh];
                 }
-                // weights: p = 2^(s - m) (row sum z), w = p * s_t * kWScale / s_ref, split e4m3 hi + lo
+                // weights: p = 2^d (row sum z), w = p * s_t * kWScale / s_ref, split e4m3 hi + lo
                 const float g = valid ? sc_t * w_mul : 0.f;
                 uint32_t whi[8], wlo[8];
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
-                    const float4 m4 = *reinterpret_cast<const float4 *>(mrow + 4 * j4);
-                    const float p0 = exp2f(s[4 * j4 + 0] - m4.x), p1 = exp2f(s[4 * j4 + 1] - m4.y);
-                    const float p2 = exp2f(s[4 * j4 + 2] - m4.z), p3 = exp2f(s[4 * j4 + 3] - m4.w);
+                    const float p0 = ex2_approx(d[4 * j4 + 0]), p1 = ex2_approx(d[4 * j4 + 1]);
+                    const float p2 = ex2_approx(d[4 * j4 + 2]), p3 = ex2_approx(d[4 * j4 + 3]);
                     z[4 * j4 + 0] += p0;
                     z[4 * j4 + 1] += p1;
                     z[4 * j4 + 2] += p2;
@@ -626,26 +638,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (i >= 1) {
                     // the previous context product must be done before its weights' lo buffer is reused
                     // and before its accumulators are rescaled
-                    if (!(ok = mbar_wait(&ms.pv_done, (i - 1) & 1, &ms.abort_flag, a.err_word))) break;
+                    if (ok) ok = mbar_wait(&ms.pv_done, (i - 1) & 1, &ms.abort_flag, a.err_word);
                     if (any_alpha) {
-                        // rescale only the changed heads' columns of the four context accumulators
+                        // rescale this half's columns of the four context accumulators
                         tc_fence_after_sync();
-                        const float *al = ms.ph.alpha[warp - 2];
-                        uint32_t changed = 0;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) changed |= (al[j] != 1.f ? 1u : 0u) << j;
-                        while (changed) {
-                            const int j = __ffs(changed) - 1;
-                            changed &= changed - 1;
-                            const float aj = al[j];
-                            const uint32_t ta = tmem + lane_addr + 256u + 32u * hh + (uint32_t)j;
-                            const uint32_t v0 = tmem_ld_32x32b_x1(ta), v1 = tmem_ld_32x32b_x1(ta + 64u);
-                            const uint32_t v2 = tmem_ld_32x32b_x1(ta + 128u), v3 = tmem_ld_32x32b_x1(ta + 192u);
+#pragma unroll 1
+                        for (int c = 0; c < 8; ++c) {
+                            const uint32_t ta = tmem + lane_addr + 256u + 64u * (c >> 1) + 32u * hh + 16u * (c & 1);
+                            uint32_t o[16];
+                            tmem_ld_32x32b_x16(ta, o);
                             tmem_wait_ld();
-                            tmem_st_32x32b_x1(ta, __float_as_uint(__uint_as_float(v0) * aj));
-                            tmem_st_32x32b_x1(ta + 64u, __float_as_uint(__uint_as_float(v1) * aj));
-                            tmem_st_32x32b_x1(ta + 128u, __float_as_uint(__uint_as_float(v2) * aj));
-                            tmem_st_32x32b_x1(ta + 192u, __float_as_uint(__uint_as_float(v3) * aj));
+                            const float *al = &ms.ph.tile.alpha[hh][16 * (c & 1)];
+#pragma unroll
+                            for (int j4 = 0; j4 < 4; ++j4) {
+                                const float4 a4 = *reinterpret_cast<const float4 *>(al + 4 * j4);
+                                o[4 * j4 + 0] = __float_as_uint(__uint_as_float(o[4 * j4 + 0]) * a4.x);
+                                o[4 * j4 + 1] = __float_as_uint(__uint_as_float(o[4 * j4 + 1]) * a4.y);
+                                o[4 * j4 + 2] = __float_as_uint(__uint_as_float(o[4 * j4 + 2]) * a4.z);
+                                o[4 * j4 + 3] = __float_as_uint(__uint_as_float(o[4 * j4 + 3]) * a4.w);
+                            }
+                            tmem_st_32x32b_x16(ta, o);
                         }
                         tmem_wait_st();
                     }
@@ -673,14 +685,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == j) zmine = v;
             }
             ms.red[q][32 * hh + lane] = zmine;
-            if (ok) ok = sync();
-            if (ok) {
-                if (q == 0) {
-                    const int h = 32 * hh + lane;
-                    ms.ph.zsum[h] = ms.red[0][h] + ms.red[1][h] + ms.red[2][h] + ms.red[3][h];
-                }
-                ok = sync();
+            named_sync(bar_id, 128);
+            if (q == 0) {
+                const int h = 32 * hh + lane;
+                ms.ph.zsum[h] = ms.red[0][h] + ms.red[1][h] + ms.red[2][h] + ms.red[3][h];
             }
+            named_sync(bar_id, 128);
             if (ok) {
                 const float out_mul = ms.out_mul;
                 const int hbase = half * kHeadsPerCta + 32 * hh;
@@ -695,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int j = 0; j < 16; ++j) o[j] = 0u;
                     }
-                    const int d = 128 * (ch >> 1) + r;
+                    const int dd = 128 * (ch >> 1) + r;
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int hl = 32 * hh + 16 * (ch & 1) + j;  // head within the CTA
@@ -703,20 +713,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (hg >= a.H) continue;
                         const float v = __uint_as_float(o[j]) * out_mul;
                         if (a.ws) {
-                            pv.cl[(((int64_t)b * a.P + part) * a.H + hg) * kKL + d] = v;
+                            pv.cl[(((int64_t)b * a.P + part) * a.H + hg) * kKL + dd] = v;
                         } else {
                             const float zz = ms.ph.zsum[hl];
-                            a.out[((int64_t)b * a.H + hg) * kKL + d] = zz > 0.f ? v / zz : 0.f;
+                            a.out[((int64_t)b * a.H + hg) * kKL + dd] = zz > 0.f ? v / zz : 0.f;
                         }
                     }
                 }
                 if (a.ws && q == 0) {
                     const int hg = hbase + lane;
                     if (hg < a.H) {
-                        const int64_t idx = ((int64_t)b * a.P + part) * a.H + hg;
-                        const float mh = ms.m_run[cur][32 * hh + lane];
-                        pv.m[idx] = (n_tiles > 0 && mh > kMStart) ? mh : -INFINITY;  // -inf: no valid row
-                        pv.z[idx] = ms.ph.zsum[32 * hh + lane];
+                        const int64_t pidx = ((int64_t)b * a.P + part) * a.H + hg;
+                        pv.m[pidx] = n_tiles > 0 ? ms.m_run[cur][32 * hh + lane] : -INFINITY;  // -inf: no valid row
+                        pv.z[pidx] = ms.ph.zsum[32 * hh + lane];
                     }
                 }
             }

@@ -58,6 +58,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 
 // Wait for the phase with the given parity to complete, giving up after `limit_ns`.  On a timeout it
 // sets KV8_ERR_TIMEOUT in *err (if given) and *abort_flag (shared), and returns false.
+// Non-blocking test of the phase with the given parity (for a thread that polls several barriers).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *err,
                                           uint64_t limit_ns = 2000000000ull) {
     if (mbar_try_wait(bar, parity)) return true;
