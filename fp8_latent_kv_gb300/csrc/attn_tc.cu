@@ -24,7 +24,8 @@
 // Warps: 0 = TMA producer, 1 = MMA issuer (and TMEM owner), 2..9 = softmax / epilogue.
 // Shared memory (231 KB): query image 72 KB, two 72 KB row stages (the weights' hi piece reuses the
 // stage's rope block once the score has read it), weights' lo piece 8 KB, barriers and scratch.
-// TMEM (512 columns): two 128-column score buffers, four 64-column context accumulators.
+// TMEM (512 columns): two 128-column score buffers (hi / lo query pieces side by side), four 64-column
+// context accumulators.
 // Every wait is an mbarrier wait bounded in time; a timeout sets KV8_ERR_TIMEOUT and the CTA winds
 // down without hanging.
 #include "internal.h"
@@ -49,6 +50,7 @@ constexpr int kPrepThreads = 288;      // warps 1..9
 constexpr uint32_t kImg = 73728;       // 4 x 16 KB (SW128, 128 B per row) + 8 KB (SW64, 64 B per row)
 constexpr uint32_t kRcOff = 65536;     // rope block inside an image / stage
 constexpr uint32_t OFF_Q = 0, OFF_ST0 = kImg, OFF_ST1 = 2 * kImg, OFF_PLO = 3 * kImg, OFF_MISC = 3 * kImg + 8192;
+constexpr int kPrefetch = 2;           // dense rows: L2 prefetch distance in tiles
 constexpr float kTau = 2.0f;           // lazy-rescale threshold (log2 units): p <= 2^kTau
 constexpr float kWScale = 64.0f;       // 2^(8 - kTau): keeps w <= 256 < 448 (e4m3 max)
 
@@ -246,6 +248,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // implies tile i-2's phase of it has completed (one arrival per phase).
                     if (lane == 0) {
                         const int y = (int)p0;
+                        // start pulling tile i + kPrefetch into L2: the loads of a two-stage ring are
+                        // issued only a tile ahead, too late to cover the memory latency on their own
+                        if (p0 + kPrefetch * kTile < t1) {
+                            const int yp = y + kPrefetch * kTile;
+#pragma unroll
+                            for (int kb = 0; kb < 4; ++kb) tma_prefetch_l2_2d(&map_lc, kb * 128, yp);
+                            tma_prefetch_l2_2d(&map_rc, 512, yp);
+                        }
                         for (int kb = 0; kb < 4 && ok_p; ++kb) {
                             if (i >= 2 && !(ok_p = mbar_wait(&ms.kv_blk[s][kb], ph, &ms.abort_flag, a.err_word))) break;
                             if (kb == 0) {
@@ -410,29 +420,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == 1) {
             // ================================ MMA issuer ================================
             if (lane == 0) {
-                const uint32_t id_s = idesc_e4m3_f32(128, 64, false, false);
+                const uint32_t id_s = idesc_e4m3_f32(128, 128, false, false);
                 const uint32_t id_pv = idesc_e4m3_f32(128, 64, true, true);
                 const uint32_t qb = sbase + OFF_Q;
                 auto issue_score = [&](int i) {
                     const int s = i & 1;
                     const uint32_t st = sbase + (s ? OFF_ST1 : OFF_ST0);
-                    // S^T = K8 Q_hi^T + K8 Q_lo^T, both pieces into the same 64 columns (the lo rows of
-                    // the query image start 64 rows = 8 KB into each latent block, 4 KB into the rope block)
-                    const uint32_t d = tmem + (uint32_t)s * 64u;
+                    // S^T = K8 [Q_hi; Q_lo]^T in one N = 128 pass: columns 0..63 hold the hi piece's
+                    // scores, 64..127 the lo piece's (one pass reads the rows once; two N = 64 passes
+                    // into one accumulator take about 60% longer on the tensor cores)
+                    const uint32_t d = tmem + (uint32_t)s * 128u;
 #pragma unroll
-                    for (int pc = 0; pc < 2; ++pc) {
+                    for (int kb = 0; kb < 4; ++kb)
 #pragma unroll
-                        for (int kb = 0; kb < 4; ++kb)
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_f8f6f4(d, smem_desc(st + kb * 16384 + kk * 32, 0, 1024, kSw128),
+                                       smem_desc(qb + kb * 16384 + kk * 32, 0, 1024, kSw128), id_s, (kb | kk) != 0);
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                mma_f8f6f4(d, smem_desc(st + kb * 16384 + kk * 32, 0, 1024, kSw128),
-                                           smem_desc(qb + kb * 16384 + pc * 8192 + kk * 32, 0, 1024, kSw128), id_s,
-                                           (pc | kb | kk) != 0);
-#pragma unroll
-                        for (int kk = 0; kk < 2; ++kk)
-                            mma_f8f6f4(d, smem_desc(st + kRcOff + kk * 32, 0, 512, kSw64),
-                                       smem_desc(qb + kRcOff + pc * 4096 + kk * 32, 0, 512, kSw64), id_s, 1);
-                    }
+                    for (int kk = 0; kk < 2; ++kk)
+                        mma_f8f6f4(d, smem_desc(st + kRcOff + kk * 32, 0, 512, kSw64),
+                                   smem_desc(qb + kRcOff + kk * 32, 0, 512, kSw64), id_s, 1);
                     mma_commit(&ms.s_full[s]);
                 };
                 auto issue_pv = [&](int j) {
@@ -534,11 +541,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 if (ok) ok = mbar_wait(&ms.s_full[bb], (i >> 1) & 1, &ms.abort_flag, a.err_word);
                 tc_fence_after_sync();
-                uint32_t sr[32];
-                tmem_ld_32x32b_x16(tmem + lane_addr + (uint32_t)bb * 64u + 32u * hh, *reinterpret_cast<uint32_t(*)[16]>(sr));
-                tmem_ld_32x32b_x16(tmem + lane_addr + (uint32_t)bb * 64u + 32u * hh + 16u,
-                                   *reinterpret_cast<uint32_t(*)[16]>(sr + 16));
-                tmem_wait_ld();
+                float sc_[32];  // S = hi piece + lo piece
+#pragma unroll
+                for (int k2 = 0; k2 < 2; ++k2) {
+                    uint32_t shi[16], slo[16];
+                    const uint32_t ta = tmem + lane_addr + (uint32_t)bb * 128u + 32u * hh + 16u * k2;
+                    tmem_ld_32x32b_x16(ta, shi);
+                    tmem_ld_32x32b_x16(ta + 64u, slo);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) sc_[16 * k2 + j] = __uint_as_float(shi[j]) + __uint_as_float(slo[j]);
+                }
                 tc_fence_before_sync();
                 mbar_arrive(&ms.s_free[bb]);
 
@@ -551,10 +564,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j4 = 0; j4 < 8; ++j4) {
                     const float4 c4 = *reinterpret_cast<const float4 *>(&ms.c_head[32 * hh + 4 * j4]);
                     const float4 r4 = *reinterpret_cast<const float4 *>(mref + 4 * j4);
-                    d[4 * j4 + 0] = fmaf(__uint_as_float(sr[4 * j4 + 0]), c4.x * sc_t, -r4.x);
-                    d[4 * j4 + 1] = fmaf(__uint_as_float(sr[4 * j4 + 1]), c4.y * sc_t, -r4.y);
-                    d[4 * j4 + 2] = fmaf(__uint_as_float(sr[4 * j4 + 2]), c4.z * sc_t, -r4.z);
-                    d[4 * j4 + 3] = fmaf(__uint_as_float(sr[4 * j4 + 3]), c4.w * sc_t, -r4.w);
+                    d[4 * j4 + 0] = fmaf(sc_[4 * j4 + 0], c4.x * sc_t, -r4.x);
+                    d[4 * j4 + 1] = fmaf(sc_[4 * j4 + 1], c4.y * sc_t, -r4.y);
+                    d[4 * j4 + 2] = fmaf(sc_[4 * j4 + 2], c4.z * sc_t, -r4.z);
+                    d[4 * j4 + 3] = fmaf(sc_[4 * j4 + 3], c4.w * sc_t, -r4.w);
                     dmax = fmaxf(dmax, fmaxf(fmaxf(d[4 * j4 + 0], d[4 * j4 + 1]), fmaxf(d[4 * j4 + 2], d[4 * j4 + 3])));
                 }
                 if (!valid) {
@@ -643,21 +656,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // rescale this half's columns of the four context accumulators
                         tc_fence_after_sync();
 #pragma unroll 1
-                        for (int c = 0; c < 8; ++c) {
-                            const uint32_t ta = tmem + lane_addr + 256u + 64u * (c >> 1) + 32u * hh + 16u * (c & 1);
-                            uint32_t o[16];
-                            tmem_ld_32x32b_x16(ta, o);
+                        for (int c = 0; c < 4; ++c) {
+                            const uint32_t ta = tmem + lane_addr + 256u + 64u * c + 32u * hh;
+                            uint32_t o[32];
+                            tmem_ld_32x32b_x16(ta, *reinterpret_cast<uint32_t(*)[16]>(o));
+                            tmem_ld_32x32b_x16(ta + 16u, *reinterpret_cast<uint32_t(*)[16]>(o + 16));
                             tmem_wait_ld();
-                            const float *al = &ms.ph.tile.alpha[hh][16 * (c & 1)];
+                            const float *al = ms.ph.tile.alpha[hh];
 #pragma unroll
-                            for (int j4 = 0; j4 < 4; ++j4) {
+                            for (int j4 = 0; j4 < 8; ++j4) {
                                 const float4 a4 = *reinterpret_cast<const float4 *>(al + 4 * j4);
                                 o[4 * j4 + 0] = __float_as_uint(__uint_as_float(o[4 * j4 + 0]) * a4.x);
                                 o[4 * j4 + 1] = __float_as_uint(__uint_as_float(o[4 * j4 + 1]) * a4.y);
                                 o[4 * j4 + 2] = __float_as_uint(__uint_as_float(o[4 * j4 + 2]) * a4.z);
                                 o[4 * j4 + 3] = __float_as_uint(__uint_as_float(o[4 * j4 + 3]) * a4.w);
                             }
-                            tmem_st_32x32b_x16(ta, o);
+                            tmem_st_32x32b_x16(ta, *reinterpret_cast<const uint32_t(*)[16]>(o));
+                            tmem_st_32x32b_x16(ta + 16u, *reinterpret_cast<const uint32_t(*)[16]>(o + 16));
                         }
                         tmem_wait_st();
                     }
