@@ -218,10 +218,54 @@ __global__ void __launch_bounds__(kThreads, 1) attn_simt_kernel(AttnArgs a) {
     }
 }
 
-// Log-sum-exp merge: block (h, quarter, b) -- 128 threads, one latent column each.  Warp 0 turns
-// the P partition maxima into weights 2^(m_p - M) in shared memory; then every thread sums its column
-// over the partitions with independent loads in flight.
-constexpr int kMergeMaxP = 1024;  // weights kept in shared memory; larger P loops over slices
+// Log-sum-exp merge: block (h, quarter, b) -- 128 threads, one latent column each.
+//
+// Small P (<= kMergeFast): every load the block needs is issued before any result is used -- each
+// thread's P partial columns, and each warp's own copy of the P maxima and row sums -- so the
+// partials' latency is paid about once.  Each warp turns the maxima into weights 2^(m_p - M) itself
+// (lane p % 32 holds partition p's) and every thread sums its column.
+constexpr int kMergeFast = 128;
+constexpr int kMergeMaxP = 1024;  // larger P: weights kept in shared memory, loops over slices
+
+template <int NP>
+__device__ __forceinline__ void merge_small(const PartialView &pv, int64_t base, int P, int H, int d, float *out) {
+    const int lane = threadIdx.x & 31;
+    const float *cl = pv.cl + base * kKL + d;
+    const int64_t pstride = (int64_t)H * kKL;
+    float c[NP];
+#pragma unroll
+    for (int u = 0; u < NP; ++u) c[u] = u < P ? cl[(int64_t)u * pstride] : 0.f;
+    constexpr int K = NP / 32;
+    float mv[K], zv[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int p = lane + 32 * k;
+        mv[k] = p < P ? pv.m[base + (int64_t)p * H] : -INFINITY;
+        zv[k] = p < P ? pv.z[base + (int64_t)p * H] : 0.f;
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < K; ++k) M = fmaxf(M, mv[k]);
+    M = warp_max(M);
+    float wv[K], Z = 0.f;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        wv[k] = (mv[k] == -INFINITY || M == -INFINITY) ? 0.f : exp2f(mv[k] - M);
+        Z = fmaf(wv[k], zv[k], Z);
+    }
+    Z = warp_sum(Z);
+    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+    for (int u = 0; u < NP; ++u) {
+        const float w = __shfl_sync(0xffffffffu, wv[u >> 5], u & 31);
+        // a partition with weight 0 may hold anything (it attended no row): do not touch its values
+        if (w != 0.f) {
+            if (u & 1) acc1 = fmaf(w, c[u], acc1);
+            else acc0 = fmaf(w, c[u], acc0);
+        }
+    }
+    *out = Z > 0.f ? (acc0 + acc1) / Z : 0.f;
+}
 
 __global__ void __launch_bounds__(128) lse_merge_kernel(const float *__restrict__ ws, int B, int P, int H,
                                                         float *__restrict__ out) {
@@ -232,7 +276,12 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const float *__restrict_
     const int h = blockIdx.x, quarter = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
     PartialView pv(const_cast<float *>(ws), B, P, H);
     const int64_t base = (int64_t)b * P * H + h;
-    // global max over partitions (every thread; P is small and the values are L2-resident)
+    const int d = quarter * 128 + tid;
+    float *o = out + ((int64_t)b * H + h) * kKL + d;
+    if (P <= 32) return merge_small<32>(pv, base, P, H, d, o);
+    if (P <= 64) return merge_small<64>(pv, base, P, H, d, o);
+    if (P <= kMergeFast) return merge_small<kMergeFast>(pv, base, P, H, d, o);
+    // large P: warp 0 turns the maxima into weights in shared memory
     float M = -INFINITY;
     if (tid < 32) {
         for (int p = tid; p < P; p += 32) M = fmaxf(M, pv.m[base + (int64_t)p * H]);
@@ -248,23 +297,25 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const float *__restrict_
         if (tid == 0) zsh = Z;
     }
     __syncthreads();
-    const int d = quarter * 128 + tid;
     const float *cl = pv.cl + base * kKL + d;
     const int64_t pstride = (int64_t)H * kKL;
     float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
     const int pw = P < kMergeMaxP ? P : kMergeMaxP;
-    int p = 0;
-    for (; p + 4 <= pw; p += 4) {
-        const float c0 = cl[(int64_t)(p + 0) * pstride], c1 = cl[(int64_t)(p + 1) * pstride];
-        const float c2 = cl[(int64_t)(p + 2) * pstride], c3 = cl[(int64_t)(p + 3) * pstride];
-        // a partition with weight 0 may hold anything (it attended no row): do not touch its values
-        if (wsh[p + 0] != 0.f) acc0 = fmaf(wsh[p + 0], c0, acc0);
-        if (wsh[p + 1] != 0.f) acc1 = fmaf(wsh[p + 1], c1, acc1);
-        if (wsh[p + 2] != 0.f) acc2 = fmaf(wsh[p + 2], c2, acc2);
-        if (wsh[p + 3] != 0.f) acc3 = fmaf(wsh[p + 3], c3, acc3);
+    // rounds of kBatch independent loads (one per partition)
+    constexpr int kBatch = 32;
+    for (int p0 = 0; p0 < pw; p0 += kBatch) {
+        float c[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) c[u] = p0 + u < pw ? cl[(int64_t)(p0 + u) * pstride] : 0.f;
+#pragma unroll
+        for (int u = 0; u < kBatch; u += 4) {
+            const int q = p0 + u;
+            if (q + 0 < pw && wsh[q + 0] != 0.f) acc0 = fmaf(wsh[q + 0], c[u + 0], acc0);
+            if (q + 1 < pw && wsh[q + 1] != 0.f) acc1 = fmaf(wsh[q + 1], c[u + 1], acc1);
+            if (q + 2 < pw && wsh[q + 2] != 0.f) acc2 = fmaf(wsh[q + 2], c[u + 2], acc2);
+            if (q + 3 < pw && wsh[q + 3] != 0.f) acc3 = fmaf(wsh[q + 3], c[u + 3], acc3);
+        }
     }
-    for (; p < pw; ++p)
-        if (wsh[p] != 0.f) acc0 = fmaf(wsh[p], cl[(int64_t)p * pstride], acc0);
     // partitions beyond the shared-memory slice (P > kMergeMaxP): weights recomputed on the fly
     if (P > kMergeMaxP) {
         float Mx = -INFINITY;
@@ -277,7 +328,7 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const float *__restrict_
     }
     const float Z = zsh;
     const float inv = Z > 0.f ? 1.f / Z : 0.f;
-    out[((int64_t)b * H + h) * kKL + d] = ((acc0 + acc1) + (acc2 + acc3)) * inv;
+    *o = ((acc0 + acc1) + (acc2 + acc3)) * inv;
 }
 
 }  // namespace
