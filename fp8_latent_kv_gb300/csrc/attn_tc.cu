@@ -50,7 +50,6 @@ constexpr int kPrepThreads = 288;      // warps 1..9
 constexpr uint32_t kImg = 73728;       // 4 x 16 KB (SW128, 128 B per row) + 8 KB (SW64, 64 B per row)
 constexpr uint32_t kRcOff = 65536;     // rope block inside an image / stage
 constexpr uint32_t OFF_Q = 0, OFF_ST0 = kImg, OFF_ST1 = 2 * kImg, OFF_PLO = 3 * kImg, OFF_MISC = 3 * kImg + 8192;
-constexpr int kPrefetch = 2;           // dense rows: L2 prefetch distance in tiles
 constexpr float kTau = 2.0f;           // lazy-rescale threshold (log2 units): p <= 2^kTau
 constexpr float kWScale = 64.0f;       // 2^(8 - kTau): keeps w <= 256 < 448 (e4m3 max)
 
@@ -219,8 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ================================ TMA producer ================================
-        // Lane 0 issues the copies and does the waits; in selection mode the whole warp reads the
-        // tile's 128 row indices (4 per lane) and lane 0 gathers them 4 rows at a time.
+        // Dense rows: lane 0 issues the tile copies and does the waits.  Selection: the whole warp reads
+        // the tile's 128 row indices (4 per lane) and every lane gathers its own 4 rows.
         if (n_tiles > 0) {
             if (lane == 0) {
                 prefetch_tensormap(&map_lc);
@@ -248,14 +247,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // implies tile i-2's phase of it has completed (one arrival per phase).
                     if (lane == 0) {
                         const int y = (int)p0;
-                        // start pulling tile i + kPrefetch into L2: the loads of a two-stage ring are
-                        // issued only a tile ahead, too late to cover the memory latency on their own
-                        if (p0 + kPrefetch * kTile < t1) {
-                            const int yp = y + kPrefetch * kTile;
-#pragma unroll
-                            for (int kb = 0; kb < 4; ++kb) tma_prefetch_l2_2d(&map_lc, kb * 128, yp);
-                            tma_prefetch_l2_2d(&map_rc, 512, yp);
-                        }
                         for (int kb = 0; kb < 4 && ok_p; ++kb) {
                             if (i >= 2 && !(ok_p = mbar_wait(&ms.kv_blk[s][kb], ph, &ms.abort_flag, a.err_word))) break;
                             if (kb == 0) {
