@@ -69,7 +69,10 @@ struct Misc {
             float alpha[2][32];                // tile loop, per head half: rescale factors 2^(m_old - m_new)
             float delta[2][32];                // and the reference shifts m_ref_old - m_ref_new
         } tile;
-        float zsum[kHeadsPerCta];              // epilogue: row sums per head
+        struct {
+            float zsum[kHeadsPerCta];          // epilogue: row sums per head
+            float zinv[kHeadsPerCta];          // and the direct output's factors s_ref / kWScale / zsum
+        } fin;
     } ph;
     uint64_t kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, pv_done, final_bar, q_full;
     uint64_t kv_blk[2][4];  // latent block kb of a stage has been read by the context product
@@ -683,24 +686,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 atomicOr(a.err_word, (int)KV8_ERR_INDEX);
             if (ok && n_tiles > 0) ok = mbar_wait(&ms.pv_done, (n_tiles - 1) & 1, &ms.abort_flag, a.err_word);
             tc_fence_after_sync();
-            // row sums: over the 32 lanes of the warp, then over the 4 quadrants
-            float zmine = 0.f;
+            // row sums per head over the warp's 32 rows: butterfly transpose-reduction (as for the max,
+            // lane l ends with head l's sum), then over the 4 quadrants
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float v = warp_sum(z[j]);
-                if (lane == j) zmine = v;
+            for (int k = 16; k >= 1; k >>= 1) {
+                const bool upper = (lane & k) != 0;
+#pragma unroll
+                for (int j = 0; j < k; ++j) {
+                    const float send = upper ? z[j] : z[j + k];
+                    const float keep = upper ? z[j + k] : z[j];
+                    z[j] = keep + __shfl_xor_sync(0xffffffffu, send, k);
+                }
             }
-            ms.red[q][32 * hh + lane] = zmine;
+            ms.red[q][32 * hh + lane] = z[0];
             named_sync(bar_id, 128);
             if (q == 0) {
                 const int h = 32 * hh + lane;
-                ms.ph.zsum[h] = ms.red[0][h] + ms.red[1][h] + ms.red[2][h] + ms.red[3][h];
+                const float zz = ms.red[0][h] + ms.red[1][h] + ms.red[2][h] + ms.red[3][h];
+                ms.ph.fin.zsum[h] = zz;
+                ms.ph.fin.zinv[h] = zz > 0.f ? ms.out_mul / zz : 0.f;
             }
             named_sync(bar_id, 128);
             if (ok) {
                 const float out_mul = ms.out_mul;
                 const int hbase = half * kHeadsPerCta + 32 * hh;
                 PartialView pv(a.ws, a.B, a.P, a.H);
+                // the 8 column chunks of this thread's row (16 heads each)
 #pragma unroll 1
                 for (int ch = 0; ch < 8; ++ch) {
                     uint32_t o[16];
@@ -717,13 +728,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int hl = 32 * hh + 16 * (ch & 1) + j;  // head within the CTA
                         const int hg = half * kHeadsPerCta + hl;
                         if (hg >= a.H) continue;
-                        const float v = __uint_as_float(o[j]) * out_mul;
-                        if (a.ws) {
-                            pv.cl[(((int64_t)b * a.P + part) * a.H + hg) * kKL + dd] = v;
-                        } else {
-                            const float zz = ms.ph.zsum[hl];
-                            a.out[((int64_t)b * a.H + hg) * kKL + dd] = zz > 0.f ? v / zz : 0.f;
-                        }
+                        if (a.ws)
+                            pv.cl[(((int64_t)b * a.P + part) * a.H + hg) * kKL + dd] = __uint_as_float(o[j]) * out_mul;
+                        else
+                            a.out[((int64_t)b * a.H + hg) * kKL + dd] = __uint_as_float(o[j]) * ms.ph.fin.zinv[hl];
                     }
                 }
                 if (a.ws && q == 0) {
@@ -731,7 +739,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (hg < a.H) {
                         const int64_t pidx = ((int64_t)b * a.P + part) * a.H + hg;
                         pv.m[pidx] = n_tiles > 0 ? ms.m_run[cur][32 * hh + lane] : -INFINITY;  // -inf: no valid row
-                        pv.z[pidx] = ms.ph.zsum[32 * hh + lane];
+                        pv.z[pidx] = ms.ph.fin.zsum[32 * hh + lane];
                     }
                 }
             }
