@@ -74,7 +74,7 @@ struct Misc {
             float zinv[kHeadsPerCta];          // and the direct output's factors s_ref / kWScale / zsum
         } fin;
     } ph;
-    uint64_t kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, pv_done, final_bar, q_full;
+    uint64_t kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, pv_done, plo_free, final_bar, q_full;
     uint64_t kv_blk[2][4];  // latent block kb of a stage has been read by the context product
     uint32_t tmem_base;
     int abort_flag;
@@ -203,6 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&ms.p_full, kSoftmaxThreads);
         mbar_init(&ms.pv_done, 1);
+        mbar_init(&ms.plo_free, 1);
         mbar_init(&ms.final_bar, 1);
         mbar_init(&ms.q_full, 1);
         ms.abort_flag = 0;
@@ -436,19 +437,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    smem_desc(qb + kRcOff + kk * 32, 0, 512, kSw64), id_s, 1);
                     mma_commit(&ms.s_full[s]);
                 };
+                // The weights' lo piece goes first: its buffer is then free for the next tile's softmax
+                // while the hi piece (in the row stage's rope block) is still being read.
                 auto issue_pv = [&](int j) {
                     const int s = j & 1;
                     const uint32_t st = sbase + (s ? OFF_ST1 : OFF_ST0);
                     const uint32_t phi = st + kRcOff, plo = sbase + OFF_PLO;
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        const uint32_t d = tmem + 256u + (uint32_t)ch * 64u;
+                    for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t ad = smem_desc(st + ch * 16384 + kk * 4096, 0, 1024, kSw128);
-                            mma_f8f6f4(d, ad, smem_desc(phi + kk * 2048, 0, 512, kSw64), id_pv, (j | kk) != 0);
-                            mma_f8f6f4(d, ad, smem_desc(plo + kk * 2048, 0, 512, kSw64), id_pv, 1);
-                        }
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_f8f6f4(tmem + 256u + (uint32_t)ch * 64u, smem_desc(st + ch * 16384 + kk * 4096, 0, 1024, kSw128),
+                                       smem_desc(plo + kk * 2048, 0, 512, kSw64), id_pv, (j | kk) != 0);
+                    mma_commit(&ms.plo_free);
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_f8f6f4(tmem + 256u + (uint32_t)ch * 64u, smem_desc(st + ch * 16384 + kk * 4096, 0, 1024, kSw128),
+                                       smem_desc(phi + kk * 2048, 0, 512, kSw64), id_pv, 1);
                         mma_commit(&ms.kv_blk[s][ch]);  // latent block ch may be refilled
                     }
                     mma_commit(&ms.kv_empty[s]);
@@ -643,9 +650,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4 *>(phi + sw64_offset(r, 32 * hh + 16)) =
                     make_uint4(whi[4], whi[5], whi[6], whi[7]);
                 if (i >= 1) {
-                    // the previous context product must be done before its weights' lo buffer is reused
-                    // and before its accumulators are rescaled
-                    if (ok) ok = mbar_wait(&ms.pv_done, (i - 1) & 1, &ms.abort_flag, a.err_word);
+                    // the previous context product must have read its weights' lo piece before the buffer
+                    // is reused, and must be done before its accumulators are rescaled
+                    if (ok) ok = mbar_wait(any_alpha ? &ms.pv_done : &ms.plo_free, (i - 1) & 1, &ms.abort_flag, a.err_word);
                     if (any_alpha) {
                         // rescale this half's columns of the four context accumulators
                         tc_fence_after_sync();
