@@ -366,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float qmax = __int_as_float(ms.ph.pro.qmax_bits[h]);
                 int E = 0;
                 if (qmax > 0.f) frexpf(qmax, &E);
-                const float qmul = qmax > 0.f ? ldexpf(1.f, 8 - E) : 1.f;
+                const int sh = qmax > 0.f ? 8 - E : 0;  // values are scaled, not a 2^sh factor: it may overflow
                 const uint32_t w[8] = {qv[k][0].x, qv[k][0].y, qv[k][0].z, qv[k][0].w,
                                        qv[k][1].x, qv[k][1].y, qv[k][1].z, qv[k][1].w};
                 uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e2 = 0; e2 < 8; ++e2) {
                     const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e2]));
                     uint32_t ph, pl;
-                    split_pair(f.x * qmul, f.y * qmul, ph, pl);
+                    split_pair(ldexpf(f.x, sh), ldexpf(f.y, sh), ph, pl);
                     hi[e2 >> 1] |= ph << ((e2 & 1) * 16);
                     lo[e2 >> 1] |= pl << ((e2 & 1) * 16);
                 }
@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float qmax = __int_as_float(ms.ph.pro.qmax_bits[pt]);
                 int E = 0;
                 if (qmax > 0.f) frexpf(qmax, &E);
-                ms.c_head[pt] = hg < a.H ? a.sm_scale_log2 * (qmax > 0.f ? ldexpf(1.f, E - 8) : 1.f) : 0.f;
+                ms.c_head[pt] = hg < a.H ? (qmax > 0.f ? ldexpf(a.sm_scale_log2, E - 8) : a.sm_scale_log2) : 0.f;
             }
         }
         if (pt < kHeadsPerCta) {
@@ -803,14 +803,14 @@ __global__ void __launch_bounds__(128) tc_prep_kernel(PrepArgs a) {
         mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
         int E = 0;
         if (mx > 0.f) frexpf(mx, &E);
-        const float qmul = mx > 0.f ? ldexpf(1.f, 8 - E) : 1.f;
+        const int sh = mx > 0.f ? 8 - E : 0;  // values are scaled, not a 2^sh factor: it may overflow
         if (tid < 36) {
             uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
                 uint32_t ph, pl;
-                split_pair(f.x * qmul, f.y * qmul, ph, pl);
+                split_pair(ldexpf(f.x, sh), ldexpf(f.y, sh), ph, pl);
                 hi[e >> 1] |= ph << ((e & 1) * 16);
                 lo[e >> 1] |= pl << ((e & 1) * 16);
             }
@@ -828,7 +828,7 @@ __global__ void __launch_bounds__(128) tc_prep_kernel(PrepArgs a) {
             *reinterpret_cast<uint4 *>(dst + off_hi) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
             *reinterpret_cast<uint4 *>(dst + off_lo) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
-        if (tid == 0) a.c_head[bid] = h < a.H ? a.sm_scale_log2 * (mx > 0.f ? ldexpf(1.f, E - 8) : 1.f) : 0.f;
+        if (tid == 0) a.c_head[bid] = h < a.H ? (mx > 0.f ? ldexpf(a.sm_scale_log2, E - 8) : a.sm_scale_log2) : 0.f;
     } else {
         const int bp = bid - a.B * a.n_heads_pad, b = bp / a.P, p = bp - b * a.P;
         const int64_t n_list = a.idx ? (int64_t)a.NS : a.T;

@@ -112,7 +112,8 @@ def _random_case(oracle, T, H, seed, mag=(0.1, 10.0)):
 
 
 @pytest.mark.parametrize("T,H,f32", [(1, 16, True), (1, 128, False), (2, 5, True), (129, 33, False),
-                                     (1000, 1, True), (4097, 128, False), (777, 96, True)])
+                                     (1000, 1, True), (4097, 128, False), (777, 96, True), (777, 96, False),
+                                     (300, 65, False), (2, 1, False)])
 def test_decode_ragged_shapes(lib, oracle, T, H, f32):
     q_o, s_o, q = _random_case(oracle, T, H, seed=T * 131 + H)
     if not f32:
@@ -141,3 +142,29 @@ def test_decode_peaky_and_tiny_magnitudes(lib, oracle):
     got = _decode(lib, _qtensor(ql, False), _qtensor(qr, False), torch.from_numpy(q_o).to(DEV),
                   torch.from_numpy(s_o).to(DEV), T)
     parity(got, oracle.attn_decode(ql, qr, q_o, s_o, synth.SM_SCALE), "peaky")
+
+
+def test_decode_query_magnitudes(lib, oracle):
+    """bf16 query heads whose magnitudes span the bf16 range (the tensor-core path scales each head by a
+    power of two before splitting it into e4m3 pieces), an all-zero head and a one-element head."""
+    rng = np.random.default_rng(91)
+    T, H = 900, 24
+    rows = synth.latent_rows(rng, T, 0.1, 10.0)
+    q_o, s_o = oracle.quant_rows(rows)
+    q = synth.normal_f32(rng, (H, 576)).astype(np.float64)
+    # up to 2^120: larger heads would give scores beyond the f32 range (|s| > 3e38 log2 units)
+    exps = np.array([-130, -126, -100, -60, -20, -5, 0, 3, 10, 20, 40, 60, 80, 100, 120, 110,
+                     -128, -110, -90, -40, 30, 50, 0, 0], dtype=np.float64)
+    q *= np.exp2(exps)[:, None]
+    q[22] = 0.0                       # all-zero head: uniform softmax
+    q[23] = 0.0
+    q[23, 511] = 3.0                  # one latent element
+    q = synth.to_bf16_values(q.astype(np.float32))
+    assert np.all(np.isfinite(q))
+    ql, qr = np.ascontiguousarray(q[:, :512]), np.ascontiguousarray(q[:, 512:])
+    got = _decode(lib, _qtensor(ql, False), _qtensor(qr, False), torch.from_numpy(q_o).to(DEV),
+                  torch.from_numpy(s_o).to(DEV), T)
+    ref = oracle.attn_decode(ql, qr, q_o, s_o, synth.SM_SCALE)
+    assert np.all(np.isfinite(got))
+    for h in range(H):  # each head against its own scale
+        parity(got[h], ref[h], f"head {h} (2^{int(exps[h])})")
