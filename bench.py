@@ -535,22 +535,18 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
 
     # One step is captured once as a CUDA graph and replayed: the same library calls and kernels, without
-    # the host's per-call launch cost (about 12 us per call from Python) between them.  Two events inside
-    # the graph bracket the dominant call.
+    # the host's per-call launch cost (about 12 us per call from Python) between them.  The graph holds
+    # no events: an event node between two calls would cut the programmatic dependent launch that lets
+    # a kernel start while its predecessor drains.  The dominant call is timed from its own graph,
+    # replayed after each step (L2 flushed before each).
     E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    try:  # events that become record nodes of the graph (timed at every replay)
-        k0, k1 = (torch.cuda.Event(enable_timing=True, external=True) for _ in range(2))
-    except TypeError:
-        k0 = k1 = None
     g_step = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_step, stream=stream):
-        case.step(stream, (k0, k1) if k0 is not None else None)
-    g_kern = None
-    if k0 is None:  # no graph-node events: the dominant call alone, as its own graph
-        k0, k1 = E(), E()
-        g_kern = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_kern, stream=stream):
-            case.kernel_call(stream)
+        case.step(stream)
+    k0, k1 = E(), E()
+    g_kern = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_kern, stream=stream):
+        case.kernel_call(stream)
     g_e2e = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_e2e, stream=stream):
         case.e2e_step(stream)
@@ -558,6 +554,7 @@ def run_ours(args, rank, world, local_rank):
         for _ in range(3):
             flush.zero_()
             g_step.replay()
+            g_kern.replay()
             g_e2e.replay()
     torch.cuda.synchronize(dev)
 
@@ -576,11 +573,10 @@ def run_ours(args, rank, world, local_rank):
             e0.record(stream)
             g_step.replay()
             e1.record(stream)
-            if g_kern is not None:
-                flush.zero_()
-                k0.record(stream)
-                g_kern.replay()
-                k1.record(stream)
+            flush.zero_()
+            k0.record(stream)
+            g_kern.replay()
+            k1.record(stream)
         k1.synchronize()
         e1.synchronize()
         step_ms.append(e0.elapsed_time(e1))
