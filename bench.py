@@ -167,6 +167,28 @@ def traffic_per_launch(key: str):
     return d.get("dram_bytes_per_launch")
 
 
+class Packed:
+    """A step's host inputs packed into one pinned buffer, copied with one transfer into one device
+    buffer whose typed views are what the library calls receive (each view 256-byte aligned)."""
+
+    def __init__(self, torch, dev, tensors):
+        offs, o = [], 0
+        for t in tensors:
+            offs.append(o)
+            o += (t.numel() * t.element_size() + 255) // 256 * 256
+        self.host = torch.empty(o, dtype=torch.uint8).pin_memory()
+        self.dev = torch.empty(o, dtype=torch.uint8, device=dev)
+        self.views = []
+        for t, off in zip(tensors, offs):
+            n = t.numel() * t.element_size()
+            self.host[off:off + n].copy_(t.detach().cpu().contiguous().view(-1).view(torch.uint8))
+            self.views.append(self.dev[off:off + n].view(t.dtype).view(t.shape))
+        self.nbytes = sum(t.numel() * t.element_size() for t in tensors)
+
+    def upload(self):
+        self.dev.copy_(self.host, non_blocking=True)
+
+
 def _bf16(torch, dev, a):
     return torch.from_numpy(np.ascontiguousarray(a)).to(dev).to(torch.bfloat16)
 
@@ -207,13 +229,10 @@ class DecodeCase(Case):
         self.P = kv.mla_decode8_partitions(H, T)
         self.ws = torch.empty(kv.mla_decode8_workspace_bytes(H, T) // 4, dtype=torch.float32, device=dev)
         self.out = torch.empty((H, 512), dtype=torch.float32, device=dev)
-        # e2e host buffers
-        self.h_q_lat = self.q_lat.cpu().pin_memory()
-        self.h_q_rope = self.q_rope.cpu().pin_memory()
-        self.h_fresh = self.fresh.cpu().pin_memory()
+        # e2e: the step's inputs (queries, fresh row) in one pinned buffer, one copy per step
+        self.pack = Packed(torch, dev, [self.q_lat, self.q_rope, self.fresh])
         self.h_out = torch.empty((H, 512), dtype=torch.float32).pin_memory()
-        self.d_fresh = torch.empty_like(self.fresh)
-        self.h2d = self.h_q_lat.numel() * 2 + self.h_q_rope.numel() * 2 + self.h_fresh.numel() * 4
+        self.h2d = self.pack.nbytes
         self.d2h = self.h_out.numel() * 4
         self.alg_bytes = T * ROW_BYTES + self.q_lat.numel() * 2 + self.q_rope.numel() * 2
         self.alg_bytes_step = T * ROW_BYTES + self.h2d + self.d2h
@@ -235,12 +254,10 @@ class DecodeCase(Case):
 
     def e2e_step(self, stream):
         kv, w = self.kv, self.w
-        self.q_lat.copy_(self.h_q_lat, non_blocking=True)
-        self.q_rope.copy_(self.h_q_rope, non_blocking=True)
-        self.d_fresh.copy_(self.h_fresh, non_blocking=True)
-        kv.kv8_quant_rows(self.d_fresh, self.kv8[w.T - 1:], self.sc[w.T - 1:], stream=stream)
-        kv.mla_absorb_decode8(self.q_lat, self.q_rope, self.kv8, self.sc, w.T, SM_SCALE(), self.ws, self.out,
-                              stream=stream)
+        self.pack.upload()
+        q_lat, q_rope, fresh = self.pack.views
+        kv.kv8_quant_rows(fresh, self.kv8[w.T - 1:], self.sc[w.T - 1:], stream=stream)
+        kv.mla_absorb_decode8(q_lat, q_rope, self.kv8, self.sc, w.T, SM_SCALE(), self.ws, self.out, stream=stream)
         self.h_out.copy_(self.out, non_blocking=True)
 
     def config(self):
@@ -292,11 +309,9 @@ class SelectCase(Case):
         self.q_lat, self.q_rope = _bf16(torch, dev, ql), _bf16(torch, dev, qr)
         self.ws = torch.empty(kv.mla_sel8_workspace_bytes(B, H, NS) // 4, dtype=torch.float32, device=dev)
         self.out = torch.empty((B, H, 512), dtype=torch.float32, device=dev)
-        self.h_q_lat = self.q_lat.cpu().pin_memory()
-        self.h_q_rope = self.q_rope.cpu().pin_memory()
-        self.h_idx = self.idx.cpu().pin_memory()
+        self.pack = Packed(torch, dev, [self.q_lat, self.q_rope, self.idx])
         self.h_out = torch.empty((B, H, 512), dtype=torch.float32).pin_memory()
-        self.h2d = self.h_q_lat.numel() * 2 + self.h_q_rope.numel() * 2 + self.h_idx.numel() * 4
+        self.h2d = self.pack.nbytes
         self.d2h = self.h_out.numel() * 4
         # listed rows (576 bytes + scale each), the index lists, the queries and the output
         self.alg_bytes = B * NS * (ROW_BYTES + 4) + self.q_lat.numel() * 2 + self.q_rope.numel() * 2 + \
@@ -320,10 +335,11 @@ class SelectCase(Case):
         self._sel(stream)
 
     def e2e_step(self, stream):
-        self.q_lat.copy_(self.h_q_lat, non_blocking=True)
-        self.q_rope.copy_(self.h_q_rope, non_blocking=True)
-        self.idx.copy_(self.h_idx, non_blocking=True)
-        self._sel(stream)
+        w = self.w
+        self.pack.upload()
+        q_lat, q_rope, idx = self.pack.views
+        self.kv.mla_absorb_sel8(q_lat, q_rope, self.kv8, self.sc, w.T, w.T, idx, SM_SCALE(), self.ws, self.out,
+                                stream=stream)
         self.h_out.copy_(self.out, non_blocking=True)
 
     def config(self):
@@ -371,12 +387,9 @@ class PrefillCase(Case):
         ql, qr = synth.queries_for(w)
         self.q_lat, self.q_rope = _bf16(torch, dev, ql), _bf16(torch, dev, qr)
         self.out = torch.empty((S, H, 512), dtype=torch.float32, device=dev)
-        self.h_q_lat = self.q_lat.cpu().pin_memory()
-        self.h_q_rope = self.q_rope.cpu().pin_memory()
-        self.h_fresh = self.fresh.cpu().pin_memory()
+        self.pack = Packed(torch, dev, [self.q_lat, self.q_rope, self.fresh])
         self.h_out = torch.empty((S, H, 512), dtype=torch.float32).pin_memory()
-        self.d_fresh = torch.empty_like(self.fresh)
-        self.h2d = self.h_q_lat.numel() * 2 + self.h_q_rope.numel() * 2 + self.h_fresh.numel() * 4
+        self.h2d = self.pack.nbytes
         self.d2h = self.h_out.numel() * 4
         self.alg_bytes = T * ROW_BYTES + self.q_lat.numel() * 2 + self.q_rope.numel() * 2 + self.out.numel() * 4
         self.alg_bytes_step = self.alg_bytes + self.fresh.numel() * 4 + S * ROW_BYTES
@@ -400,12 +413,10 @@ class PrefillCase(Case):
 
     def e2e_step(self, stream):
         kv, w = self.kv, self.w
-        self.q_lat.copy_(self.h_q_lat, non_blocking=True)
-        self.q_rope.copy_(self.h_q_rope, non_blocking=True)
-        self.d_fresh.copy_(self.h_fresh, non_blocking=True)
-        kv.kv8_quant_rows(self.d_fresh, self.kv8[w.pos0:], self.sc[w.pos0:], stream=stream)
-        kv.mla_absorb_prefill8(self.q_lat, self.q_rope, w.pos0, self.kv8, self.sc, w.T, SM_SCALE(), self.out,
-                               stream=stream)
+        self.pack.upload()
+        q_lat, q_rope, fresh = self.pack.views
+        kv.kv8_quant_rows(fresh, self.kv8[w.pos0:], self.sc[w.pos0:], stream=stream)
+        kv.mla_absorb_prefill8(q_lat, q_rope, w.pos0, self.kv8, self.sc, w.T, SM_SCALE(), self.out, stream=stream)
         self.h_out.copy_(self.out, non_blocking=True)
 
     def config(self):
