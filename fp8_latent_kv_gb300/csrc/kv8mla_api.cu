@@ -33,15 +33,16 @@ size_t sel_partial_bytes(int B, int P, int H) {
 }
 
 int decode_partitions(int H, int64_t T, int P_req) {
-    (void)H;
     if (T < 1) return 1;
     if (P_req > 0) {
         int64_t p = P_req < T ? P_req : T;
         return (int)(p > 65535 ? 65535 : p);
     }
-    // automatic: about one partition per pair of SMs, at least 128 rows each
-    int64_t p = (T + 127) / 128;
-    return (int)(p < 76 ? p : 76);
+    // automatic: one wave of tensor-core CTAs (one per SM of a 152-SM part, a CTA per partition and
+    // 64-head half), at least 128 rows per partition
+    const int64_t cap = H > 64 ? 76 : 152;
+    const int64_t p = (T + 127) / 128;
+    return (int)(p < cap ? p : cap);
 }
 
 int select_partitions(int B, int H, int NS) {

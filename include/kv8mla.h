@@ -102,13 +102,16 @@ KV8_API int kv8_quant_rows(const float *x, int64_t n, uint8_t *kv8, float *kv_sc
  *
  * Partition p of P covers rows [floor(T*p/P), floor(T*(p+1)/P)).  The workspace begins with the
  * partial sets (f32), for B batch items (B = 1 for decode):
- *     cl [B][P][H][512]   unnormalised context of each partition, relative to its own max
- *     m  [B][P][H]        partition max of score * log2(e)  (-inf for an empty partition)
+ *     cl [B][P][H][512]   unnormalised context of each partition, relative to its m
+ *     m  [B][P][H]        the partition's reference: the max of score * log2(e) over its rows, or a
+ *                         value at most 2 below it (the online softmax rescales lazily); -inf for a
+ *                         partition without rows
  *     z  [B][P][H]        sum over the partition of 2^(score*log2(e) - m)
  * The decode workspace continues with the library's own staging (the prepared queries); its size
  * is included in mla_decode8_workspace_bytes.
  * mla_decode8_partitions:      the partition count P the library uses for (H, T, P_req):
- *                              P_req = 0 picks automatically, P_req > 0 is clamped to [1, T].
+ *                              P_req = 0 picks automatically (one CTA per SM of a 152-SM GPU:
+ *                              min(ceil(T/128), 76 for H > 64, else 152)), P_req > 0 is clamped to [1, T].
  * mla_decode8_workspace_bytes: workspace bytes for (H, T, P_req).
  * --------------------------------------------------------------------------------------------- */
 KV8_API int mla_decode8_partitions(int H, int64_t T, int P_req, int *P_out);

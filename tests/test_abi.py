@@ -46,6 +46,8 @@ def test_strerror(lib):
 def test_partitions_and_workspace_sizes(lib):
     assert kv.mla_decode8_partitions(128, 262144) == 76
     assert kv.mla_decode8_partitions(16, 256) == 2
+    assert kv.mla_decode8_partitions(64, 262144) == 152   # one 64-head half: a CTA per partition
+    assert kv.mla_decode8_partitions(65, 262144) == 76
     assert kv.mla_decode8_partitions(128, 1) == 1
     assert kv.mla_decode8_partitions(128, 5, P_req=9) == 5
     assert kv.mla_decode8_partitions(128, 1000, P_req=7) == 7
