@@ -74,7 +74,7 @@ struct Misc {
             float zinv[kHeadsPerCta];          // and the direct output's factors s_ref / kWScale / zsum
         } fin;
     } ph;
-    uint64_t kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, pv_done, plo_free, final_bar, q_full;
+    uint64_t kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, pv_done, final_bar, q_full;
     uint64_t kv_blk[2][4];  // latent block kb of a stage has been read by the context product
     uint32_t tmem_base;
     int abort_flag;
@@ -203,7 +203,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&ms.p_full, kSoftmaxThreads);
         mbar_init(&ms.pv_done, 1);
-        mbar_init(&ms.plo_free, 1);
         mbar_init(&ms.final_bar, 1);
         mbar_init(&ms.q_full, 1);
         ms.abort_flag = 0;
@@ -437,25 +436,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    smem_desc(qb + kRcOff + kk * 32, 0, 512, kSw64), id_s, 1);
                     mma_commit(&ms.s_full[s]);
                 };
-                // The weights' lo piece goes first: its buffer is then free for the next tile's softmax
-                // while the hi piece (in the row stage's rope block) is still being read.
                 auto issue_pv = [&](int j) {
                     const int s = j & 1;
                     const uint32_t st = sbase + (s ? OFF_ST1 : OFF_ST0);
                     const uint32_t phi = st + kRcOff, plo = sbase + OFF_PLO;
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch)
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_f8f6f4(tmem + 256u + (uint32_t)ch * 64u, smem_desc(st + ch * 16384 + kk * 4096, 0, 1024, kSw128),
-                                       smem_desc(plo + kk * 2048, 0, 512, kSw64), id_pv, (j | kk) != 0);
-                    mma_commit(&ms.plo_free);
-#pragma unroll
                     for (int ch = 0; ch < 4; ++ch) {
+                        const uint32_t d = tmem + 256u + (uint32_t)ch * 64u;
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_f8f6f4(tmem + 256u + (uint32_t)ch * 64u, smem_desc(st + ch * 16384 + kk * 4096, 0, 1024, kSw128),
-                                       smem_desc(phi + kk * 2048, 0, 512, kSw64), id_pv, 1);
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t ad = smem_desc(st + ch * 16384 + kk * 4096, 0, 1024, kSw128);
+                            mma_f8f6f4(d, ad, smem_desc(phi + kk * 2048, 0, 512, kSw64), id_pv, (j | kk) != 0);
+                            mma_f8f6f4(d, ad, smem_desc(plo + kk * 2048, 0, 512, kSw64), id_pv, 1);
+                        }
                         mma_commit(&ms.kv_blk[s][ch]);  // latent block ch may be refilled
                     }
                     mma_commit(&ms.kv_empty[s]);
@@ -650,9 +643,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4 *>(phi + sw64_offset(r, 32 * hh + 16)) =
                     make_uint4(whi[4], whi[5], whi[6], whi[7]);
                 if (i >= 1) {
-                    // the previous context product must have read its weights' lo piece before the buffer
-                    // is reused, and must be done before its accumulators are rescaled
-                    if (ok) ok = mbar_wait(any_alpha ? &ms.pv_done : &ms.plo_free, (i - 1) & 1, &ms.abort_flag, a.err_word);
+                    // the previous context product must be done before its weights' lo buffer is reused
+                    // and before its accumulators are rescaled
+                    if (ok) ok = mbar_wait(&ms.pv_done, (i - 1) & 1, &ms.abort_flag, a.err_word);
                     if (any_alpha) {
                         // rescale this half's columns of the four context accumulators
                         tc_fence_after_sync();
@@ -757,11 +750,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-// Query prep, run once before the partial kernel (decode and selection).  Block b * n_heads_pad + h
-// splits head h of item b (scaled by 2^e_h so that max|q| * 2^e_h lies in [128, 256)) into e4m3 hi +
-// lo rows of that item's head-group image and writes its score factor sm_scale*log2(e)*2^-e_h (0 for
-// a padding head); block B * n_heads_pad + b * P + p takes the largest scale among the rows that
-// partition p of item b attends.
+// Query prep, run once before the partial kernel (decode and selection).  Block b * n_heads_pad/8 + g
+// splits heads 8g..8g+7 of item b (each scaled by 2^e_h so that max|q| * 2^e_h lies in [128, 256)) into
+// e4m3 hi + lo rows of that item's head-group image and writes their score factors
+// sm_scale*log2(e)*2^-e_h (0 for a padding head); block B * n_heads_pad/8 + b * P + p takes the largest
+// scale among the rows that partition p of item b attends.
 struct PrepArgs {
     const __nv_bfloat16 *q_lat, *q_rope;
     int B, H, n_heads_pad, P;
@@ -776,71 +769,78 @@ struct PrepArgs {
     float *smax;         // [B][P]
 };
 
-__global__ void __launch_bounds__(128) tc_prep_kernel(PrepArgs a) {
+constexpr int kPrepHeads = 8;                   // heads per query-prep block
+constexpr int kPrepBlock = kPrepHeads * 36;     // one thread per (head, 16-element chunk)
+
+__global__ void __launch_bounds__(kPrepBlock) tc_prep_kernel(PrepArgs a) {
     grid_launch_dependents();  // the partial kernel may start its row loads while this runs
-    __shared__ float red[4];
+    __shared__ float red[kPrepBlock / 32];
+    __shared__ int qmax_bits[kPrepHeads];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, bid = blockIdx.x;
-    if (bid < a.B * a.n_heads_pad) {
-        const int b = bid / a.n_heads_pad, h = bid - b * a.n_heads_pad;
+    const int n_groups = a.n_heads_pad / kPrepHeads;
+    if (bid < a.B * n_groups) {
+        const int b = bid / n_groups, g = bid - b * n_groups;
+        const int hl = tid / 36, ch = tid - hl * 36, h = g * kPrepHeads + hl;
         const int half = h / kHeadsPerCta, row = h - half * kHeadsPerCta;
+        if (tid < kPrepHeads) qmax_bits[tid] = 0;
+        __syncthreads();
         uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-        float mx = 0.f;
-        if (tid < 36 && h < a.H) {
+        if (h < a.H) {
             const int64_t qh = (int64_t)b * a.H + h;
-            const __nv_bfloat16 *src = tid < 32 ? a.q_lat + qh * kKL + tid * 16 : a.q_rope + qh * kKR + (tid - 32) * 16;
+            const __nv_bfloat16 *src = ch < 32 ? a.q_lat + qh * kKL + ch * 16 : a.q_rope + qh * kKR + (ch - 32) * 16;
             const uint4 u0 = __ldg(reinterpret_cast<const uint4 *>(src)), u1 = __ldg(reinterpret_cast<const uint4 *>(src) + 1);
             w[0] = u0.x; w[1] = u0.y; w[2] = u0.z; w[3] = u0.w;
             w[4] = u1.x; w[5] = u1.y; w[6] = u1.z; w[7] = u1.w;
+            float mx = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
                 mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
             }
+            atomicMax(&qmax_bits[hl], __float_as_int(mx));  // non-negative floats order like ints
         }
-        mx = warp_max(mx);
-        if (lane == 0) red[warp] = mx;
         __syncthreads();
-        mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+        const float mx = __int_as_float(qmax_bits[hl]);
         int E = 0;
         if (mx > 0.f) frexpf(mx, &E);
         const int sh = mx > 0.f ? 8 - E : 0;  // values are scaled, not a 2^sh factor: it may overflow
-        if (tid < 36) {
-            uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
+        uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
-                uint32_t ph, pl;
-                split_pair(ldexpf(f.x, sh), ldexpf(f.y, sh), ph, pl);
-                hi[e >> 1] |= ph << ((e & 1) * 16);
-                lo[e >> 1] |= pl << ((e & 1) * 16);
-            }
-            uint8_t *dst = a.img + ((size_t)b * (a.n_heads_pad / kHeadsPerCta) + half) * kImg;
-            uint32_t off_hi, off_lo;
-            if (tid < 32) {
-                const uint32_t kb = tid >> 3, byte = (tid & 7) * 16;
-                off_hi = kb * 16384 + sw128_offset(row, byte);
-                off_lo = kb * 16384 + sw128_offset(row + 64, byte);
-            } else {
-                const uint32_t byte = (tid - 32) * 16;
-                off_hi = kRcOff + sw64_offset(row, byte);
-                off_lo = kRcOff + sw64_offset(row + 64, byte);
-            }
-            *reinterpret_cast<uint4 *>(dst + off_hi) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4 *>(dst + off_lo) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        for (int e = 0; e < 8; ++e) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
+            uint32_t ph, pl;
+            split_pair(ldexpf(f.x, sh), ldexpf(f.y, sh), ph, pl);
+            hi[e >> 1] |= ph << ((e & 1) * 16);
+            lo[e >> 1] |= pl << ((e & 1) * 16);
         }
-        if (tid == 0) a.c_head[bid] = h < a.H ? (mx > 0.f ? ldexpf(a.sm_scale_log2, E - 8) : a.sm_scale_log2) : 0.f;
+        uint8_t *dst = a.img + ((size_t)b * (a.n_heads_pad / kHeadsPerCta) + half) * kImg;
+        uint32_t off_hi, off_lo;
+        if (ch < 32) {
+            const uint32_t kb = ch >> 3, byte = (ch & 7) * 16;
+            off_hi = kb * 16384 + sw128_offset(row, byte);
+            off_lo = kb * 16384 + sw128_offset(row + 64, byte);
+        } else {
+            const uint32_t byte = (ch - 32) * 16;
+            off_hi = kRcOff + sw64_offset(row, byte);
+            off_lo = kRcOff + sw64_offset(row + 64, byte);
+        }
+        *reinterpret_cast<uint4 *>(dst + off_hi) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(dst + off_lo) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        if (ch == 0)
+            a.c_head[(int64_t)b * a.n_heads_pad + h] =
+                h < a.H ? (mx > 0.f ? ldexpf(a.sm_scale_log2, E - 8) : a.sm_scale_log2) : 0.f;
     } else {
-        const int bp = bid - a.B * a.n_heads_pad, b = bp / a.P, p = bp - b * a.P;
+        const int bp = bid - a.B * n_groups, b = bp / a.P, p = bp - b * a.P;
         const int64_t n_list = a.idx ? (int64_t)a.NS : a.T;
         const int64_t t0 = n_list * p / a.P, t1 = n_list * (p + 1) / a.P;
         const int32_t *idx_b = a.idx ? a.idx + (int64_t)b * a.NS : nullptr;
         const float *sc_b = a.kv_scale + (int64_t)b * a.seq_stride_rows;
         float mx = 0.f;
-        for (int64_t t = t0 + tid; t < t1; t += 8 * 128) {
+        for (int64_t t = t0 + tid; t < t1; t += 8 * kPrepBlock) {
             float v[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const int64_t tu = t + (int64_t)u * 128;
+                const int64_t tu = t + (int64_t)u * kPrepBlock;
                 int64_t ri = tu < t1 ? (idx_b ? (int64_t)__ldg(idx_b + tu) : tu) : -1;
                 v[u] = (ri >= 0 && ri < a.T) ? __ldg(sc_b + ri) : 0.f;
             }
@@ -850,7 +850,11 @@ __global__ void __launch_bounds__(128) tc_prep_kernel(PrepArgs a) {
         mx = warp_max(mx);
         if (lane == 0) red[warp] = mx;
         __syncthreads();
-        if (tid == 0) a.smax[bp] = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+        if (tid == 0) {
+            float m = 0.f;
+            for (int k = 0; k < kPrepBlock / 32; ++k) m = fmaxf(m, red[k]);
+            a.smax[bp] = m;
+        }
     }
 }
 
@@ -935,7 +939,7 @@ cudaError_t launch_attn_tc(const AttnArgs &x, cudaStream_t st) {
         a.qimg = pa.img;
         a.c_head = pa.c_head;
         a.smax = pa.smax;
-        tc_prep_kernel<<<(unsigned)((int64_t)a.B * (n_heads_pad + a.P)), 128, 0, st>>>(pa);
+        tc_prep_kernel<<<(unsigned)((int64_t)a.B * (n_heads_pad / kPrepHeads + a.P)), kPrepBlock, 0, st>>>(pa);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)grid);

@@ -168,3 +168,17 @@ def test_decode_query_magnitudes(lib, oracle):
     assert np.all(np.isfinite(got))
     for h in range(H):  # each head against its own scale
         parity(got[h], ref[h], f"head {h} (2^{int(exps[h])})")
+
+
+def test_decode_repeated_calls_identical(lib, oracle):
+    """The kernels are deterministic (fixed MMA and reduction orders, order-free atomics), so repeated
+    calls must give bit-identical outputs: a race between the pipeline's stages shows up as a mismatch.
+    Few partitions (long CTAs, many tiles per CTA) give races the most chances."""
+    s = step(lib, oracle, "dec16k")
+    for P_req in (1, 2, 3):
+        first = _decode(lib, s.q_lat, s.q_rope, s.kv8, s.sc, s.w.T, P_req=P_req)
+        for _ in range(12):
+            again = _decode(lib, s.q_lat, s.q_rope, s.kv8, s.sc, s.w.T, P_req=P_req)
+            assert np.array_equal(again, first), f"P={P_req}: outputs differ between identical calls"
+        heads = list(range(0, 128, 9))
+        parity(first[heads], oracle.attn_decode(s.ql[heads], s.qr[heads], s.q_o, s.s_o, synth.SM_SCALE), f"P={P_req}")
