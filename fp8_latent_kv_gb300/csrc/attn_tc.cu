@@ -21,13 +21,17 @@
 //   context O^T[d][h]  += sum_t  V8[t][d] * W^T[t][h]        M = 128 dims (x4 chunks), N = 64, K = 128 rows
 //           A = the same cache bytes read MN-major (V^T), B = the weights MN-major.
 //
+// Rows reach shared memory by TMA: dense (and causal) ranges as 128-row tiles, selected rows (DSA) four
+// at a time with tile::gather4 from a tensor map over all items' caches.
+//
 // Warps: 0 = TMA producer, 1 = MMA issuer (and TMEM owner), 2..9 = softmax / epilogue.
 // Shared memory (231 KB): query image 72 KB, two 72 KB row stages (the weights' hi piece reuses the
 // stage's rope block once the score has read it), weights' lo piece 8 KB, barriers and scratch.
 // TMEM (512 columns): two 128-column score buffers (hi / lo query pieces side by side), four 64-column
 // context accumulators.
-// Every wait is an mbarrier wait bounded in time; a timeout sets KV8_ERR_TIMEOUT and the CTA winds
-// down without hanging.
+// Every mbarrier wait is bounded in time; a timeout sets KV8_ERR_TIMEOUT.  The softmax warps then skip
+// their remaining waits but still pass every named barrier of every tile, so the CTA winds down without
+// hanging.
 #include "internal.h"
 #include "sm100.cuh"
 
