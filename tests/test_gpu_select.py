@@ -148,3 +148,20 @@ def test_select_partitions_with_no_valid_row(lib, oracle):
     ref, bad = oracle.attn_select(ql[:, heads], qr[:, heads], q_o, s_o, T, T, idx, synth.SM_SCALE)
     assert bad == 512 + (NS - 700)
     parity(got[:, heads], ref, "partitions without valid rows")
+
+
+def test_select_repeated_calls_identical(lib, oracle):
+    """Repeated selection decodes give bit-identical outputs (a race between the row copies, the score
+    and the context product would show up as a mismatch); several tiles per partition."""
+    B, T, H = 2, 5000, 128
+    q_o, s_o, ql, qr, rng = _small(oracle, B, T, H, 6)
+    kv8, sc = torch.from_numpy(q_o).to(DEV), torch.from_numpy(s_o).to(DEV)
+    for NS in (700, 4096):
+        idx = np.stack([rng.choice(T, NS, replace=True) for _ in range(B)]).astype(np.int32)
+        tidx = torch.from_numpy(idx).to(DEV)
+        first = _sel(lib, _bf(ql), _bf(qr), kv8, sc, T, T, tidx)
+        for _ in range(10):
+            assert np.array_equal(_sel(lib, _bf(ql), _bf(qr), kv8, sc, T, T, tidx), first), f"NS={NS}"
+        heads = [0, 77, 127]
+        parity(first[:, heads], oracle.attn_select(ql[:, heads], qr[:, heads], q_o, s_o, T, T, idx,
+                                                   synth.SM_SCALE)[0], f"NS={NS}")
