@@ -235,7 +235,7 @@ __device__ __forceinline__ void merge_small(const PartialView &pv, int64_t base,
     float c[NP];
 #pragma unroll
     for (int u = 0; u < NP; ++u) c[u] = u < P ? cl[(int64_t)u * pstride] : 0.f;
-    constexpr int K = NP / 32;
+    constexpr int K = (NP + 31) / 32;
     float mv[K], zv[K];
 #pragma unroll
     for (int k = 0; k < K; ++k) {
@@ -267,10 +267,11 @@ __device__ __forceinline__ void merge_small(const PartialView &pv, int64_t base,
     *out = Z > 0.f ? (acc0 + acc1) / Z : 0.f;
 }
 
+// NP > 0: P <= NP, every load issued up front (one instantiation per size, so a small P does not pay
+// for the registers of a large one); NP == 0: any P, weights through shared memory.
+template <int NP>
 __global__ void __launch_bounds__(128) lse_merge_kernel(const float *__restrict__ ws, int B, int P, int H,
                                                         float *__restrict__ out) {
-    __shared__ float wsh[kMergeMaxP];
-    __shared__ float zsh;
     // launched as a programmatic dependent of the partial kernel: wait until its partials are written
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int h = blockIdx.x, quarter = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
@@ -278,10 +279,13 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const float *__restrict_
     const int64_t base = (int64_t)b * P * H + h;
     const int d = quarter * 128 + tid;
     float *o = out + ((int64_t)b * H + h) * kKL + d;
-    if (P <= 32) return merge_small<32>(pv, base, P, H, d, o);
-    if (P <= 64) return merge_small<64>(pv, base, P, H, d, o);
-    if (P <= kMergeFast) return merge_small<kMergeFast>(pv, base, P, H, d, o);
+    if constexpr (NP > 0) {
+        merge_small<NP>(pv, base, P, H, d, o);
+        return;
+    }
     // large P: warp 0 turns the maxima into weights in shared memory
+    __shared__ float wsh[kMergeMaxP];
+    __shared__ float zsh;
     float M = -INFINITY;
     if (tid < 32) {
         for (int p = tid; p < P; p += 32) M = fmaxf(M, pv.m[base + (int64_t)p * H]);
@@ -352,7 +356,12 @@ cudaError_t launch_lse_merge(const float *ws, int B, int P, int H, float *out, c
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, lse_merge_kernel, ws, B, P, H, out);
+    cudaError_t e = P <= 16   ? cudaLaunchKernelEx(&cfg, lse_merge_kernel<16>, ws, B, P, H, out)
+                    : P <= 32 ? cudaLaunchKernelEx(&cfg, lse_merge_kernel<32>, ws, B, P, H, out)
+                    : P <= 64 ? cudaLaunchKernelEx(&cfg, lse_merge_kernel<64>, ws, B, P, H, out)
+                    : P <= 96 ? cudaLaunchKernelEx(&cfg, lse_merge_kernel<96>, ws, B, P, H, out)
+                    : P <= kMergeFast ? cudaLaunchKernelEx(&cfg, lse_merge_kernel<kMergeFast>, ws, B, P, H, out)
+                                      : cudaLaunchKernelEx(&cfg, lse_merge_kernel<0>, ws, B, P, H, out);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
