@@ -103,6 +103,35 @@ def test_partial_then_merge_equals_combined(lib, oracle):
     assert np.array_equal(out.cpu().numpy(), combined)
 
 
+@pytest.mark.parametrize("P", [1, 5, 16, 17, 32, 33, 64, 65, 96, 97, 128, 129, 300])
+def test_merge_alone_every_partition_class(lib, oracle, P):
+    """The merge kernel fed the oracle's own split-T partials (cl, m, z in double; m in natural-log
+    units, so m * log2(e) in the library's layout) for B = 3 queries: every kernel size class of P,
+    and P > T, where some partitions are empty (m = -inf, z = 0)."""
+    T, H, B = 257, 8, 3
+    rng = np.random.default_rng(1000 + P)
+    rows = synth.latent_rows(rng, T, 0.1, 10.0)
+    q_o, s_o = oracle.quant_rows(rows)
+    cl = np.zeros((B, P, H, 512), np.float32)
+    m = np.zeros((B, P, H), np.float32)
+    z = np.zeros((B, P, H), np.float32)
+    ref = np.zeros((B, H, 512), np.float32)
+    for b in range(B):
+        q = synth.normal_f32(rng, (H, 576)) * np.float32(1 + 3 * b)
+        ref[b], cl_b, m_b, z_b = oracle.attn_decode_split(q[:, :512], q[:, 512:], q_o, s_o, synth.SM_SCALE, P)
+        cl[b], m[b], z[b] = cl_b, m_b * np.log2(np.e), z_b
+    if P > T:
+        assert np.isinf(m).any(), "some partitions are empty"
+    ws = torch.from_numpy(np.concatenate([cl.ravel(), m.ravel(), z.ravel()])).to(DEV)
+    out = torch.empty((B, H, 512), dtype=torch.float32, device=DEV)
+    lib.mla_lse_merge8(ws, B, P, H, out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    # inputs rounded to f32 (m to ~1e-5 log2 units): far inside the attention tolerance
+    err = np.abs(got - ref).max() / np.abs(ref).max()
+    assert err <= 1e-4, f"P={P}: max error {err:.2e} of max |out|"
+
+
 def _random_case(oracle, T, H, seed, mag=(0.1, 10.0)):
     rng = np.random.default_rng(seed)
     rows = synth.latent_rows(rng, T, *mag)
