@@ -33,6 +33,7 @@ SIGNATURES = {
     "mla_absorb_sel8": (_I, [_P, _P, _I, _I, _I, _P, _P, _I64, _I64, _P, _I, _F, _P, _SZ, _P, _P, _P]),
     "mla_absorb_prefill8": (_I, [_P, _P, _I, _I, _I, _I64, _P, _P, _I64, _F, _P, _P, _P]),
     "mla_absorb_decode8_noalloc": (_I, [_P, _P, _I, _I, _P, _P, _I64, _F, _I, _P, _P, _P]),
+    "kv8_copy": (_I, [_P, _P, _SZ, _P]),
     "kv8_strerror": (ctypes.c_char_p, [_I]),
 }
 
@@ -122,6 +123,13 @@ def mla_decode8_partial(q_lat, q_rope, kv8, kv_scale, T: int, sm_scale: float, w
     _check("mla_decode8_partial", load().mla_decode8_partial(
         _ptr(q_lat), _ptr(q_rope), _qdtype(q_lat), H, _ptr(kv8), _ptr(kv_scale), T, sm_scale, P_req,
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err_word), _stream(stream)))
+
+
+def kv8_copy(dst, src, nbytes: int | None = None, stream=None) -> None:
+    """Copy nbytes (default: all of src) from src to dst with a kernel; either may be a CUDA tensor or a
+    pinned (page-locked) CPU tensor."""
+    n = src.numel() * src.element_size() if nbytes is None else int(nbytes)
+    _check("kv8_copy", load().kv8_copy(_ptr(dst), _ptr(src), n, _stream(stream)))
 
 
 def mla_lse_merge8(workspace, B: int, P: int, H: int, out, stream=None) -> None:

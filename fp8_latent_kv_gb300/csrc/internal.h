@@ -35,6 +35,7 @@ cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t st);
 // need tc_scratch and (B-1)*seq_stride_rows + T < 2^31).
 cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st);
 size_t tc_scratch_bytes(int B, int P);
+cudaError_t launch_copy(void *dst, const void *src, size_t bytes, cudaStream_t st);
 cudaError_t launch_lse_merge(const float *ws, int B, int P, int H, float *out, cudaStream_t st);
 
 // Partition policy shared by the workspace queries and the launchers.

@@ -22,6 +22,25 @@ inline bool valid_cache(const uint8_t *kv8, const float *kv_scale, int64_t T) {
     return aligned(kv8, 16) && aligned(kv_scale, 4) && T >= 1 && T <= KV8_MAX_ROWS;
 }
 
+// The address the current device's kernels use for p: device memory of the current device as is,
+// page-locked host memory through its mapping; null for anything a kernel cannot reach (pageable
+// host memory, another device's memory, an unknown pointer).
+const void *device_view(const void *p) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();  // clear the error the query left
+        return nullptr;
+    }
+    switch (at.type) {
+        case cudaMemoryTypeDevice: return at.device == dev ? p : nullptr;
+        case cudaMemoryTypeManaged: return p;
+        case cudaMemoryTypeHost: return at.devicePointer;
+        default: return nullptr;
+    }
+}
+
 }  // namespace
 
 size_t decode_partial_bytes(int P, int H) {
@@ -72,6 +91,17 @@ const char *kv8_strerror(int code) {
         case KV8_EUNSUPPORTED: return "unsupported device or shape";
         default: return "unknown kv8 error code";
     }
+}
+
+int kv8_copy(void *dst, const void *src, size_t bytes, void *stream) {
+    if (bytes == 0) return KV8_OK;
+    if (!dst || !src) return KV8_EINVAL;
+    const uintptr_t d = reinterpret_cast<uintptr_t>(dst), s = reinterpret_cast<uintptr_t>(src);
+    if (d < s + bytes && s < d + bytes) return KV8_EINVAL;  // overlapping ranges
+    void *dd = const_cast<void *>(device_view(dst));
+    const void *ds = device_view(src);
+    if (!dd || !ds) return KV8_EINVAL;
+    return status(launch_copy(dd, ds, bytes, (cudaStream_t)stream));
 }
 
 int kv8_encode_e4m3(const float *y, int64_t n, uint8_t *out, void *stream) {

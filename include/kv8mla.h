@@ -196,6 +196,21 @@ KV8_API int mla_absorb_decode8_noalloc(const void *q_lat, const void *q_rope, in
                                        const uint8_t *kv8, const float *kv_scale, int64_t T, float sm_scale,
                                        int P_req, int *err_word, float *out, void *stream);
 
+/* -----------------------------------------------------------------------------------------------
+ * kv8_copy -- copy `bytes` bytes from src to dst with a kernel (the SMs' loads and stores, not a
+ * copy engine).  The pages have no counterpart to this call; it exists for users of this library:
+ * on a GPU whose host memory is coherently attached (NVLink-C2C), it moves a step's small inputs
+ * and outputs between page-locked host memory and the device with less fixed cost per transfer
+ * than a copy-engine memcpy.
+ *   dst, src: device memory of the current device, managed memory, or page-locked host memory
+ *   (cudaHostAlloc / cudaMallocHost / cudaHostRegister), in any combination and any alignment
+ *   (16-byte aligned pointers take the vector path).  The ranges must not overlap.
+ *   Pageable host memory, another device's memory or an unknown pointer is KV8_EINVAL (checked
+ *   with cudaPointerGetAttributes on the host; nothing is enqueued).  bytes == 0 enqueues nothing.
+ *   Stream-ordered and asynchronous like every call.
+ * --------------------------------------------------------------------------------------------- */
+KV8_API int kv8_copy(void *dst, const void *src, size_t bytes, void *stream);
+
 /* Name of a return code (static string). */
 KV8_API const char *kv8_strerror(int code);
 
