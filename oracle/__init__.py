@@ -65,6 +65,8 @@ def _load():
             "kv8o_attn_decode_split": (None, [P, P, i32, P, P, i64, f32, i32, P, P, P, P]),
             "kv8o_attn_select": (None, [P, P, i32, i32, P, P, i64, i64, P, i32, f32, P, P]),
             "kv8o_attn_prefill": (None, [P, P, i32, i32, P, P, P, i64, f32, P]),
+            "kv8o_q_absorb": (None, [P, i32, i32, P, P, P]),
+            "kv8o_out_project": (None, [P, i32, i32, P, P, P]),
             "kv8o_num_threads": (i32, []),
             "kv8o_set_num_threads": (None, [i32]),
         }
@@ -206,6 +208,39 @@ def attn_prefill(q_lat, q_rope, pos, kv8, scale, sm_scale) -> np.ndarray:
     out = np.empty((nq, H, KL), dtype=np.float32)
     _load().kv8o_attn_prefill(_ptr(ql), _ptr(qr), nq, H, _ptr(pos), _ptr(kv8), _ptr(scale), T,
                               float(np.float32(sm_scale)), _ptr(out))
+    return out
+
+
+NOPE, VH, BLK = 128, 128, 128
+
+
+def _kvb(w8, w_scale, H):
+    w8 = np.ascontiguousarray(w8, dtype=np.uint8).reshape(H * (NOPE + VH), KL)
+    w_scale = _f32(w_scale).reshape(-1)
+    assert w_scale.size == (H * (NOPE + VH) // BLK) * (KL // BLK), "one scale per 128x128 block"
+    return w8, w_scale
+
+
+def q_absorb(q_nope, w8, w_scale) -> np.ndarray:
+    """q_lat [..., H, 512] f32 = each head's 128 no-position query values through its W_UK rows of the
+    fmt=8 kv_b (w8 [H*256][512] e4m3 bytes, w_scale [H*2][4] block scales); double accumulation."""
+    q = _f32(q_nope)
+    H = q.shape[-2]
+    S = int(q.size // (H * NOPE))
+    w8, w_scale = _kvb(w8, w_scale, H)
+    out = np.empty(q.shape[:-1] + (KL,), dtype=np.float32)
+    _load().kv8o_q_absorb(_ptr(q), S, H, _ptr(w8), _ptr(w_scale), _ptr(out))
+    return out
+
+
+def out_project(ctx, w8, w_scale) -> np.ndarray:
+    """out [..., H, 128] f32 = each head's 512-wide context through its W_UV rows of the fmt=8 kv_b."""
+    x = _f32(ctx)
+    H = x.shape[-2]
+    S = int(x.size // (H * KL))
+    w8, w_scale = _kvb(w8, w_scale, H)
+    out = np.empty(x.shape[:-1] + (VH,), dtype=np.float32)
+    _load().kv8o_out_project(_ptr(x), S, H, _ptr(w8), _ptr(w_scale), _ptr(out))
     return out
 
 

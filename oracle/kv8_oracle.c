@@ -451,6 +451,60 @@ void kv8o_attn_prefill(const float *q_lat, const float *q_rope, int nq, int H, c
     free(rows);
 }
 
+/* ---------------------------------------------------------------------------------------------
+ * Absorb projections through kv_b_proj stored as fmt=8 ([FMT8]: raw e4m3 bytes, one f32 scale per
+ * 128x128 block, block-row-major, ceil(O/128) x ceil(I/128) scales).  kv_b has O = H*256 rows of
+ * I = 512 columns; head h owns rows 256h..256h+127 (W_UK: the no-position key part, qk_nope = 128)
+ * and rows 256h+128..256h+255 (W_UV: the value part, v_head = 128).  The dequantized weight is
+ *     W[o][i] = e4m3(w8[o][i]) * w_scale[(o/128) * nbc + i/128],   nbc = ceil(I/128) = 4.
+ * Every product is widened to double and summed in double; each output is rounded once to f32.
+ *
+ * Query side (the absorbed query, [KV8] first commit: the latent is the key):
+ *     q_lat[s][h][c] = sum_{j<128} q_nope[s][h][j] * W[256h + j][c]          (c < 512)
+ * Output side (the context leaves the latent space through the value rows):
+ *     out[s][h][v]   = sum_{c<512} W[256h + 128 + v][c] * ctx[s][h][c]        (v < 128)
+ * ------------------------------------------------------------------------------------------- */
+#define KV8O_NOPE 128
+#define KV8O_VH 128
+#define KV8O_BLK 128
+
+static double kvb_weight(const uint8_t *w8, const float *w_scale, int64_t o, int i)
+{
+    const int nbc = (KV8O_KL + KV8O_BLK - 1) / KV8O_BLK;
+    return kv8o_e4m3_decode(w8[o * KV8O_KL + i]) * (double)w_scale[(o / KV8O_BLK) * nbc + i / KV8O_BLK];
+}
+
+void kv8o_q_absorb(const float *q_nope, int S, int H, const uint8_t *w8, const float *w_scale, float *q_lat)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t sh = 0; sh < (int64_t)S * H; ++sh) {
+        const int h = (int)(sh % H);
+        const float *q = q_nope + sh * KV8O_NOPE;
+        for (int c = 0; c < KV8O_KL; ++c) {
+            double acc = 0.0;
+            for (int j = 0; j < KV8O_NOPE; ++j)
+                acc += (double)q[j] * kvb_weight(w8, w_scale, (int64_t)h * (KV8O_NOPE + KV8O_VH) + j, c);
+            q_lat[sh * KV8O_KL + c] = (float)acc;
+        }
+    }
+}
+
+void kv8o_out_project(const float *ctx, int S, int H, const uint8_t *w8, const float *w_scale, float *out)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t sh = 0; sh < (int64_t)S * H; ++sh) {
+        const int h = (int)(sh % H);
+        const float *x = ctx + sh * KV8O_KL;
+        for (int v = 0; v < KV8O_VH; ++v) {
+            const int64_t o = (int64_t)h * (KV8O_NOPE + KV8O_VH) + KV8O_NOPE + v;
+            double acc = 0.0;
+            for (int c = 0; c < KV8O_KL; ++c)
+                acc += kvb_weight(w8, w_scale, o, c) * (double)x[c];
+            out[sh * KV8O_VH + v] = (float)acc;
+        }
+    }
+}
+
 int kv8o_num_threads(void)
 {
 #ifdef _OPENMP

@@ -136,3 +136,33 @@ def selection_for(w: Workload) -> np.ndarray:
     for b in range(w.B):
         out[b] = np.sort(rng.choice(w.T, size=w.NS, replace=False)).astype(np.int32)
     return out
+
+
+NOPE, VH, BLK = 128, 128, 128
+
+
+def kvb_fmt8(H: int, seed: int = 2000):
+    """Synthetic kv_b_proj in fmt=8 for H heads: (w8 [H*256][512] u8, w_scale [H*2][4] f32).
+
+    The bytes are drawn directly as e4m3 codes (no encoding): random sign, exponent field uniform in
+    6..11 and mantissa uniform in 0..7, so |code value| spans 0.5 .. 30 (never a NaN code, never
+    zero); the 128x128 block scales are log-uniform in [1e-3, 1e-2] (weights of magnitude ~1e-3 ..
+    0.3, the range of a trained up-projection)."""
+    rng = np.random.default_rng([seed, H])
+    n = H * (NOPE + VH) * KL
+    sign = rng.integers(0, 2, n, dtype=np.uint8)
+    expo = rng.integers(6, 12, n, dtype=np.uint8)
+    mant = rng.integers(0, 8, n, dtype=np.uint8)
+    w8 = ((sign << 7) | (expo << 3) | mant).astype(np.uint8).reshape(H * (NOPE + VH), KL)
+    w_scale = (10.0 ** rng.uniform(-3.0, -2.0, (H * (NOPE + VH) // BLK, KL // BLK))).astype(np.float32)
+    return w8, w_scale
+
+
+def q_nope_for(w: Workload, n_query: int | None = None) -> np.ndarray:
+    """The queries' no-position parts [nq][H][128] (f32 holding bf16-representable N(0,1) values unless
+    the workload's queries are f32)."""
+    if n_query is None:
+        n_query = w.S if w.key == "prefill" else w.B
+    rng = rng_for(w, 4)
+    q = normal_f32(rng, (n_query, w.H, NOPE))
+    return q if w.q_f32 else to_bf16_values(q)

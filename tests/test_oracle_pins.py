@@ -416,3 +416,112 @@ def test_prefill_query_equals_decode_over_prefix(oracle):
     kv2[pos0 + 1:] = 0x7E
     out2 = oracle.attn_prefill(ql[:1], qr[:1], pos[:1], kv2, sc, 0.09)
     np.testing.assert_array_equal(out2[0], out[0])
+
+
+# ------------------------------------------------------------------------------------------------
+# absorb projections through an fmt=8 kv_b (e4m3 bytes, one f32 scale per 128x128 block)
+# ------------------------------------------------------------------------------------------------
+def _kvb_dense(w8, w_scale):
+    """Dequantized kv_b in double, decoded by torch's float8_e4m3fn (independent of the oracle's table)."""
+    vals = torch.from_numpy(np.ascontiguousarray(w8)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return vals * np.repeat(np.repeat(w_scale.astype(np.float64), 128, axis=0), 128, axis=1)
+
+
+def test_q_absorb_identity_weights_copy_the_query(oracle):
+    H = 3
+    w8 = np.zeros((H * 256, KL), np.uint8)
+    for h in range(H):
+        w8[h * 256 + np.arange(128), np.arange(128)] = 0x38  # 1.0
+    sc = np.ones((H * 2, 4), np.float32)
+    q = np.random.default_rng(1).standard_normal((5, H, 128)).astype(np.float32)
+    got = oracle.q_absorb(q, w8, sc)
+    assert np.array_equal(got[..., :128], q) and not got[..., 128:].any()
+
+
+@pytest.mark.parametrize("h,j,c", [(0, 0, 0), (1, 127, 511), (2, 5, 300), (2, 64, 129)])
+def test_q_absorb_single_weight_lands_at_its_index(oracle, h, j, c):
+    """One nonzero weight at kv_b row 256h+j, column c: only q_lat[:, h, c] is nonzero, equal to
+    q_nope[:, h, j] * value * block scale (pins the row/column order and the head offset)."""
+    H = 3
+    w8 = np.zeros((H * 256, KL), np.uint8)
+    w8[256 * h + j, c] = 0x4C  # 1.5 * 2^2 = 6
+    sc = np.full((H * 2, 4), 0.5, np.float32)
+    sc[2 * h, c // 128] = 0.125
+    q = np.random.default_rng(2).standard_normal((4, H, 128)).astype(np.float32)
+    got = oracle.q_absorb(q, w8, sc)
+    want = np.zeros_like(got)
+    want[:, h, c] = (q[:, h, j].astype(np.float64) * 6.0 * 0.125).astype(np.float32)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("h,v,c", [(0, 0, 0), (1, 127, 511), (2, 9, 200)])
+def test_out_project_single_weight_lands_at_its_index(oracle, h, v, c):
+    H = 3
+    w8 = np.zeros((H * 256, KL), np.uint8)
+    w8[256 * h + 128 + v, c] = 0xC4  # -(1.5) * 2^1 = -3
+    sc = np.full((H * 2, 4), 0.5, np.float32)
+    sc[2 * h + 1, c // 128] = 2.0
+    x = np.random.default_rng(3).standard_normal((2, H, KL)).astype(np.float32)
+    got = oracle.out_project(x, w8, sc)
+    want = np.zeros_like(got)
+    want[:, h, v] = (x[:, h, c].astype(np.float64) * -3.0 * 2.0).astype(np.float32)
+    assert np.array_equal(got, want)
+
+
+def test_projections_match_a_double_matmul(oracle):
+    """Against torch-decoded weights times block scales and an einsum in double."""
+    import synth
+    H = 4
+    w8, sc = synth.kvb_fmt8(H, seed=7)
+    W = _kvb_dense(w8, sc).reshape(H, 256, KL)
+    rng = np.random.default_rng(4)
+    q = rng.standard_normal((3, H, 128)).astype(np.float32)
+    x = rng.standard_normal((3, H, KL)).astype(np.float32)
+    want_q = np.einsum("shj,hjc->shc", q.astype(np.float64), W[:, :128, :])
+    want_o = np.einsum("hvc,shc->shv", W[:, 128:, :], x.astype(np.float64))
+    np.testing.assert_allclose(oracle.q_absorb(q, w8, sc), want_q, rtol=2e-7, atol=1e-30 + 1e-7 * np.abs(want_q).max())
+    np.testing.assert_allclose(oracle.out_project(x, w8, sc), want_o, rtol=2e-7, atol=1e-7 * np.abs(want_o).max())
+
+
+def test_block_scale_enters_only_its_block(oracle):
+    import synth
+    H = 2
+    w8, sc = synth.kvb_fmt8(H, seed=8)
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((2, H, 128)).astype(np.float32)
+    x = rng.standard_normal((2, H, KL)).astype(np.float32)
+    base_q, base_o = oracle.q_absorb(q, w8, sc), oracle.out_project(x, w8, sc)
+    sc2 = sc.copy()
+    sc2[2 * 1 + 0, 2] *= 2.0  # head 1, W_UK, columns 256..383
+    got = oracle.q_absorb(q, w8, sc2)
+    assert np.array_equal(got[:, 1, 256:384], 2 * base_q[:, 1, 256:384])
+    keep = np.ones(got.shape, bool)
+    keep[:, 1, 256:384] = False
+    assert np.array_equal(got[keep], base_q[keep])
+    # value side: the block's share of head 1's outputs doubles, i.e. is added once more
+    sc3 = sc.copy()
+    sc3[2 * 1 + 1, 3] *= 2.0
+    only = np.zeros_like(sc)
+    only[2 * 1 + 1, 3] = sc[2 * 1 + 1, 3]
+    share = oracle.out_project(x, w8, only)
+    got_o = oracle.out_project(x, w8, sc3)
+    np.testing.assert_allclose(got_o[:, 1], base_o[:, 1] + share[:, 1], rtol=1e-6, atol=1e-6 * np.abs(base_o).max())
+    assert np.array_equal(got_o[:, 0], base_o[:, 0])
+
+
+def test_absorbed_score_equals_unabsorbed_score(oracle):
+    """The absorption identity: q_lat . c == q_nope . (W_UK c) for a latent row c.  W_UK c is computed
+    with the value-side function on a kv_b whose value rows are the key rows."""
+    import synth
+    H = 3
+    w8, sc = synth.kvb_fmt8(H, seed=9)
+    swapped8 = w8.reshape(H, 2, 128, KL)[:, ::-1].reshape(H * 256, KL).copy()
+    swapped_sc = sc.reshape(H, 2, 4)[:, ::-1].reshape(H * 2, 4).copy()
+    rng = np.random.default_rng(6)
+    q = rng.standard_normal((1, H, 128)).astype(np.float32)
+    c = rng.standard_normal((1, 1, KL)).astype(np.float32)
+    q_lat = oracle.q_absorb(q, w8, sc)[0].astype(np.float64)                        # [H][512]
+    k_nope = oracle.out_project(np.repeat(c, H, axis=1), swapped8, swapped_sc)[0]    # [H][128] = W_UK c
+    absorbed = q_lat @ c[0, 0].astype(np.float64)
+    direct = np.einsum("hj,hj->h", q[0].astype(np.float64), k_nope.astype(np.float64))
+    np.testing.assert_allclose(absorbed, direct, rtol=1e-5, atol=1e-5 * np.abs(direct).max())
