@@ -35,6 +35,10 @@ cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t st);
 // need tc_scratch and (B-1)*seq_stride_rows + T < 2^31).
 cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st);
 size_t tc_scratch_bytes(int B, int P);
+cudaError_t launch_q_absorb(const void *q_nope, int q_bf16, int S, int H, const uint8_t *w8, const float *w_scale,
+                            void *q_lat, int out_bf16, cudaStream_t st);
+cudaError_t launch_out_project(const float *ctx, int S, int H, const uint8_t *w8, const float *w_scale, float *out,
+                               cudaStream_t st);
 cudaError_t launch_copy(void *dst, const void *src, size_t bytes, cudaStream_t st);
 cudaError_t launch_lse_merge(const float *ws, int B, int P, int H, float *out, cudaStream_t st);
 

@@ -10,6 +10,8 @@
  *   [B1]   "B1 Mixed FP8/BF16 FMHA first pass", sections "New files" (C ABI launcher driven from
  *          Python through ctypes) and "Intentional first-pass limits" (unsupported shapes are a
  *          hard error, not a fallback).
+ *   [FMT8] "feat: fmt=8 (fp8-e4m3) decode on the kv_b absorb path, CPU and CUDA" (colibri pull
+ *          request #1102): kv_b_proj as raw e4m3 bytes with one f32 scale per 128x128 block.
  *
  * Cache layout (one layer).  Row t of the latent cache is KV8_ROW_BYTES = 576 e4m3 bytes:
  * bytes 0..511 are Lc (kv_lora latent), bytes 512..575 are Rc (qk_rope key), followed in a separate
@@ -56,6 +58,9 @@ extern "C" {
 #define KV8_MAX_HEADS 128      /* query heads per call */
 #define KV8_MAX_ROWS (1 << 20) /* rows per cache: the 1M cap of [KV8] second commit */
 #define KV8_MAX_SELECT 4096    /* selected rows per sequence: NS <= 4096 ([KV8] second commit) */
+#define KV8_NOPE 128           /* per-head no-position query / key width (kv_b_proj key rows per head) */
+#define KV8_VHEAD 128          /* per-head value width (kv_b_proj value rows per head) */
+#define KV8_KVB_BLOCK 128      /* fmt=8 scale block edge: one f32 scale per 128x128 weight block */
 
 /* return codes */
 #define KV8_OK 0
@@ -195,6 +200,27 @@ KV8_API int mla_absorb_prefill8(const void *q_lat, const void *q_rope, int q_dty
 KV8_API int mla_absorb_decode8_noalloc(const void *q_lat, const void *q_rope, int q_dtype, int H,
                                        const uint8_t *kv8, const float *kv_scale, int64_t T, float sm_scale,
                                        int P_req, int *err_word, float *out, void *stream);
+
+/* -----------------------------------------------------------------------------------------------
+ * Absorb projections through kv_b_proj stored as fmt=8 ([FMT8] "feat: fmt=8 (fp8-e4m3) decode on
+ * the kv_b absorb path, CPU and CUDA": raw e4m3 bytes plus one f32 scale per 128x128 block,
+ * block-row-major; the absorbed attention of [KV8] first commit works in the 512-wide latent).
+ *   w8 [H*256][512] e4m3 bytes: head h's rows 256h..256h+127 are W_UK (no-position key part,
+ *      KV8_NOPE), rows 256h+128..256h+255 are W_UV (value part, KV8_VHEAD).
+ *   w_scale [H*2][4] f32: block (r, c) covers rows 128r.., columns 128c..; the weight is
+ *      W[o][i] = e4m3(w8[o][i]) * w_scale[(o/128)*4 + i/128].
+ * mla_q_absorb8:    q_lat[s][h][c] = sum_{j<128} q_nope[s][h][j] * W[256h + j][c]      (c < 512)
+ *   q_nope [S][H][128] of type q_dtype; q_lat [S][H][512] of type out_dtype (KV8_F32 / KV8_BF16;
+ *   bf16 rounds the f32 sum to nearest even) -- the query the decode / selection / prefill calls take.
+ * mla_out_project8: out[s][h][v] = sum_{c<512} W[256h + 128 + v][c] * ctx[s][h][c]     (v < 128)
+ *   ctx [S][H][512] f32 (a normalised context, e.g. mla_lse_merge8's out); out [S][H][128] f32.
+ * Sums in f32 over exactly decoded weights; the block scale is applied per 128-column block.
+ * S in [1, KV8_MAX_ROWS]; H in [1, 128]; all buffers 16-byte aligned; outputs must not overlap inputs.
+ * --------------------------------------------------------------------------------------------- */
+KV8_API int mla_q_absorb8(const void *q_nope, int q_dtype, int S, int H, const uint8_t *w8, const float *w_scale,
+                          void *q_lat, int out_dtype, void *stream);
+KV8_API int mla_out_project8(const float *ctx, int S, int H, const uint8_t *w8, const float *w_scale, float *out,
+                             void *stream);
 
 /* -----------------------------------------------------------------------------------------------
  * kv8_copy -- copy `bytes` bytes from src to dst with a kernel (the SMs' loads and stores, not a
