@@ -10,6 +10,8 @@ Other workloads (--workload), each one step of its own hot path:
   dec16k   the same decode step at T = 16384
   dsa      selected-row decode: 8 sequences x 2048 listed rows of a 131072-row cache each
   prefill  kv8_quant_rows of the chunk's 1024 fresh rows + causal prefill of 1024 queries over T = 65536
+  proj_dec / proj_prefill   the absorb projections through an fmt=8 kv_b (q_nope -> q_lat, context ->
+           head output) for 1 query / a 1024-query chunk of 128 heads
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload KEY]
 For N > 1 launch with torchrun; every rank runs an independent replica (one layer's attention does
@@ -150,19 +152,19 @@ def sources_digest(paths) -> str:
     return h.hexdigest()[:16]
 
 
-def traffic_file(key: str) -> str:
-    return os.path.join(ROOT, "profiles", f"{TC_KERNEL}_{key}_traffic.json")
+def traffic_file(key: str, kernel: str = TC_KERNEL) -> str:
+    return os.path.join(ROOT, "profiles", f"{kernel}_{key}_traffic.json")
 
 
-def traffic_per_launch(key: str):
+def traffic_per_launch(key: str, kernel: str = TC_KERNEL, sources=None):
     """DRAM bytes per launch of the dominant kernel from the committed ncu summary, or None when there
     is none for this workload or the kernel's sources changed since the counters were taken."""
-    path = traffic_file(key)
+    path = traffic_file(key, kernel)
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
-    if d.get("sources_digest") != sources_digest(TC_KERNEL_SOURCES):
+    if d.get("sources_digest") != sources_digest(sources or TC_KERNEL_SOURCES):
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -204,9 +206,24 @@ class Case:
     launches_per_step = 0
     kernel_calls = ""       # what the events around the dominant call bracket
     step_desc = ""
+    dtype = "e4m3*e4m3->f32"
 
     def config(self) -> dict:
         raise NotImplementedError
+
+    def roofline(self, kern_s: float, peaks: dict, key: str) -> dict:
+        """The attention kernel's roofline: a tensor-core contraction of e4m3 operands."""
+        hbm_gbs = self.alg_bytes / kern_s / 1e9
+        # the contraction is e4m3 x e4m3: its peak is the measured bf16 burst peak x 2 (nominal fp8/bf16 ratio)
+        peak = peaks["bf16_tflops"] * 2.0
+        achieved = self.flops / kern_s / 1e12
+        return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"fp8 = 2 x bf16 burst ({peaks['source']})",
+                "traffic": traffic_per_launch(key), "kernel": TC_KERNEL, "events_bracket": self.kernel_calls,
+                "mma_tflops_issued": MMA_PIECES * achieved, "mma_frac": MMA_PIECES * achieved / peak,
+                "bf16_equiv_frac": achieved / peaks["bf16_tflops"],
+                "algorithmic_bytes": self.alg_bytes, "algorithmic_flops": self.flops, "kernel_us": kern_s * 1e6,
+                "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / peaks["hbm_gbs"], "hbm_peak_gbs": peaks["hbm_gbs"]}
 
 
 class DecodeCase(Case):
@@ -450,9 +467,108 @@ class PrefillCase(Case):
         return (time.perf_counter() - t0) * self._scale
 
 
-CASES = {"dec262k": DecodeCase, "dec16k": DecodeCase, "dsa": SelectCase, "prefill": PrefillCase}
-ORACLE_HEADS = {"dec262k": 32, "dec16k": 128, "dsa": 128, "prefill": 8}
-REFERENCE_HEADS = {"dec262k": 8, "dec16k": 32, "dsa": 32, "prefill": 4}
+SIMT_F32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # 152 SMs x 128 f32 lanes x FMA x 2070 MHz = 80.5
+
+
+class ProjCase(Case):
+    """The absorb projections through an fmt=8 kv_b: q_nope -> q_lat (bf16, the attention's query) and a
+    context -> the head outputs, both on one stream.  A decode step (S = 1) reads every weight byte once
+    (HBM-bound); a prefill chunk (S = 1024) is f32 FMA work on the CUDA cores."""
+    launches_per_step = 2
+    kernel_calls = "mla_q_absorb8 + mla_out_project8"
+
+    @property
+    def unit(self):
+        return "us/chunk" if self.w.S > 1 else "us/layer-step"
+
+    step_desc = "q_nope -> q_lat (bf16) through the kv_b key rows + context -> head output through the value rows"
+    dtype = "e4m3*f32->f32"
+
+    def __init__(self, kv, torch, dev, w):
+        import synth
+        self.kv, self.torch, self.w = kv, torch, w
+        S, H = w.S, w.H
+        self.w8_np, self.sc_np = synth.kvb_fmt8(H)
+        self.w8 = torch.from_numpy(self.w8_np).to(dev)
+        self.wsc = torch.from_numpy(self.sc_np).to(dev)
+        self.q_nope = _bf16(torch, dev, synth.q_nope_for(w))
+        self.ctx = torch.from_numpy(synth.context_for(w)).to(dev)
+        self.q_lat = torch.empty((S, H, 512), dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty((S, H, 128), dtype=torch.float32, device=dev)
+        self.pack = Packed(torch, dev, [self.q_nope, self.ctx])
+        self.h_q_lat = torch.empty((S, H, 512), dtype=torch.bfloat16).pin_memory()
+        self.h_out = torch.empty((S, H, 128), dtype=torch.float32).pin_memory()
+        self.h2d = self.pack.nbytes
+        self.d2h = self.h_q_lat.numel() * 2 + self.h_out.numel() * 4
+        act = self.q_nope.numel() * 2 + self.q_lat.numel() * 2 + self.ctx.numel() * 4 + self.out.numel() * 4
+        self.alg_bytes = self.w8_np.nbytes + self.sc_np.nbytes + act
+        self.alg_bytes_step = self.alg_bytes
+        self.flops = 2.0 * S * H * 128 * 512 * 2  # two products of 128 x 512 per (row, head)
+
+    def step(self, stream, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        self.kernel_call(stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def kernel_call(self, stream):
+        self.kv.mla_q_absorb8(self.q_nope, self.w8, self.wsc, self.q_lat, stream=stream)
+        self.kv.mla_out_project8(self.ctx, self.w8, self.wsc, self.out, stream=stream)
+
+    def e2e_step(self, stream):
+        kv = self.kv
+        self.pack.upload(kv, stream)
+        q_nope, ctx = self.pack.views
+        kv.mla_q_absorb8(q_nope, self.w8, self.wsc, self.q_lat, stream=stream)
+        kv.mla_out_project8(ctx, self.w8, self.wsc, self.out, stream=stream)
+        kv.kv8_copy(self.h_q_lat, self.q_lat, stream=stream)
+        kv.kv8_copy(self.h_out, self.out, stream=stream)
+
+    def config(self):
+        return {"S": self.w.S, "H": self.w.H, "kv_b": "fmt=8: 128x256 rows x 512 e4m3 bytes, 128x128-block f32 scales"}
+
+    def roofline(self, kern_s, peaks, key):
+        hbm_gbs = self.alg_bytes / kern_s / 1e9
+        tflops = self.flops / kern_s / 1e12
+        common = {"kernel": "q_absorb + out_project (proj8.cu)", "events_bracket": self.kernel_calls,
+                  "traffic": traffic_per_launch(key, "proj8", ["fp8_latent_kv_gb300/csrc/proj8.cu"]),
+                  "algorithmic_bytes": self.alg_bytes, "algorithmic_flops": self.flops, "kernel_us": kern_s * 1e6,
+                  "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / peaks["hbm_gbs"], "hbm_peak_gbs": peaks["hbm_gbs"],
+                  "tflops": tflops}
+        if self.w.S <= 8:
+            return dict({"bound": "hbm", "achieved": hbm_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": hbm_gbs / peaks["hbm_gbs"], "peak_source": f"copy bandwidth ({peaks['source']})"},
+                        **common)
+        return dict({"bound": "alu", "achieved": tflops, "peak": SIMT_F32_PEAK_TFLOPS, "unit": "TFLOP/s",
+                     "frac": tflops / SIMT_F32_PEAK_TFLOPS,
+                     "peak_source": "152 SMs x 128 f32 lanes x 2 flop (FMA) x 2070 MHz (the maximum SM clock)"},
+                    **common)
+
+    def oracle_setup(self, n_rows):
+        import synth
+        w = self.w
+        if not hasattr(self, "w8_np"):
+            self.w8_np, self.sc_np = synth.kvb_fmt8(w.H)
+        rows = np.unique(np.linspace(0, w.S - 1, min(n_rows, w.S)).astype(int))
+        self._o = (np.ascontiguousarray(synth.q_nope_for(w)[rows]), np.ascontiguousarray(synth.context_for(w)[rows]))
+        self._scale = w.S / len(rows)
+        return f"{len(rows)} of {w.S} query rows, all {w.H} heads, both projections, scaled by rows to the whole step"
+
+    def oracle_step(self) -> float:
+        import oracle
+        q, x = self._o
+        t0 = time.perf_counter()
+        oracle.q_absorb(q, self.w8_np, self.sc_np)
+        oracle.out_project(x, self.w8_np, self.sc_np)
+        return (time.perf_counter() - t0) * self._scale
+
+
+CASES = {"dec262k": DecodeCase, "dec16k": DecodeCase, "dsa": SelectCase, "prefill": PrefillCase,
+         "proj_dec": ProjCase, "proj_prefill": ProjCase}
+# the oracle's sample: heads for the attention workloads, query rows for the projections
+ORACLE_HEADS = {"dec262k": 32, "dec16k": 128, "dsa": 128, "prefill": 8, "proj_dec": 1, "proj_prefill": 64}
+REFERENCE_HEADS = {"dec262k": 8, "dec16k": 32, "dsa": 32, "prefill": 4, "proj_dec": 1, "proj_prefill": 16}
 
 
 def SM_SCALE():
@@ -621,18 +737,7 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return
     peaks = measured_peaks()
-    kern_s = kern_ms_mean / 1e3
-    hbm_gbs = case.alg_bytes / kern_s / 1e9
-    # the contraction is e4m3 x e4m3: its peak is the measured bf16 burst peak x 2 (nominal fp8/bf16 ratio)
-    peak = peaks["bf16_tflops"] * 2.0
-    achieved = case.flops / kern_s / 1e12
-    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-            "peak_source": f"fp8 = 2 x bf16 burst ({peaks['source']})",
-            "traffic": traffic_per_launch(key), "kernel": TC_KERNEL, "events_bracket": case.kernel_calls,
-            "mma_tflops_issued": MMA_PIECES * achieved, "mma_frac": MMA_PIECES * achieved / peak,
-            "bf16_equiv_frac": achieved / peaks["bf16_tflops"],
-            "algorithmic_bytes": case.alg_bytes, "algorithmic_flops": case.flops, "kernel_us": kern_ms_mean * 1e3,
-            "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / peaks["hbm_gbs"], "hbm_peak_gbs": peaks["hbm_gbs"]}
+    roof = case.roofline(kern_ms_mean / 1e3, peaks, key)
 
     n_heads = ORACLE_HEADS[key]
     base = cpu_baseline(case, n_heads) if (world == 1 and not args.no_cpu_baseline) else None
@@ -646,7 +751,7 @@ def run_ours(args, rank, world, local_rank):
     line = {
         "metric": metric_for(key), "value": value, "unit": case.unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": False, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3*e4m3->f32", "data": "synthetic", "config": cfg,
+        "vs_baseline": None, "dtype": case.dtype, "data": "synthetic", "config": cfg,
         "step_hbm_gbs": case.alg_bytes_step / (ms_per_step / 1e3) / 1e9,
         "step_hbm_frac": case.alg_bytes_step / (ms_per_step / 1e3) / 1e9 / peaks["hbm_gbs"],
         "e2e": {"value": whole_job_us_per_step(e2e_ms, world), "unit": case.unit, "h2d_bytes_per_step": case.h2d,

@@ -195,9 +195,10 @@ __global__ void __launch_bounds__(256) q_absorb_tiled(const void *__restrict__ q
 }
 
 // ------------------------------------------------------------------------------------------------
-// out project, few rows.  CTA (h, 32 value rows): warp w takes rows 4w..4w+3 of them; per row each
-// lane reads 16 contiguous weight bytes (the warp one whole 512-byte row), multiplies by its 16
-// context values, scales by its block's factor (lanes 8b..8b+7 cover block b) and the warp sums.
+// out project, few rows.  CTA (h, 32 value rows): warp w takes rows 4w..4w+3 of them.  For a row, lane
+// l reads the 4 weight bytes at columns 128k + 4l (k = 0..3: one per scale block; each warp
+// instruction reads 128 contiguous bytes) and the matching context values (consecutive lanes,
+// consecutive 16 bytes of shared memory); each block's partial sum takes its scale, the warp sums.
 // ------------------------------------------------------------------------------------------------
 template <int NS>
 __global__ void __launch_bounds__(256) out_project_small(const float *__restrict__ ctx, int S, int H,
@@ -211,39 +212,36 @@ __global__ void __launch_bounds__(256) out_project_small(const float *__restrict
             s < S ? __ldg(reinterpret_cast<const float4 *>(ctx + ((int64_t)s * H + h) * kKL) + c4)
                   : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    uint4 wv[4];
+    uint32_t wv[4][kNbc];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-        const int v = v0 + 4 * warp + r;
-        wv[r] = __ldg(reinterpret_cast<const uint4 *>(w8 + ((int64_t)h * kKvbRows + kNope + v) * kKL) + lane);
+        const uint8_t *row = w8 + ((int64_t)h * kKvbRows + kNope + v0 + 4 * warp + r) * kKL + 4 * lane;
+#pragma unroll
+        for (int k = 0; k < kNbc; ++k) wv[r][k] = __ldg(reinterpret_cast<const uint32_t *>(row + k * kBlk));
     }
-    const float sc = __ldg(w_scale + (int64_t)(2 * h + 1) * kNbc + (lane >> 3));
+    float sc[kNbc];
+#pragma unroll
+    for (int k = 0; k < kNbc; ++k) sc[k] = __ldg(w_scale + (int64_t)(2 * h + 1) * kNbc + k);
     __syncthreads();
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-        float w[16];
-        const uint32_t u[4] = {wv[r].x, wv[r].y, wv[r].z, wv[r].w};
+        float4 w[kNbc];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float4 f = dec4(u[k]);
-            w[4 * k + 0] = f.x;
-            w[4 * k + 1] = f.y;
-            w[4 * k + 2] = f.z;
-            w[4 * k + 3] = f.w;
-        }
+        for (int k = 0; k < kNbc; ++k) w[k] = dec4(wv[r][k]);
 #pragma unroll
         for (int s = 0; s < NS; ++s) {
             if (s >= S) break;
             float a = 0.f;
 #pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {
-                const float4 x = *reinterpret_cast<const float4 *>(&xs[s][16 * lane + 4 * k4]);
-                a = fmaf(w[4 * k4 + 0], x.x, a);
-                a = fmaf(w[4 * k4 + 1], x.y, a);
-                a = fmaf(w[4 * k4 + 2], x.z, a);
-                a = fmaf(w[4 * k4 + 3], x.w, a);
+            for (int k = 0; k < kNbc; ++k) {
+                const float4 x = *reinterpret_cast<const float4 *>(&xs[s][k * kBlk + 4 * lane]);
+                float p = w[k].x * x.x;
+                p = fmaf(w[k].y, x.y, p);
+                p = fmaf(w[k].z, x.z, p);
+                p = fmaf(w[k].w, x.w, p);
+                a = fmaf(sc[k], p, a);
             }
-            a = warp_sum(a * sc);
+            a = warp_sum(a);
             if (lane == 0) out[((int64_t)s * H + h) * kVH + v0 + 4 * warp + r] = a;
         }
     }

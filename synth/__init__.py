@@ -14,6 +14,8 @@ Workloads (one query position = one decode step of one layer):
   3 dec262k   H=128, T=262144  as 2, plus a seeded 1% of rows times 50; q bf16
   4 dsa       B=8, H=128, T=131072 per sequence, NS=2048 sorted unique indices uniform in [0,T)
   5 prefill   S=1024, H=128, T=65536, pos0=64512; rows 64512.. are the fresh f32 rows; q bf16
+  6 proj_dec      absorb projections, S=1, H=128: q_nope N(0,1) bf16, context N(0,1) f32, fmt=8 kv_b
+  7 proj_prefill  the same for S=1024 query rows
 """
 from __future__ import annotations
 
@@ -52,6 +54,9 @@ WORKLOADS = {
     "dec262k": Workload("dec262k", 3, H=128, T=262144, heavy_frac=0.01, heavy_mult=50.0),
     "dsa": Workload("dsa", 4, H=128, T=131072, B=8, NS=2048),
     "prefill": Workload("prefill", 5, H=128, T=65536, S=1024, pos0=64512),
+    # the absorb projections through an fmt=8 kv_b, at a decode step and at a prefill chunk
+    "proj_dec": Workload("proj_dec", 6, H=128, T=0, S=1),
+    "proj_prefill": Workload("proj_prefill", 7, H=128, T=0, S=1024),
 }
 
 DESCRIPTIONS = {
@@ -61,6 +66,9 @@ DESCRIPTIONS = {
                "1 fresh row quantized per step, 1% of rows x50",
     "dsa": "DSA sparse decode: B=8 sequences x T=131072 rows, NS=2048 selected rows each, H=128, bf16 queries",
     "prefill": "causal prefill chunk: S=1024 queries at 64512..65535 over T=65536 rows, H=128, bf16 queries",
+    "proj_dec": "absorb projections at a decode step: 1 query x H=128 heads through an fmt=8 kv_b "
+                "(128x256 rows x 512, 128x128-block scales): q_nope -> q_lat and context -> head output",
+    "proj_prefill": "absorb projections for a prefill chunk: S=1024 queries x H=128 heads through an fmt=8 kv_b",
 }
 
 
@@ -162,7 +170,12 @@ def q_nope_for(w: Workload, n_query: int | None = None) -> np.ndarray:
     """The queries' no-position parts [nq][H][128] (f32 holding bf16-representable N(0,1) values unless
     the workload's queries are f32)."""
     if n_query is None:
-        n_query = w.S if w.key == "prefill" else w.B
+        n_query = w.S if w.S > 1 else w.B
     rng = rng_for(w, 4)
     q = normal_f32(rng, (n_query, w.H, NOPE))
     return q if w.q_f32 else to_bf16_values(q)
+
+
+def context_for(w: Workload) -> np.ndarray:
+    """A normalised-context stand-in [S][H][512] f32 N(0,1) for the output projection."""
+    return normal_f32(rng_for(w, 5), (max(w.S, w.B), w.H, KL))
