@@ -1,7 +1,7 @@
 // attn_simt.cu -- absorbed MLA attention over e4m3 cache rows on the CUDA cores (sm_103a).
 //
 // Page "KV8 long-context CUDA: fp8 device shadow, split-T kernels, DSA-aware gather":
-//   first commit message  -- the latent is both key and value; the row scale is hoisted out of the
+//   first commit message  -- the latent row serves as key and value; the row scale is hoisted out of the
 //                            dot (score = sm_scale * s_t * q.e4m3(row)); context = softmax-weighted
 //                            sum of s_t * e4m3(Lc_t).
 //   second commit message -- split-T: partial online-softmax blocks (cl[K], m, z) plus a log-sum-exp

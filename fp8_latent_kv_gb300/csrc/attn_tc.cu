@@ -3,8 +3,8 @@
 //
 // Page "KV8 long-context CUDA: fp8 device shadow, split-T kernels, DSA-aware gather":
 //   first commit message  -- score = sm_scale * s_t * q.e4m3(row) (the row scale hoisted out of the dot);
-//                            context = softmax-weighted sum of s_t * e4m3(Lc_t) (the latent is both key
-//                            and value).
+//                            context = softmax-weighted sum of s_t * e4m3(Lc_t) (the latent row serves
+//                            as the key and as the value).
 //   second commit message -- split-T: partial online-softmax blocks (cl[K], m, z) + log-sum-exp merge;
 //                            the batch/prefill path streams tiles of rows.
 //

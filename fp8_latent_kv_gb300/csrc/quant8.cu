@@ -1,9 +1,9 @@
 // quant8.cu -- e4m3 row quantizer and element encoder (sm_103a).
 //
 // Page "KV8 long-context CUDA: fp8 device shadow, split-T kernels, DSA-aware gather", first commit
-// message, c/kv_fp8.h item: RNE encoder that saturates at +-448, keeps signed zero and stores NaN as
-// inert 0; per-row quantizer with a per-row f32 amax/448 scale and a guard for a subnormal amax
-// (448/amax would overflow to +inf).
+// message, c/kv_fp8.h item: round-to-nearest-even encoder clamped to +-448 that keeps the sign of zero
+// and turns NaN into a zero byte; per-row quantizer with a per-row f32 amax/448 scale and a guard for
+// an amax so small that 448/amax is not finite.
 //
 // Design: one warp per 576-element row.  Each lane loads 4 or 5 float4 (coalesced 16-byte loads:
 // the row is 144 float4), the warp takes amax with a shuffle reduction, every f32 step is an

@@ -8,8 +8,8 @@
  *          commit message (device-resident shadow, split-T partial blocks + log-sum-exp merge,
  *          DSA gather attention_absorb_sel_kernel8 with NS <= 4096, batch cap lifted to 1M rows).
  *   [B1]   "B1 Mixed FP8/BF16 FMHA first pass", sections "New files" (C ABI launcher driven from
- *          Python through ctypes) and "Intentional first-pass limits" (unsupported shapes are a
- *          hard error, not a fallback).
+ *          Python through ctypes) and "Intentional first-pass limits" (an unsupported shape is an
+ *          error code; there is no fallback path).
  *   [FMT8] "feat: fmt=8 (fp8-e4m3) decode on the kv_b absorb path, CPU and CUDA" (colibri pull
  *          request #1102): kv_b_proj as raw e4m3 bytes with one f32 scale per 128x128 block.
  *
@@ -19,7 +19,8 @@
  * kv_scale is [T] f32.  The attended value of row t, head h:
  *     score[h,t] = sm_scale * s_t * ( q_lat[h].e4m3(Lc8_t) + q_rope[h].e4m3(Rc8_t) )
  *     cl[h]      = sum_t softmax_t(score[h,:]) * s_t * e4m3(Lc8_t)            (512 f32 per head)
- * ("the latent is both key and value"; the row scale is hoisted out of the dot: [KV8] first commit.)
+ * (The latent row serves as key and as value, and the row scale is applied outside the dot product:
+ * [KV8] first commit.)
  *
  * Conventions for every call:
  *   - Pointers are DEVICE pointers owned by the caller (unless stated).  The library allocates no

@@ -42,7 +42,7 @@ _Static_assert(FLT_EVAL_METHOD == 0, "f32 arithmetic must be evaluated in f32");
 #define KV8O_KR 64
 
 /* ---------------------------------------------------------------------------------------------
- * e4m3 decode, by the closed form of the format ([KV8] first commit: "256-entry decode LUT").
+ * e4m3 decode, by the closed form of the format ([KV8] first commit decodes through a table of all 256 codes).
  * byte b = s eeee mmm; e == 0 is subnormal (m * 2^-9); e == 15, m == 7 is NaN; otherwise
  * (1 + m/8) * 2^(e-7).  The largest finite magnitude is 0x7E = 448.
  * ------------------------------------------------------------------------------------------- */
@@ -81,8 +81,8 @@ void kv8o_e4m3_table(double *out256)
 }
 
 /* ---------------------------------------------------------------------------------------------
- * e4m3 encode ([KV8] first commit, c/kv_fp8.h item: round-to-nearest-even, saturating at
- * +-448, signed zero preserved, NaN stored as inert 0).
+ * e4m3 encode ([KV8] first commit, c/kv_fp8.h item: round to nearest with ties to even,
+ * clamped to +-448, the sign of zero kept, NaN turned into a zero byte).
  *
  * Definition used: the nearest of the 127 non-negative finite e4m3 magnitudes (codes 0x00..0x7E,
  * ascending), distance measured exactly in double; on an exact tie the code whose mantissa LSB is
@@ -203,8 +203,8 @@ int64_t kv8o_encode_change_points(uint32_t *out, int64_t cap)
 }
 
 /* ---------------------------------------------------------------------------------------------
- * Row quantizer ([KV8] first commit, c/kv_fp8.h item: "per-row quantizer with a subnormal-amax
- * guard (448/amax would overflow to +inf)"; the row format: e4m3 bytes with a per-row f32
+ * Row quantizer ([KV8] first commit, c/kv_fp8.h item: a per-row quantizer guarded against an
+ * amax so small that 448/amax overflows; the row format: e4m3 bytes with a per-row f32
  * amax/448 scale).  All arithmetic in f32 with IEEE round-to-nearest:
  *   amax  = max |x_i| over finite elements
  *   scale = amax / 448
@@ -263,7 +263,7 @@ void kv8o_dequant_rows(const uint8_t *q, const float *scale, int64_t n, double *
 
 /* ---------------------------------------------------------------------------------------------
  * Absorbed attention of one query head over a list of rows ([KV8] first commit, attention_rows
- * item: "the latent is both key and value"; absorb score loop dequantizes inline with the row
+ * item: the latent row serves as key and as value; the absorb score loop dequantizes inline with the row
  * scale hoisted out of the dot):
  *   score_t = sm_scale * s_t * ( sum_{i<512} q_lat[i] e4m3(Lc8_t[i]) + sum_{j<64} q_rope[j] e4m3(Rc8_t[j]) )
  *   cl[i]   = sum_t softmax(score)_t * s_t * e4m3(Lc8_t[i])
