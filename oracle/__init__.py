@@ -66,6 +66,9 @@ def _load():
             "kv8o_attn_select": (None, [P, P, i32, i32, P, P, i64, i64, P, i32, f32, P, P]),
             "kv8o_attn_prefill": (None, [P, P, i32, i32, P, P, P, i64, f32, P]),
             "kv8o_q_absorb": (None, [P, i32, i32, P, P, P]),
+            "kv8o_quant_rows_w": (None, [P, i64, i32, P, P]),
+            "kv8o_index_scores": (None, [P, P, P, i32, i32, i32, P, P, i64, i64, P]),
+            "kv8o_topk": (None, [P, i64, i32, P]),
             "kv8o_out_project": (None, [P, i32, i32, P, P, P]),
             "kv8o_num_threads": (i32, []),
             "kv8o_set_num_threads": (None, [i32]),
@@ -130,6 +133,16 @@ def quant_rows(x) -> tuple[np.ndarray, np.ndarray]:
     q = np.empty((n, D), dtype=np.uint8)
     s = np.empty(n, dtype=np.float32)
     _load().kv8o_quant_rows(_ptr(x), n, _ptr(q), _ptr(s))
+    return q, s
+
+
+def quant_rows_w(x, width: int) -> tuple[np.ndarray, np.ndarray]:
+    """Rows of any width [n][width] f32 -> (bytes [n][width] u8, scale [n] f32): the row quantizer above."""
+    x = _f32(x).reshape(-1, width)
+    n = x.shape[0]
+    q = np.empty((n, width), dtype=np.uint8)
+    s = np.empty(n, dtype=np.float32)
+    _load().kv8o_quant_rows_w(_ptr(x), n, int(width), _ptr(q), _ptr(s))
     return q, s
 
 
@@ -241,6 +254,31 @@ def out_project(ctx, w8, w_scale) -> np.ndarray:
     w8, w_scale = _kvb(w8, w_scale, H)
     out = np.empty(x.shape[:-1] + (VH,), dtype=np.float32)
     _load().kv8o_out_project(_ptr(x), S, H, _ptr(w8), _ptr(w_scale), _ptr(out))
+    return out
+
+
+def index_scores(q8, q_scale, w, k8, k_scale, T: int, seq_stride_rows: int) -> np.ndarray:
+    """Indexer scores [B][T] (double): q8 [B][HI][DI] u8, q_scale [B][HI], w [B][HI] f32, k8 [rows][DI] u8,
+    k_scale [rows] f32; item b's position t reads key row b * seq_stride_rows + t."""
+    q8 = np.ascontiguousarray(q8, dtype=np.uint8)
+    B, HI, DI = q8.shape
+    q_scale = _f32(q_scale).reshape(B, HI)
+    w = _f32(w).reshape(B, HI)
+    k8 = np.ascontiguousarray(k8, dtype=np.uint8).reshape(-1, DI)
+    k_scale = _f32(k_scale).reshape(-1)
+    assert (B - 1) * seq_stride_rows + T <= k8.shape[0] and k_scale.size == k8.shape[0]
+    out = np.empty((B, T), dtype=np.float64)
+    _load().kv8o_index_scores(_ptr(q8), _ptr(q_scale), _ptr(w), B, HI, DI, _ptr(k8), _ptr(k_scale), int(T),
+                              int(seq_stride_rows), _ptr(out))
+    return out
+
+
+def topk(scores, k: int) -> np.ndarray:
+    """Indices of the k largest scores (smaller index first among equals), ascending, int32."""
+    s = np.ascontiguousarray(scores, dtype=np.float64).reshape(-1)
+    kk = min(int(k), s.size)
+    out = np.empty(kk, dtype=np.int32)
+    _load().kv8o_topk(_ptr(s), s.size, int(k), _ptr(out))
     return out
 
 

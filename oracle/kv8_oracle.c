@@ -213,15 +213,15 @@ int64_t kv8o_encode_change_points(uint32_t *out, int64_t cap)
  *   inv overflows:       y_i = (x_i * 2^64) * (448 / (amax * 2^64))   (the guard)
  *   byte_i = encode(y_i)
  * ------------------------------------------------------------------------------------------- */
-void kv8o_quant_rows(const float *x, int64_t n, uint8_t *q, float *scale)
+void kv8o_quant_rows_w(const float *x, int64_t n, int width, uint8_t *q, float *scale)
 {
     lut_init();
 #pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < n; ++r) {
-        const float *xr = x + r * KV8O_D;
-        uint8_t *qr = q + r * KV8O_D;
+        const float *xr = x + r * width;
+        uint8_t *qr = q + r * width;
         float amax = 0.0f;
-        for (int i = 0; i < KV8O_D; ++i) {
+        for (int i = 0; i < width; ++i) {
             float a = fabsf(xr[i]);
             if (isfinite(a) && a > amax)
                 amax = a;
@@ -229,7 +229,7 @@ void kv8o_quant_rows(const float *x, int64_t n, uint8_t *q, float *scale)
         float s = amax / 448.0f;
         scale[r] = s;
         if (amax == 0.0f) {
-            for (int i = 0; i < KV8O_D; ++i)
+            for (int i = 0; i < width; ++i)
                 qr[i] = kv8o_e4m3_encode(xr[i]);
             continue;
         }
@@ -238,18 +238,24 @@ void kv8o_quant_rows(const float *x, int64_t n, uint8_t *q, float *scale)
             const float two64 = 18446744073709551616.0f; /* 2^64 */
             float amax_up = amax * two64;
             float inv_up = 448.0f / amax_up;
-            for (int i = 0; i < KV8O_D; ++i) {
+            for (int i = 0; i < width; ++i) {
                 float xi = xr[i] * two64;
                 float yi = xi * inv_up;
                 qr[i] = kv8o_e4m3_encode(yi);
             }
         } else {
-            for (int i = 0; i < KV8O_D; ++i) {
+            for (int i = 0; i < width; ++i) {
                 float yi = xr[i] * inv;
                 qr[i] = kv8o_e4m3_encode(yi);
             }
         }
     }
+}
+
+/* The cache rows: width 576. */
+void kv8o_quant_rows(const float *x, int64_t n, uint8_t *q, float *scale)
+{
+    kv8o_quant_rows_w(x, n, KV8O_D, q, scale);
 }
 
 /* Dequantize rows to double: value = table[byte] * scale (exact in double). */
@@ -503,6 +509,68 @@ void kv8o_out_project(const float *ctx, int S, int H, const uint8_t *w8, const f
             out[sh * KV8O_VH + v] = (float)acc;
         }
     }
+}
+
+/* ---------------------------------------------------------------------------------------------
+ * DSA lightning-indexer score and top-k ([B1] page, the indexer_fp8_score_topk commit: the index
+ * query (64 heads x 128) quantized from bf16 to e4m3, the index keys read as e4m3; dequantize with
+ * q_scale * k_scale, ReLU, weighted sum over the heads, then top-k).  Our reading of the formula:
+ *     I[b][t] = sum_h w[b][h] * max(0, q_scale[b][h] * k_scale[t'] * sum_i e4m3(q8[b][h][i]) e4m3(k8[t'][i]))
+ * with t' = b * seq_stride_rows + t the key row of item b's position t, and the scales the per-row
+ * amax/448 of the row quantizer above (index keys: rows of width DI; index query: one row per head).
+ * Products of two e4m3 values and their sums over DI <= 512 terms are exact in double.
+ * ------------------------------------------------------------------------------------------- */
+void kv8o_index_scores(const uint8_t *q8, const float *q_scale, const float *w, int B, int HI, int DI,
+                       const uint8_t *k8, const float *k_scale, int64_t T, int64_t seq_stride_rows, double *scores)
+{
+    lut_init();
+#pragma omp parallel for schedule(static)
+    for (int64_t bt = 0; bt < (int64_t)B * T; ++bt) {
+        const int b = (int)(bt / T);
+        const int64_t row = (int64_t)b * seq_stride_rows + (bt - (int64_t)b * T);
+        const uint8_t *kr = k8 + row * DI;
+        double acc = 0.0;
+        for (int h = 0; h < HI; ++h) {
+            const uint8_t *qr = q8 + ((int64_t)b * HI + h) * DI;
+            double dot = 0.0;
+            for (int i = 0; i < DI; ++i)
+                dot += g_lut[qr[i]] * g_lut[kr[i]];
+            const double v = (double)q_scale[b * HI + h] * (double)k_scale[row] * dot;
+            if (v > 0.0)
+                acc += (double)w[b * HI + h] * v;
+        }
+        scores[bt] = acc;
+    }
+}
+
+/* The k largest of n scores, the smaller index first among equal scores; indices returned in
+ * ascending order (the order the selected-row attention takes them in). */
+static const double *g_topk_scores;
+static int topk_cmp(const void *a, const void *b)
+{
+    const int64_t i = *(const int64_t *)a, j = *(const int64_t *)b;
+    const double si = g_topk_scores[i], sj = g_topk_scores[j];
+    if (si != sj)
+        return si > sj ? -1 : 1;
+    return i < j ? -1 : (i > j ? 1 : 0);
+}
+static int idx_cmp(const void *a, const void *b)
+{
+    const int32_t i = *(const int32_t *)a, j = *(const int32_t *)b;
+    return i < j ? -1 : (i > j ? 1 : 0);
+}
+void kv8o_topk(const double *scores, int64_t n, int k, int32_t *idx)
+{
+    int64_t *order = (int64_t *)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1));
+    for (int64_t i = 0; i < n; ++i)
+        order[i] = i;
+    g_topk_scores = scores;  /* single-threaded: qsort has no context argument in C11 */
+    qsort(order, (size_t)n, sizeof(int64_t), topk_cmp);
+    const int kk = (int64_t)k < n ? k : (int)n;
+    for (int i = 0; i < kk; ++i)
+        idx[i] = (int32_t)order[i];
+    qsort(idx, (size_t)kk, sizeof(int32_t), idx_cmp);
+    free(order);
 }
 
 int kv8o_num_threads(void)

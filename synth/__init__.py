@@ -16,6 +16,8 @@ Workloads (one query position = one decode step of one layer):
   5 prefill   S=1024, H=128, T=65536, pos0=64512; rows 64512.. are the fresh f32 rows; q bf16
   6 proj_dec      absorb projections, S=1, H=128: q_nope N(0,1) bf16, context N(0,1) f32, fmt=8 kv_b
   7 proj_prefill  the same for S=1024 query rows
+  8 indexer   B=8 queries x 64 index heads x 128 (bf16 N(0,1)), head weights N(0,1)/8; per query its own
+              T=131072 index-key rows N(0,1)*10^U(-0.5,0.5) of width 128; top NS=2048
 """
 from __future__ import annotations
 
@@ -57,6 +59,8 @@ WORKLOADS = {
     # the absorb projections through an fmt=8 kv_b, at a decode step and at a prefill chunk
     "proj_dec": Workload("proj_dec", 6, H=128, T=0, S=1),
     "proj_prefill": Workload("proj_prefill", 7, H=128, T=0, S=1024),
+    # the DSA lightning indexer that chooses the selection: 64 index heads of width 128 per query
+    "indexer": Workload("indexer", 8, H=64, T=131072, B=8, NS=2048, mag_lo=10 ** -0.5, mag_hi=10 ** 0.5),
 }
 
 DESCRIPTIONS = {
@@ -69,6 +73,8 @@ DESCRIPTIONS = {
     "proj_dec": "absorb projections at a decode step: 1 query x H=128 heads through an fmt=8 kv_b "
                 "(128x256 rows x 512, 128x128-block scales): q_nope -> q_lat and context -> head output",
     "proj_prefill": "absorb projections for a prefill chunk: S=1024 queries x H=128 heads through an fmt=8 kv_b",
+    "indexer": "DSA lightning indexer: B=8 queries, each scoring its own T=131072 e4m3 index keys (width 128) "
+               "with 64 index heads, then top-2048",
 }
 
 
@@ -179,3 +185,34 @@ def q_nope_for(w: Workload, n_query: int | None = None) -> np.ndarray:
 def context_for(w: Workload) -> np.ndarray:
     """A normalised-context stand-in [S][H][512] f32 N(0,1) for the output projection."""
     return normal_f32(rng_for(w, 5), (max(w.S, w.B), w.H, KL))
+
+
+IDX_D = 128  # index head / key width
+
+
+def index_keys_for(w: Workload, seq: int = 0, start: int = 0, count: int | None = None) -> np.ndarray:
+    """Index-key rows [count][128] f32 of sequence `seq`: N(0,1) times a per-row magnitude
+    10^U(log10 mag_lo, log10 mag_hi), drawn in blocks of 4096 rows so any sub-range reproduces."""
+    if count is None:
+        count = w.T - start
+    out = np.empty((count, IDX_D), dtype=np.float32)
+    blk = 4096
+    b0, b1 = start // blk, (start + count + blk - 1) // blk
+    for bi in range(b0, b1):
+        rng = np.random.default_rng([w.seed, 6, seq, bi])
+        x = normal_f32(rng, (blk, IDX_D))
+        mag = 10.0 ** rng.uniform(np.log10(w.mag_lo), np.log10(w.mag_hi), blk)
+        x = (x * mag[:, None]).astype(np.float32)
+        lo, hi = max(start, bi * blk), min(start + count, (bi + 1) * blk)
+        out[lo - start:hi - start] = x[lo - bi * blk:hi - bi * blk]
+    return out
+
+
+def index_queries_for(w: Workload) -> np.ndarray:
+    """Index queries [B][64][128]: bf16-representable N(0,1)."""
+    return to_bf16_values(normal_f32(rng_for(w, 7), (w.B, w.H, IDX_D)))
+
+
+def index_weights_for(w: Workload) -> np.ndarray:
+    """Per-query head weights [B][64] f32: N(0,1)/8 (either sign)."""
+    return (normal_f32(rng_for(w, 8), (w.B, w.H)) / np.float32(8.0)).astype(np.float32)

@@ -525,3 +525,90 @@ def test_absorbed_score_equals_unabsorbed_score(oracle):
     absorbed = q_lat @ c[0, 0].astype(np.float64)
     direct = np.einsum("hj,hj->h", q[0].astype(np.float64), k_nope.astype(np.float64))
     np.testing.assert_allclose(absorbed, direct, rtol=1e-5, atol=1e-5 * np.abs(direct).max())
+
+
+# ------------------------------------------------------------------------------------------------
+# DSA lightning indexer: quantized index query / keys, ReLU-weighted head sum, top-k
+# ------------------------------------------------------------------------------------------------
+def test_quant_rows_any_width_matches_torch(oracle):
+    """Width-128 rows (index keys, index query heads) through the same row quantizer = torch's f32
+    amax / multiply-by-448/amax / float8_e4m3fn conversion."""
+    rng = np.random.default_rng(20)
+    x = (rng.standard_normal((300, 128)) * 10.0 ** rng.uniform(-3, 3, (300, 1))).astype(np.float32)
+    q, s = oracle.quant_rows_w(x, 128)
+    t = torch.from_numpy(x)
+    amax = t.abs().amax(dim=1, keepdim=True)
+    y = t * (torch.tensor(448.0, dtype=torch.float32) / amax)
+    assert np.array_equal(q, torch_e4m3(y.numpy()))
+    assert np.array_equal(s, (amax[:, 0] / torch.tensor(448.0, dtype=torch.float32)).numpy())
+    # width 576 through the generic entry = the cache-row quantizer
+    x5 = rng.standard_normal((7, 576)).astype(np.float32)
+    a, b = oracle.quant_rows(x5), oracle.quant_rows_w(x5, 576)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def _index_case(seed, B=2, HI=5, T=37, stride=50):
+    rng = np.random.default_rng(seed)
+    qf = rng.standard_normal((B, HI, 128)).astype(np.float32)
+    import oracle as o
+    q8, qs = o.quant_rows_w(qf.reshape(B * HI, 128), 128)
+    kf = (rng.standard_normal(((B - 1) * stride + T, 128)) * 10.0 ** rng.uniform(-1, 1, (((B - 1) * stride + T), 1))).astype(np.float32)
+    k8, ks = o.quant_rows_w(kf, 128)
+    w = rng.standard_normal((B, HI)).astype(np.float32)
+    return q8.reshape(B, HI, 128), qs.reshape(B, HI), w, k8, ks, T, stride
+
+
+def test_index_scores_match_a_double_einsum(oracle):
+    q8, qs, w, k8, ks, T, stride = _index_case(21)
+    B, HI, _ = q8.shape
+    dq = torch.from_numpy(q8).view(torch.float8_e4m3fn).to(torch.float64).numpy() * qs[..., None].astype(np.float64)
+    dk = torch.from_numpy(k8).view(torch.float8_e4m3fn).to(torch.float64).numpy() * ks[:, None].astype(np.float64)
+    want = np.zeros((B, T))
+    for b in range(B):
+        dots = dq[b] @ dk[b * stride:b * stride + T].T          # [HI][T]
+        want[b] = (w[b].astype(np.float64)[:, None] * np.maximum(dots, 0.0)).sum(axis=0)
+    got = oracle.index_scores(q8, qs, w, k8, ks, T, stride)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12 * np.abs(want).max())
+
+
+def test_index_score_single_element_closed_form(oracle):
+    """One head whose query is a single 1.0 at position j (q_scale 1), weight 2: I_t = 2 max(0, k_scale_t * key_t[j])."""
+    T, j = 40, 77
+    rng = np.random.default_rng(22)
+    k8, ks = oracle.quant_rows_w(rng.standard_normal((T, 128)).astype(np.float32), 128)
+    q8 = np.zeros((1, 1, 128), np.uint8)
+    q8[0, 0, j] = 0x38
+    got = oracle.index_scores(q8, np.ones((1, 1), np.float32), np.full((1, 1), 2.0, np.float32), k8, ks, T, 0)
+    key = torch.from_numpy(k8[:, j].copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(got[0], 2.0 * np.maximum(ks.astype(np.float64) * key, 0.0))
+
+
+def test_index_scores_relu_and_linearity(oracle):
+    q8, qs, w, k8, ks, T, stride = _index_case(23)
+    base = oracle.index_scores(q8, qs, w, k8, ks, T, stride)
+    # negating a head's query (sign bit of every byte) swaps which rows its ReLU passes
+    neg = q8.copy()
+    neg[:, 0] ^= 0x80
+    only0 = np.zeros_like(w)
+    only0[:, 0] = w[:, 0]
+    pos_part = oracle.index_scores(q8, qs, only0, k8, ks, T, stride)
+    neg_part = oracle.index_scores(neg, qs, only0, k8, ks, T, stride)
+    assert np.all((pos_part == 0) | (neg_part == 0)), "a row passes the ReLU for q or for -q, not both"
+    # the weights enter linearly; permuting heads together with their weights changes nothing
+    np.testing.assert_allclose(oracle.index_scores(q8, qs, 2 * w, k8, ks, T, stride), 2 * base, rtol=1e-15, atol=0)
+    perm = np.array([3, 1, 4, 0, 2])
+    np.testing.assert_allclose(oracle.index_scores(q8[:, perm], qs[:, perm], w[:, perm], k8, ks, T, stride), base,
+                               rtol=1e-12, atol=1e-12 * np.abs(base).max())
+
+
+def test_topk_ties_order_and_brute_force(oracle):
+    assert list(oracle.topk(np.array([3.0, 1.0, 3.0, 2.0, 3.0]), 2)) == [0, 2]   # ties: the smaller index
+    assert list(oracle.topk(np.array([3.0, 1.0, 3.0, 2.0, 3.0]), 4)) == [0, 2, 3, 4]
+    assert list(oracle.topk(np.array([1.0, 2.0]), 5)) == [0, 1]                  # k > n: every index
+    rng = np.random.default_rng(24)
+    for n, k in ((1, 1), (10, 3), (1000, 100), (5000, 2048)):
+        s = np.round(rng.standard_normal(n), 1)  # many ties
+        got = oracle.topk(s, k)
+        order = sorted(range(n), key=lambda i: (-s[i], i))[:k]
+        assert list(got) == sorted(order)
+        assert np.all(np.diff(got) > 0)
