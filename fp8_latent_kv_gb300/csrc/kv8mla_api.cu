@@ -93,6 +93,29 @@ const char *kv8_strerror(int code) {
     }
 }
 
+int kv8_quant_rows_w(const float *x, int64_t n, int width, uint8_t *q, float *scale, void *stream) {
+    if (n < 0 || (width != KV8_ROW_BYTES && width != KV8_IDX_D)) return KV8_EINVAL;
+    if (n == 0) return KV8_OK;
+    if (!aligned(x, 16) || !aligned(q, 16) || !aligned(scale, 4)) return KV8_EINVAL;
+    return status(launch_quant_rows_w(x, n, width, q, scale, (cudaStream_t)stream));
+}
+
+int dsa_index_topk8(const void *q_idx, int q_dtype, const float *w, int B, int HI, const uint8_t *k8,
+                    const float *k_scale, int64_t T, int64_t seq_stride_rows, int NS, float *scores, int32_t *idx,
+                    int *err_word, void *stream) {
+    if (B < 1 || HI < 16 || HI > KV8_MAX_IDX_HEADS || HI % 16 != 0 || T < 1 || T > KV8_MAX_ROWS || NS < 1 ||
+        NS > KV8_MAX_SELECT || seq_stride_rows < 0)
+        return KV8_EINVAL;
+    if ((int64_t)(B - 1) * seq_stride_rows + T >= (1LL << 31) - 128) return KV8_EINVAL;
+    if ((q_dtype != KV8_F32 && q_dtype != KV8_BF16) || !aligned(q_idx, 16) || !aligned(w, 4) || !aligned(k8, 16) ||
+        !aligned(k_scale, 4) || !aligned(scores, 16) || !aligned(idx, 16))
+        return KV8_EINVAL;
+    cudaError_t e = launch_index_scores(q_idx, q_dtype == KV8_BF16, w, B, HI, k8, k_scale, T, seq_stride_rows, scores,
+                                        err_word, (cudaStream_t)stream);
+    if (e != cudaSuccess) return KV8_ECUDA;
+    return status(launch_topk(scores, B, T, NS, idx, (cudaStream_t)stream));
+}
+
 int mla_q_absorb8(const void *q_nope, int q_dtype, int S, int H, const uint8_t *w8, const float *w_scale,
                   void *q_lat, int out_dtype, void *stream) {
     if (S < 1 || S > KV8_MAX_ROWS || H < 1 || H > KV8_MAX_HEADS) return KV8_EINVAL;

@@ -62,6 +62,8 @@ extern "C" {
 #define KV8_NOPE 128           /* per-head no-position query / key width (kv_b_proj key rows per head) */
 #define KV8_VHEAD 128          /* per-head value width (kv_b_proj value rows per head) */
 #define KV8_KVB_BLOCK 128      /* fmt=8 scale block edge: one f32 scale per 128x128 weight block */
+#define KV8_IDX_D 128          /* DSA indexer: index key / index query head width */
+#define KV8_MAX_IDX_HEADS 128  /* DSA indexer: index heads per query (a multiple of 16) */
 
 /* return codes */
 #define KV8_OK 0
@@ -100,6 +102,11 @@ KV8_API int kv8_encode_e4m3(const float *y, int64_t n, uint8_t *out, void *strea
  *   n >= 0.  x and kv8 16-byte aligned, kv_scale 4-byte aligned.
  * --------------------------------------------------------------------------------------------- */
 KV8_API int kv8_quant_rows(const float *x, int64_t n, uint8_t *kv8, float *kv_scale, void *stream);
+
+/* kv8_quant_rows_w -- the same row quantizer for rows of `width` elements: width = KV8_ROW_BYTES (cache
+ * rows, as kv8_quant_rows) or KV8_IDX_D (DSA index keys).  x [n][width] f32 -> q [n][width] e4m3,
+ * scale [n] f32.  Any other width is KV8_EINVAL. */
+KV8_API int kv8_quant_rows_w(const float *x, int64_t n, int width, uint8_t *q, float *scale, void *stream);
 
 /* -----------------------------------------------------------------------------------------------
  * Split-T decode ([KV8] second commit: flash-decoding style partial online-softmax blocks
@@ -222,6 +229,26 @@ KV8_API int mla_q_absorb8(const void *q_nope, int q_dtype, int S, int H, const u
                           void *q_lat, int out_dtype, void *stream);
 KV8_API int mla_out_project8(const float *ctx, int S, int H, const uint8_t *w8, const float *w_scale, float *out,
                              void *stream);
+
+/* -----------------------------------------------------------------------------------------------
+ * dsa_index_topk8 -- the DSA lightning indexer and its top-k ([B1] page, the commit adding
+ * indexer_fp8_score_topk: an e4m3 index query of 64 heads x 128 quantized from bf16, e4m3 index keys
+ * read as they are, the score dequantized by q_scale * k_scale, ReLU, weighted sum over the heads,
+ * top-k).  For each of B queries b and each position t < T of its key rows t' = b*seq_stride_rows + t:
+ *     I[b][t] = sum_h w[b][h] * max(0, q_scale[b][h] * k_scale[t'] * sum_i e4m3(q8[b][h][i]) e4m3(k8[t'][i]))
+ * where (q8[b][h], q_scale[b][h]) is the row quantizer applied to q_idx[b][h] (amax/448 per head row).
+ *   q_idx [B][HI][128] of type q_dtype (KV8_F32 / KV8_BF16); w [B][HI] f32 (either sign);
+ *   k8 [rows][128] e4m3 and k_scale [rows] f32 as written by kv8_quant_rows_w(width = KV8_IDX_D).
+ *   scores [B][T] f32 (written: I); idx [B][NS] int32 (written): the min(NS, T) positions with the
+ *   largest scores, the smaller position first among equal scores, in ascending position order -- the
+ *   selection list mla_absorb_sel8 takes.
+ *   HI a multiple of 16 in [16, KV8_MAX_IDX_HEADS]; T in [1, KV8_MAX_ROWS]; NS in [1, KV8_MAX_SELECT];
+ *   seq_stride_rows >= 0 and (B-1)*seq_stride_rows + T < 2^31 - 128; buffers 16-byte aligned.
+ *   err_word: optional (KV8_ERR_TIMEOUT).  The scores run on the tensor cores (e4m3 x e4m3, f32 sums).
+ * --------------------------------------------------------------------------------------------- */
+KV8_API int dsa_index_topk8(const void *q_idx, int q_dtype, const float *w, int B, int HI, const uint8_t *k8,
+                            const float *k_scale, int64_t T, int64_t seq_stride_rows, int NS, float *scores,
+                            int32_t *idx, int *err_word, void *stream);
 
 /* -----------------------------------------------------------------------------------------------
  * kv8_copy -- copy `bytes` bytes from src to dst with a kernel (the SMs' loads and stores, not a
