@@ -12,6 +12,7 @@ Other workloads (--workload), each one step of its own hot path:
   prefill  kv8_quant_rows of the chunk's 1024 fresh rows + causal prefill of 1024 queries over T = 65536
   proj_dec / proj_prefill   the absorb projections through an fmt=8 kv_b (q_nope -> q_lat, context ->
            head output) for 1 query / a 1024-query chunk of 128 heads
+  indexer  the DSA lightning indexer: 8 queries x 64 index heads over 131072 e4m3 index keys each, top-2048
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload KEY]
 For N > 1 launch with torchrun; every rank runs an independent replica (one layer's attention does
@@ -564,11 +565,106 @@ class ProjCase(Case):
         return (time.perf_counter() - t0) * self._scale
 
 
+class IndexerCase(Case):
+    """The DSA lightning indexer for B queries: e4m3 index keys streamed from HBM through the tensor cores
+    (scores), then the top-NS positions of each query."""
+    launches_per_step = 2  # score kernel + top-k kernel (plus a memset of the top-k's counters)
+    kernel_calls = "dsa_index_topk8: index_score_kernel + topk_kernel"
+    step_desc = "index scores (e4m3 query x e4m3 keys, ReLU-weighted head sum) + top-2048 per query"
+    dtype = "e4m3*e4m3->f32"
+
+    def __init__(self, kv, torch, dev, w):
+        import synth
+        self.kv, self.torch, self.w = kv, torch, w
+        B, T, HI = w.B, w.T, w.H
+        self.k8 = torch.empty((B * T, 128), dtype=torch.uint8, device=dev)
+        self.ks = torch.empty(B * T, dtype=torch.float32, device=dev)
+        for b in range(B):
+            rows = torch.from_numpy(synth.index_keys_for(w, b)).to(dev)
+            kv.kv8_quant_rows_w(rows, self.k8[b * T:(b + 1) * T], self.ks[b * T:(b + 1) * T])
+            del rows
+        self.q = _bf16(torch, dev, synth.index_queries_for(w))
+        self.wts = torch.from_numpy(synth.index_weights_for(w)).to(dev)
+        self.scores = torch.empty((B, T), dtype=torch.float32, device=dev)
+        self.idx = torch.empty((B, w.NS), dtype=torch.int32, device=dev)
+        self.ws = torch.empty(kv.dsa_index_workspace_bytes(B) // 4, dtype=torch.int32, device=dev)
+        self.pack = Packed(torch, dev, [self.q, self.wts])
+        self.h_idx = torch.empty((B, w.NS), dtype=torch.int32).pin_memory()
+        self.h2d = self.pack.nbytes
+        self.d2h = self.h_idx.numel() * 4
+        self.alg_bytes = (B * T * (128 + 4) + self.q.numel() * 2 + self.wts.numel() * 4 + B * T * 4
+                          + self.idx.numel() * 4)
+        self.alg_bytes_step = self.alg_bytes
+        self.flops = 2.0 * B * T * HI * 128
+
+    def _call(self, q, wts, stream):
+        w = self.w
+        self.kv.dsa_index_topk8(q, wts, self.k8, self.ks, w.T, w.T, w.NS, self.ws, self.scores, self.idx,
+                                stream=stream)
+
+    def step(self, stream, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        self._call(self.q, self.wts, stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def kernel_call(self, stream):
+        self._call(self.q, self.wts, stream)
+
+    def e2e_step(self, stream):
+        kv = self.kv
+        self.pack.upload(kv, stream)
+        q, wts = self.pack.views
+        self._call(q, wts, stream)
+        kv.kv8_copy(self.h_idx, self.idx, stream=stream)
+
+    def config(self):
+        w = self.w
+        return {"B": w.B, "T": w.T, "index_heads": w.H, "index_dim": 128, "NS": w.NS}
+
+    def roofline(self, kern_s, peaks, key):
+        hbm_gbs = self.alg_bytes / kern_s / 1e9
+        tflops = self.flops / kern_s / 1e12
+        return {"bound": "hbm", "achieved": hbm_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": hbm_gbs / peaks["hbm_gbs"], "peak_source": f"copy bandwidth ({peaks['source']})",
+                "kernel": "index_score_kernel + topk_kernel (indexer.cu)", "events_bracket": self.kernel_calls,
+                "traffic": traffic_per_launch(key, "index_score_kernel", ["fp8_latent_kv_gb300/csrc/indexer.cu"]),
+                "algorithmic_bytes": self.alg_bytes, "algorithmic_flops": self.flops, "kernel_us": kern_s * 1e6,
+                "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / peaks["hbm_gbs"], "hbm_peak_gbs": peaks["hbm_gbs"],
+                "tflops": tflops, "tensor_frac_of_fp8_peak": tflops / (2.0 * peaks["bf16_tflops"])}
+
+    def oracle_setup(self, n_seq):
+        import oracle
+        import synth
+        w = self.w
+        n_seq = max(1, min(n_seq, w.B))
+        q8, qs = oracle.quant_rows_w(synth.index_queries_for(w).reshape(w.B * w.H, 128), 128)
+        q8, qs = q8.reshape(w.B, w.H, 128), qs.reshape(w.B, w.H)
+        wts = synth.index_weights_for(w)
+        keys = [oracle.quant_rows_w(synth.index_keys_for(w, b), 128) for b in range(n_seq)]
+        self._o = (q8[:n_seq], qs[:n_seq], wts[:n_seq], keys)
+        self._scale = w.B / n_seq
+        return (f"{n_seq} of {w.B} queries over all T={w.T} index keys (the index query quantized first), "
+                f"scaled by queries to the whole step")
+
+    def oracle_step(self) -> float:
+        import oracle
+        q8, qs, wts, keys = self._o
+        t0 = time.perf_counter()
+        for b, (k8, ks) in enumerate(keys):
+            sc = oracle.index_scores(q8[b:b + 1], qs[b:b + 1], wts[b:b + 1], k8, ks, self.w.T, 0)
+            oracle.topk(sc[0], self.w.NS)
+        return (time.perf_counter() - t0) * self._scale
+
+
 CASES = {"dec262k": DecodeCase, "dec16k": DecodeCase, "dsa": SelectCase, "prefill": PrefillCase,
-         "proj_dec": ProjCase, "proj_prefill": ProjCase}
+         "proj_dec": ProjCase, "proj_prefill": ProjCase, "indexer": IndexerCase}
 # the oracle's sample: heads for the attention workloads, query rows for the projections
-ORACLE_HEADS = {"dec262k": 32, "dec16k": 128, "dsa": 128, "prefill": 8, "proj_dec": 1, "proj_prefill": 64}
-REFERENCE_HEADS = {"dec262k": 8, "dec16k": 32, "dsa": 32, "prefill": 4, "proj_dec": 1, "proj_prefill": 16}
+ORACLE_HEADS = {"dec262k": 32, "dec16k": 128, "dsa": 128, "prefill": 8, "proj_dec": 1, "proj_prefill": 64,
+                "indexer": 1}
+REFERENCE_HEADS = {"dec262k": 8, "dec16k": 32, "dsa": 32, "prefill": 4, "proj_dec": 1, "proj_prefill": 16,
+                   "indexer": 1}
 
 
 def SM_SCALE():

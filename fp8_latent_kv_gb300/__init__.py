@@ -35,7 +35,8 @@ SIGNATURES = {
     "mla_absorb_decode8_noalloc": (_I, [_P, _P, _I, _I, _P, _P, _I64, _F, _I, _P, _P, _P]),
     "mla_q_absorb8": (_I, [_P, _I, _I, _I, _P, _P, _P, _I, _P]),
     "kv8_quant_rows_w": (_I, [_P, _I64, _I, _P, _P, _P]),
-    "dsa_index_topk8": (_I, [_P, _I, _P, _I, _I, _P, _P, _I64, _I64, _I, _P, _P, _P, _P]),
+    "dsa_index_workspace_bytes": (_I, [_I, _P]),
+    "dsa_index_topk8": (_I, [_P, _I, _P, _I, _I, _P, _P, _I64, _I64, _I, _P, _SZ, _P, _P, _P, _P]),
     "mla_out_project8": (_I, [_P, _I, _I, _P, _P, _P, _P]),
     "kv8_copy": (_I, [_P, _P, _SZ, _P]),
     "kv8_strerror": (ctypes.c_char_p, [_I]),
@@ -136,14 +137,21 @@ def kv8_quant_rows_w(x, q, scale, stream=None) -> None:
     _check("kv8_quant_rows_w", load().kv8_quant_rows_w(_ptr(x), n, width, _ptr(q), _ptr(scale), _stream(stream)))
 
 
-def dsa_index_topk8(q_idx, w, k8, k_scale, T: int, seq_stride_rows: int, NS: int, scores, idx, err_word=None,
-                    stream=None) -> None:
+def dsa_index_workspace_bytes(B: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check("dsa_index_workspace_bytes", load().dsa_index_workspace_bytes(B, ctypes.addressof(out)))
+    return out.value
+
+
+def dsa_index_topk8(q_idx, w, k8, k_scale, T: int, seq_stride_rows: int, NS: int, workspace, scores, idx,
+                    err_word=None, stream=None) -> None:
     """DSA indexer: q_idx [B][HI][128] (f32/bf16), w [B][HI] f32, index keys k8 [rows][128] uint8 + k_scale
     [rows] f32 -> scores [B][T] f32 and idx [B][NS] int32 (top positions, ascending)."""
     B, HI = q_idx.shape[0], q_idx.shape[1]
-    _check("dsa_index_topk8", load().dsa_index_topk8(_ptr(q_idx), _qdtype(q_idx), _ptr(w), B, HI, _ptr(k8),
-                                                     _ptr(k_scale), T, seq_stride_rows, NS, _ptr(scores), _ptr(idx),
-                                                     _ptr(err_word), _stream(stream)))
+    _check("dsa_index_topk8", load().dsa_index_topk8(
+        _ptr(q_idx), _qdtype(q_idx), _ptr(w), B, HI, _ptr(k8), _ptr(k_scale), T, seq_stride_rows, NS,
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(scores), _ptr(idx), _ptr(err_word),
+        _stream(stream)))
 
 
 def mla_q_absorb8(q_nope, w8, w_scale, q_lat, stream=None) -> None:

@@ -14,9 +14,10 @@
 // read a row's HI scores, apply the ReLU and weights and store the row's score.  The CTA quantizes its
 // query's HI heads itself (same f32 steps as the row quantizer).  Every wait is bounded in time.
 //
-// top-k kernel: one CTA per query; a radix select over the scores' order-preserving 32-bit keys
-// (11 + 11 + 10 bits) finds the k-th largest key, then an index-ordered pass keeps every larger score
-// and, among scores equal to the k-th, the smallest positions -- written in ascending position order.
+// top-k kernel: a radix select over the scores' order-preserving 32-bit keys (11 + 11 + 10 bits) finds
+// the k-th largest key, then an index-ordered pass keeps every larger score and, among scores equal to
+// the k-th, the smallest positions -- written in ascending position order.  Each query's positions are
+// split over several CTAs of one cooperative launch that meet at bounded barriers.
 #include "internal.h"
 #include "quant_row.cuh"
 #include "sm100.cuh"
@@ -31,7 +32,7 @@ using namespace sm100;
 
 constexpr int kIdxD = KV8_IDX_D;  // 128 bytes per key row and per query head
 constexpr int kITile = 128;       // key rows per tile (MMA M)
-constexpr int kIStages = 6;
+constexpr int kIStages = 12;
 constexpr int kIAcc = 4;          // TMEM accumulator buffers
 constexpr int kIThreads = 192;    // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr uint32_t kIStageBytes = kITile * kIdxD;  // 16 KB
@@ -40,7 +41,7 @@ struct IdxSmem {
     alignas(1024) uint8_t stage[kIStages][kIStageBytes];
     alignas(1024) uint8_t qimg[KV8_MAX_IDX_HEADS * kIdxD];  // B operand: HI rows of 128 bytes, 128B-swizzled
     alignas(16) float wq[KV8_MAX_IDX_HEADS];                // w[h] * q_scale[h]
-    uint64_t full[kIStages], empty[kIStages], dfull[kIAcc], dempty[kIAcc], final_bar;
+    uint64_t full[kIStages], empty[kIStages], dfull[kIAcc], dempty[kIAcc], final_bar, qready;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -57,6 +58,10 @@ struct IdxArgs {
     int *err_word;
 };
 
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __global__ void __launch_bounds__(kIThreads, 1) index_score_kernel(const __grid_constant__ CUtensorMap map_k, IdxArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     IdxSmem &sm = *reinterpret_cast<IdxSmem *>(smem);
@@ -71,6 +76,34 @@ __global__ void __launch_bounds__(kIThreads, 1) index_score_kernel(const __grid_
     const int n_tiles = (int)(i1 - i0);
     const int HI = a.HI;
     const int64_t row_base = (int64_t)b * a.seq_stride_rows;
+
+    // The epilogue warps load their query head rows and weights first, before any key tile is
+    // requested: issued behind the key stream they would wait for it.  Lane j holds the weight of the
+    // warp's j-th head row; lane l holds elements 4l..4l+3 of each row.
+    constexpr int kRowsPerWarp = KV8_MAX_IDX_HEADS / 4;
+    static_assert(kRowsPerWarp <= 32, "one head weight per lane");
+    float4 v[kRowsPerWarp];
+    float w_lane = 0.f;
+    if (warp >= 2) {
+        const int hw = warp - 2 + 4 * lane;
+        if (lane < kRowsPerWarp && hw < a.HI) w_lane = __ldg(a.w + (int64_t)b * a.HI + hw);
+#pragma unroll
+        for (int j = 0; j < kRowsPerWarp; ++j) {
+            const int h = warp - 2 + 4 * j;
+            v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (h < a.HI) {
+                const int64_t e = ((int64_t)b * a.HI + h) * kIdxD + 4 * lane;
+                if (a.q_bf16) {
+                    const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(a.q) + e));
+                    const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.x));
+                    const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.y));
+                    v[j] = make_float4(f0.x, f0.y, f1.x, f1.y);
+                } else {
+                    v[j] = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(a.q) + e));
+                }
+            }
+        }
+    }
     // each accumulator starts at a power-of-two column: stride >= HI
     const uint32_t dstride = HI <= 16 ? 16u : HI <= 32 ? 32u : HI <= 64 ? 64u : 128u;
     const uint32_t ncols = dstride * kIAcc < 32u ? 32u : dstride * kIAcc;
@@ -85,39 +118,13 @@ __global__ void __launch_bounds__(kIThreads, 1) index_score_kernel(const __grid_
             mbar_init(&sm.dempty[k], 128);
         }
         mbar_init(&sm.final_bar, 1);
+        mbar_init(&sm.qready, 128);  // the four epilogue warps have written the query image
         sm.abort_flag = 0;
         fence_barrier_init();
     }
     if (warp == 1) {
         tmem_alloc(&sm.tmem_base, ncols);
         tmem_relinquish();
-    }
-    // the query image: warps 2..5 quantize the HI heads of query b (one warp per head row at a time;
-    // lane l takes elements 4l..4l+3), exactly as the row quantizer does
-    if (warp >= 2) {
-        for (int h = warp - 2; h < HI; h += 4) {
-            float4 v;
-            const int64_t e = ((int64_t)b * HI + h) * kIdxD + 4 * lane;
-            if (a.q_bf16) {
-                const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(a.q) + e));
-                const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.x));
-                const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.y));
-                v = make_float4(f0.x, f0.y, f1.x, f1.y);
-            } else {
-                v = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(a.q) + e));
-            }
-            float amax = 0.f;
-            amax = finite_abs_max(amax, v.x);
-            amax = finite_abs_max(amax, v.y);
-            amax = finite_abs_max(amax, v.z);
-            amax = finite_abs_max(amax, v.w);
-            amax = warp_max(amax);
-            float pre, mul, qs;
-            row_quant_factors(amax, pre, mul, qs);
-            *reinterpret_cast<uint32_t *>(sm.qimg + sw128_offset(h, 4 * lane)) = enc4(scale4(v, pre, mul));
-            if (lane == 0) sm.wq[h] = __ldg(a.w + (int64_t)b * HI + h) * qs;
-        }
-        fence_proxy_async_smem();  // the MMAs read the image through the async proxy
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -148,7 +155,8 @@ __global__ void __launch_bounds__(kIThreads, 1) index_score_kernel(const __grid_
         if (lane == 0 && n_tiles > 0) {
             const uint32_t idesc = idesc_e4m3_f32(kITile, HI, false, false);
             const uint32_t qb = smem_u32(sm.qimg);
-            for (int i = 0; i < n_tiles; ++i) {
+            const bool q_ok = mbar_wait(&sm.qready, 0, &sm.abort_flag, a.err_word);
+            for (int i = 0; i < n_tiles && q_ok; ++i) {
                 const int s = i % kIStages, buf = i % kIAcc;
                 if (!mbar_wait(&sm.full[s], (i / kIStages) & 1, &sm.abort_flag, a.err_word)) break;
                 if (i >= kIAcc && !mbar_wait(&sm.dempty[buf], ((i / kIAcc) - 1) & 1, &sm.abort_flag, a.err_word))
@@ -169,27 +177,73 @@ __global__ void __launch_bounds__(kIThreads, 1) index_score_kernel(const __grid_
         __syncwarp();
     } else {
         // ================================ epilogue ================================
+        // first the query image (its rows were loaded at the top of the kernel): warp w quantizes head
+        // rows w-2, w+2, ... (lane l takes elements 4l..4l+3) with the row quantizer's f32 steps
+        {
+#pragma unroll
+            for (int j = 0; j < kRowsPerWarp; ++j) {
+                const int h = warp - 2 + 4 * j;
+                if (h >= HI) break;
+                float amax = 0.f;
+                amax = finite_abs_max(amax, v[j].x);
+                amax = finite_abs_max(amax, v[j].y);
+                amax = finite_abs_max(amax, v[j].z);
+                amax = finite_abs_max(amax, v[j].w);
+                amax = warp_max(amax);
+                float pre, mul, qs;
+                row_quant_factors(amax, pre, mul, qs);
+                *reinterpret_cast<uint32_t *>(sm.qimg + sw128_offset(h, 4 * lane)) = enc4(scale4(v[j], pre, mul));
+                const float wj = __shfl_sync(0xffffffffu, w_lane, j);
+                if (lane == 0) sm.wq[h] = wj * qs;
+            }
+            fence_proxy_async_smem();  // the MMAs read the image through the async proxy
+            named_barrier_sync(1, 128);  // wq complete for every epilogue thread
+            mbar_arrive(&sm.qready);
+        }
         const int q = warp & 3;  // TMEM lane quadrant
         const int r = q * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
         bool ok = true;
+        // the row's key scale, loaded one tile ahead so its latency hides behind the previous tile
+        auto kscale = [&](int i) -> float {
+            const int64_t t = (i0 + i) * kITile + r;
+            return (i < n_tiles && t < a.T) ? __ldg(a.k_scale + row_base + t) : 0.f;
+        };
+        float ks_next = kscale(0);
         for (int i = 0; i < n_tiles && ok; ++i) {
             const int buf = i % kIAcc;
+            const float ks = ks_next;
+            ks_next = kscale(i + 1);
             ok = mbar_wait(&sm.dfull[buf], (i / kIAcc) & 1, &sm.abort_flag, a.err_word);
             if (!ok) break;
             tc_fence_after_sync();
             float acc = 0.f;
-            for (int h0 = 0; h0 < HI; h0 += 16) {
-                uint32_t v[16];
-                tmem_ld_32x32b_x16(tmem + lane_addr + (uint32_t)buf * dstride + (uint32_t)h0, v);
+            for (int h0 = 0; h0 < HI; h0 += 64) {
+                // up to 64 columns in flight, one wait
+                uint32_t v[4][16];
+                const uint32_t ta = tmem + lane_addr + (uint32_t)buf * dstride + (uint32_t)h0;
+                const int nq = (HI - h0) >= 64 ? 4 : (HI - h0) / 16;
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq)
+                    if (qq < nq) tmem_ld_32x32b_x16(ta + 16u * qq, v[qq]);
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) acc = fmaf(sm.wq[h0 + j], fmaxf(__uint_as_float(v[j]), 0.f), acc);
+                for (int qq = 0; qq < 4; ++qq) {
+                    if (qq >= nq) break;
+#pragma unroll
+                    for (int j4 = 0; j4 < 4; ++j4) {
+                        const float4 wq = *reinterpret_cast<const float4 *>(&sm.wq[h0 + 16 * qq + 4 * j4]);
+                        acc = fmaf(wq.x, fmaxf(__uint_as_float(v[qq][4 * j4 + 0]), 0.f), acc);
+                        acc = fmaf(wq.y, fmaxf(__uint_as_float(v[qq][4 * j4 + 1]), 0.f), acc);
+                        acc = fmaf(wq.z, fmaxf(__uint_as_float(v[qq][4 * j4 + 2]), 0.f), acc);
+                        acc = fmaf(wq.w, fmaxf(__uint_as_float(v[qq][4 * j4 + 3]), 0.f), acc);
+                    }
+                }
             }
             tc_fence_before_sync();
             mbar_arrive(&sm.dempty[buf]);
             const int64_t t = (i0 + i) * kITile + r;
-            if (t < a.T) a.scores[(int64_t)b * a.T + t] = __ldg(a.k_scale + row_base + t) * acc;
+            if (t < a.T) a.scores[(int64_t)b * a.T + t] = ks * acc;
         }
     }
     tc_fence_before_sync();
@@ -198,10 +252,19 @@ __global__ void __launch_bounds__(kIThreads, 1) index_score_kernel(const __grid_
 }
 
 // ------------------------------------------------------------------------------------------------
-// top-k: one CTA of 1024 threads per query
+// top-k: C CTAs per query (a cooperative launch: all CTAs resident), CTA c owning positions
+// [c*T/C, (c+1)*T/C).  Each radix pass: a warp-aggregated shared histogram of the CTA's candidates,
+// added once into the query's global histogram; a barrier of the query's C CTAs; every CTA then finds
+// the pass's bin from the global histogram.  The final pass counts keys above / equal to the k-th key
+// per CTA, and after a last barrier each CTA writes its selected positions at their global offsets.
 // ------------------------------------------------------------------------------------------------
-constexpr int kKThreads = 1024;
+constexpr int kKThreads = 512;
 constexpr int kKBins = 2048;
+constexpr int kKMaxC = 152;
+constexpr int kKCache = 8192;  // a CTA's scores staged in shared memory when its range is this short
+// per-query workspace (u32): three pass histograms, per-CTA (above, equal) counts, barrier counter
+constexpr int kKWsHist = 3 * kKBins;
+constexpr int kKWsPerItem = kKWsHist + 2 * kKMaxC + 32;
 
 // order-preserving key: larger float -> larger unsigned key (-0 sorts just below +0)
 __device__ __forceinline__ uint32_t fkey(float f) {
@@ -209,10 +272,9 @@ __device__ __forceinline__ uint32_t fkey(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Block-wide exclusive scan of one value per thread (1024 threads); returns the exclusive prefix and
-// writes the total to *total.
+// Block-wide exclusive scan of one value per thread; returns the prefix, *total gets the sum.
 __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *warp_sums, uint32_t *total) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
     uint32_t x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -222,34 +284,67 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *w
     if (lane == 31) warp_sums[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        uint32_t w = warp_sums[lane];
+        uint32_t w = lane < nw ? warp_sums[lane] : 0u;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
             if (lane >= o) w += y;
         }
-        warp_sums[lane] = w;  // inclusive over warps
+        if (lane < nw) warp_sums[lane] = w;  // inclusive over warps
     }
     __syncthreads();
     const uint32_t before = (warp > 0 ? warp_sums[warp - 1] : 0u) + x - v;
-    *total = warp_sums[31];
-    __syncthreads();  // warp_sums may be reused by the caller's next scan
+    *total = warp_sums[nw - 1];
+    __syncthreads();  // warp_sums is reused by the next scan
     return before;
 }
 
-__global__ void __launch_bounds__(kKThreads, 1) topk_kernel(const float *__restrict__ scores, int64_t T, int NS,
-                                                           int32_t *__restrict__ idx) {
+// Barrier of the C CTAs of one query: arrive on the query's counter, wait (bounded) until it reaches
+// `target`.  A wait that gives up sets KV8_ERR_TIMEOUT and returns false; the CTA then stops.
+__device__ bool query_barrier(uint32_t *ctr, uint32_t target, int *err_word, int *abort_sh) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(ctr, 1u);
+        const uint64_t t0 = globaltimer_ns();
+        while (*reinterpret_cast<volatile uint32_t *>(ctr) < target) {
+            if (globaltimer_ns() - t0 > 1000000000ull) {  // 1 s
+                if (err_word) atomicOr(err_word, (int)KV8_ERR_TIMEOUT);
+                *abort_sh = 1;
+                break;
+            }
+            __nanosleep(100);
+        }
+        __threadfence();
+    }
+    __syncthreads();
+    return *abort_sh == 0;
+}
+
+__global__ void __launch_bounds__(kKThreads) topk_kernel(const float *__restrict__ scores, int64_t T, int NS, int C,
+                                                          int32_t *__restrict__ idx, uint32_t *__restrict__ ws,
+                                                          int *err_word) {
     __shared__ uint32_t hist[kKBins];
     __shared__ uint32_t warp_sums[32];
     __shared__ uint32_t sh_bin, sh_need;
-    const int tid = threadIdx.x;
-    const int b = blockIdx.x;
+    __shared__ int abort_sh;
+    __shared__ uint32_t keys_sh[kKCache];
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int b = blockIdx.x / C, c = blockIdx.x - b * C;
     const float *s = scores + (int64_t)b * T;
     int32_t *out = idx + (int64_t)b * NS;
+    uint32_t *wsb = ws + (size_t)b * kKWsPerItem;
+    uint32_t *ghist = wsb, *gcnt = wsb + kKWsHist, *gbar = wsb + kKWsHist + 2 * kKMaxC;
     const uint32_t k = (uint32_t)((int64_t)NS < T ? NS : T);
+    const int64_t c0 = T * c / C, c1 = T * (c + 1) / C;
+    if (tid == 0) abort_sh = 0;
+    // the CTA's keys, staged once when they fit (every pass below reads them again)
+    const bool cached = c1 - c0 <= kKCache;
+    if (cached)
+        for (int64_t t = c0 + tid; t < c1; t += kKThreads) keys_sh[t - c0] = fkey(__ldg(s + t));
+    __syncthreads();
+    auto key_at = [&](int64_t t) -> uint32_t { return cached ? keys_sh[t - c0] : fkey(__ldg(s + t)); };
 
-    // ---- radix select: prefix / mask of the k-th largest key, `need` = how many of the keys equal to it
-    // (after the last pass) still belong to the top k
     uint32_t prefix = 0, mask = 0, need = k;
     const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
     for (int p = 0; p < 3; ++p) {
@@ -257,25 +352,38 @@ __global__ void __launch_bounds__(kKThreads, 1) topk_kernel(const float *__restr
         const uint32_t nb = 1u << widths[p];
         for (int i = tid; i < kKBins; i += kKThreads) hist[i] = 0;
         __syncthreads();
-        for (int64_t t = tid; t < T; t += kKThreads) {
-            const uint32_t key = fkey(__ldg(s + t));
-            if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & (nb - 1)], 1u);
+        for (int64_t t0 = c0; t0 < c1; t0 += kKThreads) {
+            const int64_t t = t0 + tid;
+            const bool in = t < c1;
+            const uint32_t key = in ? key_at(t) : 0u;
+            const bool cand = in && (key & mask) == prefix;
+            const uint32_t bin = cand ? (key >> shift) & (nb - 1) : 0xFFFFFFFFu;
+            // lanes with the same bin add once (the leader adds the group's count)
+            const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+            if (cand && (__ffs(peers) - 1) == lane) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
         }
         __syncthreads();
-        // bins from the top: thread j holds bins nb-1-2j and nb-2-2j (in descending order)
-        uint32_t c0 = 0, c1 = 0;
-        const int j0 = (int)nb - 1 - 2 * tid, j1 = j0 - 1;
-        if (j0 >= 0) c0 = hist[j0];
-        if (j1 >= 0) c1 = hist[j1];
+        for (int i = tid; i < (int)nb; i += kKThreads)
+            if (hist[i]) atomicAdd(&ghist[p * kKBins + i], hist[i]);
+        if (!query_barrier(gbar, (uint32_t)(p + 1) * (uint32_t)C, err_word, &abort_sh)) return;
+        // the bin where the count from the top reaches `need`: thread j holds 4 bins in descending order
+        uint32_t cnt[4], sum = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int bi = (int)nb - 1 - (4 * tid + u);
+            cnt[u] = bi >= 0 ? __ldcg(&ghist[p * kKBins + bi]) : 0u;
+            sum += cnt[u];
+        }
         uint32_t total;
-        const uint32_t above = block_exclusive_scan(c0 + c1, warp_sums, &total);
-        // the bin where the running count from the top reaches `need`
-        if (j0 >= 0 && above < need && above + c0 >= need) {
-            sh_bin = (uint32_t)j0;
-            sh_need = need - above;
-        } else if (j1 >= 0 && above + c0 < need && above + c0 + c1 >= need) {
-            sh_bin = (uint32_t)j1;
-            sh_need = need - above - c0;
+        uint32_t above = block_exclusive_scan(sum, warp_sums, &total);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int bi = (int)nb - 1 - (4 * tid + u);
+            if (bi >= 0 && above < need && above + cnt[u] >= need) {
+                sh_bin = (uint32_t)bi;
+                sh_need = need - above;
+            }
+            above += cnt[u];
         }
         __syncthreads();
         prefix |= sh_bin << shift;
@@ -285,22 +393,37 @@ __global__ void __launch_bounds__(kKThreads, 1) topk_kernel(const float *__restr
     }
     const uint32_t thr = prefix;  // the k-th largest key; `need` of the keys equal to it are taken
 
-    // ---- index-ordered selection: thread j owns positions [j*C, (j+1)*C)
-    const int64_t C = (T + kKThreads - 1) / kKThreads;
-    const int64_t t0 = (int64_t)tid * C, t1 = t0 + C < T ? t0 + C : T;
+    // ---- positions in order: thread j of CTA c owns a contiguous sub-range of the CTA's range
+    const int64_t per = (c1 - c0 + kKThreads - 1) / kKThreads;
+    const int64_t t0 = c0 + (int64_t)tid * per, t1 = t0 + per < c1 ? t0 + per : c1;
     uint32_t n_gt = 0, n_eq = 0;
     for (int64_t t = t0; t < t1; ++t) {
-        const uint32_t key = fkey(__ldg(s + t));
+        const uint32_t key = key_at(t);
         n_gt += key > thr;
         n_eq += key == thr;
     }
+    uint32_t cta_gt, cta_eq;
+    const uint32_t gt_before = block_exclusive_scan(n_gt, warp_sums, &cta_gt);
+    const uint32_t eq_before = block_exclusive_scan(n_eq, warp_sums, &cta_eq);
+    if (tid == 0) {
+        gcnt[2 * c] = cta_gt;
+        gcnt[2 * c + 1] = cta_eq;
+    }
+    if (!query_barrier(gbar, 4u * (uint32_t)C, err_word, &abort_sh)) return;
+    uint32_t gt_prev = 0, eq_prev = 0;  // over the query's earlier CTAs
+    for (int cc = 0; cc < c; ++cc) {
+        gt_prev += __ldcg(&gcnt[2 * cc]);
+        eq_prev += __ldcg(&gcnt[2 * cc + 1]);
+    }
+    const uint32_t eq_all_before = eq_prev + eq_before;
+    const uint32_t eq_take = eq_all_before >= need ? 0u : (need - eq_all_before < n_eq ? need - eq_all_before : n_eq);
+    const uint32_t eq_taken_prev = eq_prev < need ? eq_prev : need;  // equals taken by earlier CTAs
     uint32_t tot;
-    const uint32_t eq_before = block_exclusive_scan(n_eq, warp_sums, &tot);
-    const uint32_t eq_take = eq_before >= need ? 0u : (need - eq_before < n_eq ? need - eq_before : n_eq);
-    const uint32_t pos0 = block_exclusive_scan(n_gt + eq_take, warp_sums, &tot);
-    uint32_t pos = pos0, eq_used = 0;
+    const uint32_t pos_in_cta = block_exclusive_scan(n_gt + eq_take, warp_sums, &tot);
+    uint32_t pos = gt_prev + eq_taken_prev + pos_in_cta, eq_used = 0;
+    (void)gt_before;
     for (int64_t t = t0; t < t1; ++t) {
-        const uint32_t key = fkey(__ldg(s + t));
+        const uint32_t key = key_at(t);
         if (key > thr || (key == thr && eq_used < eq_take)) {
             if (key == thr) ++eq_used;
             if (pos < k) out[pos] = (int32_t)t;
@@ -359,8 +482,24 @@ cudaError_t launch_index_scores(const void *q, int q_bf16, const float *w, int B
     return cudaGetLastError();
 }
 
-cudaError_t launch_topk(const float *scores, int B, int64_t T, int NS, int32_t *idx, cudaStream_t st) {
-    topk_kernel<<<(unsigned)B, kKThreads, 0, st>>>(scores, T, NS, idx);
+size_t topk_workspace_bytes(int B) { return (size_t)B * kKWsPerItem * sizeof(uint32_t); }
+
+cudaError_t launch_topk(const float *scores, int B, int64_t T, int NS, int32_t *idx, void *ws, int *err_word,
+                        cudaStream_t st) {
+    cudaError_t e = cudaMemsetAsync(ws, 0, topk_workspace_bytes(B), st);
+    if (e != cudaSuccess) return e;
+    const int C = B >= kKMaxC ? 1 : kKMaxC / B;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(B * C));
+    cfg.blockDim = dim3(kKThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;  // the CTAs of a query wait for one another
+    attr[0].val.cooperative = C > 1 ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, topk_kernel, scores, T, NS, C, idx, static_cast<uint32_t *>(ws), err_word);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -33,7 +33,9 @@ cudaError_t launch_quant_rows_w(const float *x, int64_t n, int width, uint8_t *q
 cudaError_t launch_index_scores(const void *q, int q_bf16, const float *w, int B, int HI, const uint8_t *k8,
                                 const float *k_scale, int64_t T, int64_t seq_stride_rows, float *scores,
                                 int *err_word, cudaStream_t st);
-cudaError_t launch_topk(const float *scores, int B, int64_t T, int NS, int32_t *idx, cudaStream_t st);
+size_t topk_workspace_bytes(int B);
+cudaError_t launch_topk(const float *scores, int B, int64_t T, int NS, int32_t *idx, void *ws, int *err_word,
+                        cudaStream_t st);
 cudaError_t launch_encode(const float *y, int64_t n, uint8_t *out, cudaStream_t st);
 cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t st);
 // tcgen05 kernel for bf16 queries: a dense (optionally causal) row range, or selection lists (which

@@ -100,20 +100,27 @@ int kv8_quant_rows_w(const float *x, int64_t n, int width, uint8_t *q, float *sc
     return status(launch_quant_rows_w(x, n, width, q, scale, (cudaStream_t)stream));
 }
 
+int dsa_index_workspace_bytes(int B, size_t *bytes) {
+    if (B < 1 || !bytes) return KV8_EINVAL;
+    *bytes = topk_workspace_bytes(B);
+    return KV8_OK;
+}
+
 int dsa_index_topk8(const void *q_idx, int q_dtype, const float *w, int B, int HI, const uint8_t *k8,
-                    const float *k_scale, int64_t T, int64_t seq_stride_rows, int NS, float *scores, int32_t *idx,
-                    int *err_word, void *stream) {
+                    const float *k_scale, int64_t T, int64_t seq_stride_rows, int NS, void *workspace,
+                    size_t ws_bytes, float *scores, int32_t *idx, int *err_word, void *stream) {
     if (B < 1 || HI < 16 || HI > KV8_MAX_IDX_HEADS || HI % 16 != 0 || T < 1 || T > KV8_MAX_ROWS || NS < 1 ||
         NS > KV8_MAX_SELECT || seq_stride_rows < 0)
         return KV8_EINVAL;
     if ((int64_t)(B - 1) * seq_stride_rows + T >= (1LL << 31) - 128) return KV8_EINVAL;
     if ((q_dtype != KV8_F32 && q_dtype != KV8_BF16) || !aligned(q_idx, 16) || !aligned(w, 4) || !aligned(k8, 16) ||
-        !aligned(k_scale, 4) || !aligned(scores, 16) || !aligned(idx, 16))
+        !aligned(k_scale, 4) || !aligned(scores, 16) || !aligned(idx, 16) || !aligned(workspace, 16))
         return KV8_EINVAL;
+    if (ws_bytes < topk_workspace_bytes(B)) return KV8_EWORKSPACE;
     cudaError_t e = launch_index_scores(q_idx, q_dtype == KV8_BF16, w, B, HI, k8, k_scale, T, seq_stride_rows, scores,
                                         err_word, (cudaStream_t)stream);
     if (e != cudaSuccess) return KV8_ECUDA;
-    return status(launch_topk(scores, B, T, NS, idx, (cudaStream_t)stream));
+    return status(launch_topk(scores, B, T, NS, idx, workspace, err_word, (cudaStream_t)stream));
 }
 
 int mla_q_absorb8(const void *q_nope, int q_dtype, int S, int H, const uint8_t *w8, const float *w_scale,

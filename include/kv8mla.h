@@ -244,11 +244,15 @@ KV8_API int mla_out_project8(const float *ctx, int S, int H, const uint8_t *w8, 
  *   selection list mla_absorb_sel8 takes.
  *   HI a multiple of 16 in [16, KV8_MAX_IDX_HEADS]; T in [1, KV8_MAX_ROWS]; NS in [1, KV8_MAX_SELECT];
  *   seq_stride_rows >= 0 and (B-1)*seq_stride_rows + T < 2^31 - 128; buffers 16-byte aligned.
- *   err_word: optional (KV8_ERR_TIMEOUT).  The scores run on the tensor cores (e4m3 x e4m3, f32 sums).
+ *   workspace: >= dsa_index_workspace_bytes(B) bytes (the top-k's histograms and the barrier counters of
+ *   the CTAs that share a query; zeroed by the call itself).  err_word: optional (KV8_ERR_TIMEOUT).
+ *   The scores run on the tensor cores (e4m3 x e4m3, f32 sums); the top-k is one cooperative launch
+ *   whose CTAs meet at time-bounded barriers (a barrier that gives up sets KV8_ERR_TIMEOUT).
  * --------------------------------------------------------------------------------------------- */
+KV8_API int dsa_index_workspace_bytes(int B, size_t *bytes);
 KV8_API int dsa_index_topk8(const void *q_idx, int q_dtype, const float *w, int B, int HI, const uint8_t *k8,
-                            const float *k_scale, int64_t T, int64_t seq_stride_rows, int NS, float *scores,
-                            int32_t *idx, int *err_word, void *stream);
+                            const float *k_scale, int64_t T, int64_t seq_stride_rows, int NS, void *workspace,
+                            size_t ws_bytes, float *scores, int32_t *idx, int *err_word, void *stream);
 
 /* -----------------------------------------------------------------------------------------------
  * kv8_copy -- copy `bytes` bytes from src to dst with a kernel (the SMs' loads and stores, not a

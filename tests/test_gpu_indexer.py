@@ -28,7 +28,8 @@ def _run(lib, q, w, tk8, tks, B, T, stride, NS):
     scores = torch.empty((B, T), dtype=torch.float32, device=DEV)
     idx = torch.full((B, NS), -7, dtype=torch.int32, device=DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
-    lib.dsa_index_topk8(q, w, tk8, tks, T, stride, NS, scores, idx, err_word=err)
+    ws = torch.empty(lib.dsa_index_workspace_bytes(B) // 4, dtype=torch.int32, device=DEV)
+    lib.dsa_index_topk8(q, w, tk8, tks, T, stride, NS, ws, scores, idx, err_word=err)
     torch.cuda.synchronize()
     assert err.item() == 0
     return scores.cpu().numpy(), idx.cpu().numpy()
