@@ -35,6 +35,9 @@ SIGNATURES = {
     "mla_absorb_decode8_noalloc": (_I, [_P, _P, _I, _I, _P, _P, _I64, _F, _I, _P, _P, _P]),
     "mla_q_absorb8": (_I, [_P, _I, _I, _I, _P, _P, _P, _I, _P]),
     "kv8_quant_rows_w": (_I, [_P, _I64, _I, _P, _P, _P]),
+    "kv8_quant_rows_scatter": (_I, [_P, _I64, _P, _P, _P, _I64, _P, _P]),
+    "mla_batch_decode8_workspace_bytes": (_I, [_I, _I, _I64, _P]),
+    "mla_absorb_batch_decode8": (_I, [_P, _P, _I, _I, _I, _P, _P, _I64, _I64, _P, _F, _P, _SZ, _P, _P, _P]),
     "dsa_index_workspace_bytes": (_I, [_I, _P]),
     "dsa_index_topk8": (_I, [_P, _I, _P, _I, _I, _P, _P, _I64, _I64, _I, _P, _SZ, _P, _P, _P, _P]),
     "mla_out_project8": (_I, [_P, _I, _I, _P, _P, _P, _P]),
@@ -128,6 +131,31 @@ def mla_decode8_partial(q_lat, q_rope, kv8, kv_scale, T: int, sm_scale: float, w
     _check("mla_decode8_partial", load().mla_decode8_partial(
         _ptr(q_lat), _ptr(q_rope), _qdtype(q_lat), H, _ptr(kv8), _ptr(kv_scale), T, sm_scale, P_req,
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err_word), _stream(stream)))
+
+
+def kv8_quant_rows_scatter(x, dst_rows, kv8, kv_scale, err_word=None, stream=None) -> None:
+    """Quantize rows x [n][576] f32 into cache rows dst_rows [n] (int64 tensor) of kv8 [rows][576] / kv_scale."""
+    n = x.numel() // 576
+    _check("kv8_quant_rows_scatter", load().kv8_quant_rows_scatter(
+        _ptr(x), n, _ptr(dst_rows), _ptr(kv8), _ptr(kv_scale), kv8.shape[0], _ptr(err_word), _stream(stream)))
+
+
+def mla_batch_decode8_workspace_bytes(B: int, H: int, T_max: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check("mla_batch_decode8_workspace_bytes", load().mla_batch_decode8_workspace_bytes(B, H, T_max,
+                                                                                         ctypes.addressof(out)))
+    return out.value
+
+
+def mla_absorb_batch_decode8(q_lat, q_rope, kv8, kv_scale, T_max: int, seq_stride_rows: int, lens, sm_scale: float,
+                             workspace, out, err_word=None, stream=None) -> None:
+    """B sequences, sequence b attending its first lens[b] rows of cache rows b*seq_stride_rows.. (lens: int32
+    CUDA tensor [B]) -> out [B][H][512] f32."""
+    B, H = q_lat.shape[0], q_lat.shape[1]
+    _check("mla_absorb_batch_decode8", load().mla_absorb_batch_decode8(
+        _ptr(q_lat), _ptr(q_rope), _qdtype(q_lat), B, H, _ptr(kv8), _ptr(kv_scale), T_max, seq_stride_rows,
+        _ptr(lens), sm_scale, _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err_word),
+        _ptr(out), _stream(stream)))
 
 
 def kv8_quant_rows_w(x, q, scale, stream=None) -> None:

@@ -52,6 +52,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_simt_kernel(AttnArgs a) {
     int64_t n_list;
     if (a.idx) n_list = a.NS;
     else if (a.pos0 >= 0) n_list = (a.pos0 + b + 1 < a.T) ? a.pos0 + b + 1 : a.T;
+    else if (a.lens) n_list = min((int64_t)max(__ldg(a.lens + b), 0), a.T);
     else n_list = a.T;
     const int64_t j0 = n_list * part / a.P, j1 = n_list * (part + 1) / a.P;
     const uint8_t *kv_b = a.kv8 + (int64_t)b * a.seq_stride_rows * kRow;

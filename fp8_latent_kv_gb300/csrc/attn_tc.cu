@@ -99,6 +99,7 @@ struct TcArgs {
     const float *kv_scale;
     int64_t T;
     int64_t pos0;                // causal: item b attends rows [0, pos0 + b]; -1: rows [0, T)
+    const int32_t *lens;         // batched dense decode: item b attends its rows [0, lens[b]) (clamped to T)
     const int32_t *idx;          // selection: item b attends rows idx[b][0..NS) of its own cache (else null)
     int NS;
     int64_t seq_stride_rows;     // selection: rows between consecutive items' caches
@@ -191,9 +192,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int b = blockIdx.x / per_item, rem = blockIdx.x - b * per_item;
     const int part = rem / a.n_half, half = rem - part * a.n_half;
     // the list this CTA walks: positions [t0, t1) of rows 0..n_rows-1 (dense / causal) or of idx[b] (selection)
-    const int64_t n_rows = a.idx ? (int64_t)a.NS : a.pos0 >= 0 ? ((a.pos0 + b + 1 < a.T) ? a.pos0 + b + 1 : a.T) : a.T;
+    const int64_t n_rows = a.idx           ? (int64_t)a.NS
+                           : a.pos0 >= 0   ? ((a.pos0 + b + 1 < a.T) ? a.pos0 + b + 1 : a.T)
+                           : a.lens        ? min((int64_t)max(__ldg(a.lens + b), 0), a.T)
+                                           : a.T;
     const int32_t *idx_b = a.idx ? a.idx + (int64_t)b * a.NS : nullptr;
-    const int64_t seq_base = a.idx ? (int64_t)b * a.seq_stride_rows : 0;
+    // each item's cache starts seq_stride_rows after the previous one (0 for one cache shared by all items)
+    const int64_t seq_base = (int64_t)b * a.seq_stride_rows;
     const int64_t t0 = n_rows * part / a.P, t1 = n_rows * (part + 1) / a.P;
     const int n_tiles = (int)((t1 - t0 + kTile - 1) / kTile);
 
@@ -253,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // product.  The stage's full barrier is re-armed only after the first release: that
                     // implies tile i-2's phase of it has completed (one arrival per phase).
                     if (lane == 0) {
-                        const int y = (int)p0;
+                        const int y = (int)(seq_base + p0);
                         for (int kb = 0; kb < 4 && ok_p; ++kb) {
                             if (i >= 2 && !(ok_p = mbar_wait(&ms.kv_blk[s][kb], ph, &ms.abort_flag, a.err_word))) break;
                             if (kb == 0) {
@@ -518,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool bad_index = false;
             auto row_scale = [&](int64_t pos) -> float {
                 if (pos >= t1) return -1.f;
-                if (!idx_b) return __ldg(a.kv_scale + pos);
+                if (!idx_b) return __ldg(a.kv_scale + seq_base + pos);
                 const int ri = __ldg(idx_b + pos);
                 if (ri < 0 || (int64_t)ri >= a.T) {
                     bad_index = true;
@@ -768,6 +773,7 @@ struct PrepArgs {
     const int32_t *idx;  // selection lists [B][NS], or null (rows 0..T-1 of one item)
     int NS;
     int64_t seq_stride_rows;
+    const int32_t *lens; // batched dense decode: rows per item, or null
     uint8_t *img;        // [B][n_half][kImg]
     float *c_head;       // [B][n_heads_pad]
     float *smax;         // [B][P]
@@ -835,7 +841,7 @@ __global__ void __launch_bounds__(kPrepBlock) tc_prep_kernel(PrepArgs a) {
                 h < a.H ? (mx > 0.f ? ldexpf(a.sm_scale_log2, E - 8) : a.sm_scale_log2) : 0.f;
     } else {
         const int bp = bid - a.B * n_groups, b = bp / a.P, p = bp - b * a.P;
-        const int64_t n_list = a.idx ? (int64_t)a.NS : a.T;
+        const int64_t n_list = a.idx ? (int64_t)a.NS : a.lens ? min((int64_t)max(__ldg(a.lens + b), 0), a.T) : a.T;
         const int64_t t0 = n_list * p / a.P, t1 = n_list * (p + 1) / a.P;
         const int32_t *idx_b = a.idx ? a.idx + (int64_t)b * a.NS : nullptr;
         const float *sc_b = a.kv_scale + (int64_t)b * a.seq_stride_rows;
@@ -885,7 +891,8 @@ cudaError_t launch_attn_tc(const AttnArgs &x, cudaStream_t st) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
     const bool sel = x.idx != nullptr;
-    const int64_t rows = sel ? (int64_t)(x.B - 1) * x.seq_stride_rows + x.T : x.T;
+    // the tensor maps cover every item's cache (items seq_stride_rows apart; 0 when they share one)
+    const int64_t rows = (int64_t)(x.B - 1) * x.seq_stride_rows + x.T;
     if (rows > 0x7fffffffLL) return cudaErrorInvalidValue;  // tensor-map row coordinates are 32-bit
     CUtensorMap m_lc, m_rc;
     const cuuint64_t dims[2] = {(cuuint64_t)kRow, (cuuint64_t)rows};
@@ -910,6 +917,7 @@ cudaError_t launch_attn_tc(const AttnArgs &x, cudaStream_t st) {
     a.kv_scale = x.kv_scale;
     a.T = x.T;
     a.pos0 = x.pos0;
+    a.lens = x.lens;
     a.idx = x.idx;
     a.NS = x.NS;
     a.seq_stride_rows = x.seq_stride_rows;
@@ -937,6 +945,7 @@ cudaError_t launch_attn_tc(const AttnArgs &x, cudaStream_t st) {
         pa.idx = a.idx;
         pa.NS = a.NS;
         pa.seq_stride_rows = a.seq_stride_rows;
+        pa.lens = a.lens;
         pa.img = static_cast<uint8_t *>(x.tc_scratch);
         pa.c_head = reinterpret_cast<float *>(pa.img + (size_t)a.B * 2 * kImg);
         pa.smax = pa.c_head + (size_t)a.B * 2 * kHeadsPerCta;

@@ -19,6 +19,8 @@ struct AttnArgs {
     const int32_t *idx;       // selection lists [B][NS], or nullptr for a dense row range
     int NS;                   // selection length
     int64_t pos0;             // causal prefill: item i attends rows [0, pos0 + i]; -1 = not causal
+    const int32_t *lens;      // batched dense decode: item i attends its rows [0, lens[i]) (device; clamped
+                              // to [0, T]), or null
     float sm_scale_log2;      // sm_scale * log2(e)
     int P;                    // partitions per batch item
     float *ws;                // partial sets (PartialView layout), or nullptr when `out` is written directly
@@ -29,6 +31,8 @@ struct AttnArgs {
 };
 
 cudaError_t launch_quant_rows(const float *x, int64_t n, uint8_t *q, float *scale, cudaStream_t st);
+cudaError_t launch_quant_rows_scatter(const float *x, int64_t n, const int64_t *dst, int64_t cache_rows, uint8_t *q,
+                                      float *scale, int *err_word, cudaStream_t st);
 cudaError_t launch_quant_rows_w(const float *x, int64_t n, int width, uint8_t *q, float *scale, cudaStream_t st);
 cudaError_t launch_index_scores(const void *q, int q_bf16, const float *w, int B, int HI, const uint8_t *k8,
                                 const float *k_scale, int64_t T, int64_t seq_stride_rows, float *scores,
@@ -52,5 +56,7 @@ cudaError_t launch_lse_merge(const float *ws, int B, int P, int H, float *out, c
 // Partition policy shared by the workspace queries and the launchers.
 int decode_partitions(int H, int64_t T, int P_req);
 int select_partitions(int B, int H, int NS);
+int batch_partitions(int B, int H, int64_t T_max);
+size_t decode_partial_bytes_b(int B, int P, int H);
 
 }  // namespace kv8

@@ -64,6 +64,20 @@ int decode_partitions(int H, int64_t T, int P_req) {
     return (int)(p < cap ? p : cap);
 }
 
+int batch_partitions(int B, int H, int64_t T_max) {
+    // one wave of tensor-core CTAs (one per SM of a 152-SM part): B items x P partitions x head halves,
+    // at least 128 rows per partition
+    const int64_t n_half = H > 64 ? 2 : 1;
+    int64_t cap = 152 / ((int64_t)B * n_half);
+    if (cap < 1) cap = 1;
+    const int64_t p = (T_max + 127) / 128;
+    return (int)(p < cap ? p : cap);
+}
+
+size_t decode_partial_bytes_b(int B, int P, int H) {
+    return ((PartialView::floats(B, P, H) * sizeof(float)) + 255) & ~(size_t)255;
+}
+
 int select_partitions(int B, int H, int NS) {
     // one wave of tensor-core CTAs (one per SM of a 152-SM part): B items x P partitions x head
     // halves, with the list's 128-row tiles spread evenly over the partitions
@@ -91,6 +105,59 @@ const char *kv8_strerror(int code) {
         case KV8_EUNSUPPORTED: return "unsupported device or shape";
         default: return "unknown kv8 error code";
     }
+}
+
+int kv8_quant_rows_scatter(const float *x, int64_t n, const int64_t *dst_rows, uint8_t *kv8, float *kv_scale,
+                           int64_t cache_rows, int *err_word, void *stream) {
+    if (n < 0 || cache_rows < 0) return KV8_EINVAL;
+    if (n == 0) return KV8_OK;
+    if (!aligned(x, 16) || !aligned(dst_rows, 8) || !aligned(kv8, 16) || !aligned(kv_scale, 4)) return KV8_EINVAL;
+    return status(launch_quant_rows_scatter(x, n, dst_rows, cache_rows, kv8, kv_scale, err_word, (cudaStream_t)stream));
+}
+
+int mla_batch_decode8_workspace_bytes(int B, int H, int64_t T_max, size_t *bytes) {
+    if (B < 1 || H < 1 || H > KV8_MAX_HEADS || T_max < 1 || T_max > KV8_MAX_ROWS || !bytes) return KV8_EINVAL;
+    const int P = batch_partitions(B, H, T_max);
+    *bytes = decode_partial_bytes_b(B, P, H) + tc_scratch_bytes(B, P);
+    return KV8_OK;
+}
+
+int mla_absorb_batch_decode8(const void *q_lat, const void *q_rope, int q_dtype, int B, int H, const uint8_t *kv8,
+                             const float *kv_scale, int64_t T_max, int64_t seq_stride_rows, const int32_t *lens,
+                             float sm_scale, void *workspace, size_t ws_bytes, int *err_word, float *out,
+                             void *stream) {
+    size_t need = 0;
+    int rc = mla_batch_decode8_workspace_bytes(B, H, T_max, &need);
+    if (rc != KV8_OK) return rc;
+    if (!valid_q(q_lat, q_rope, q_dtype) || !valid_cache(kv8, kv_scale, T_max) || !aligned(lens, 4) ||
+        !isfinite(sm_scale) || !aligned(workspace, 16) || !aligned(out, 16) || seq_stride_rows < 0 ||
+        (B > 1 && seq_stride_rows < T_max))
+        return KV8_EINVAL;
+    if (ws_bytes < need) return KV8_EWORKSPACE;
+    AttnArgs a{};
+    a.q_lat = q_lat;
+    a.q_rope = q_rope;
+    a.q_bf16 = q_dtype == KV8_BF16;
+    a.B = B;
+    a.H = H;
+    a.kv8 = kv8;
+    a.kv_scale = kv_scale;
+    a.T = T_max;
+    a.seq_stride_rows = B > 1 ? seq_stride_rows : 0;
+    a.idx = nullptr;
+    a.lens = lens;
+    a.pos0 = -1;
+    a.sm_scale_log2 = sm_scale * kLog2e;
+    a.P = batch_partitions(B, H, T_max);
+    a.ws = static_cast<float *>(workspace);
+    a.out = nullptr;
+    a.err_word = err_word;
+    a.tc_scratch = static_cast<uint8_t *>(workspace) + decode_partial_bytes_b(B, a.P, H);
+    // bf16 queries: tensor cores (32-bit tensor-map row coordinates); f32 queries: CUDA cores
+    const bool tc = a.q_bf16 && (int64_t)(B - 1) * a.seq_stride_rows + T_max <= 0x7fffffffLL;
+    rc = status(tc ? launch_attn_tc(a, (cudaStream_t)stream) : launch_attn_simt(a, (cudaStream_t)stream));
+    if (rc != KV8_OK) return rc;
+    return mla_lse_merge8(workspace, B, a.P, H, out, stream);
 }
 
 int kv8_quant_rows_w(const float *x, int64_t n, int width, uint8_t *q, float *scale, void *stream) {

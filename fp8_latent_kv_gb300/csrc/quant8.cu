@@ -15,15 +15,27 @@
 
 namespace kv8 {
 
-// One warp per row of W elements (W/4 float4, coalesced: lane l takes float4 l, l+32, ...).
+// One warp per row of W elements (W/4 float4, coalesced: lane l takes float4 l, l+32, ...).  With
+// `dst`, input row r is written to output row dst[r] (appending one row to each of several caches); a
+// destination outside [0, cache_rows) is skipped and reported.
 template <int W>
 __global__ void __launch_bounds__(256) quant_rows_kernel(const float *__restrict__ x, int64_t n,
-                                                          uint8_t *__restrict__ q, float *__restrict__ scale) {
+                                                          uint8_t *__restrict__ q, float *__restrict__ scale,
+                                                          const int64_t *__restrict__ dst, int64_t cache_rows,
+                                                          int *err_word) {
     constexpr int kF4 = W / 4, kPer = (kF4 + 31) / 32;
     const int lane = threadIdx.x & 31;
-    const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (row >= n) return;
-    const float4 *xr = reinterpret_cast<const float4 *>(x + row * W);
+    const int64_t in_row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (in_row >= n) return;
+    int64_t row = in_row;
+    if (dst) {
+        row = __ldg(dst + in_row);
+        if (row < 0 || row >= cache_rows) {
+            if (lane == 0 && err_word) atomicOr(err_word, (int)KV8_ERR_INDEX);
+            return;
+        }
+    }
+    const float4 *xr = reinterpret_cast<const float4 *>(x + in_row * W);
     float4 v[kPer];
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
@@ -70,11 +82,19 @@ cudaError_t launch_quant_rows_w(const float *x, int64_t n, int width, uint8_t *q
     const int rows_per_block = 8;  // 256 threads
     const int64_t blocks = (n + rows_per_block - 1) / rows_per_block;
     if (width == kRow)
-        quant_rows_kernel<kRow><<<(unsigned)blocks, 256, 0, st>>>(x, n, q, scale);
+        quant_rows_kernel<kRow><<<(unsigned)blocks, 256, 0, st>>>(x, n, q, scale, nullptr, 0, nullptr);
     else if (width == KV8_IDX_D)
-        quant_rows_kernel<KV8_IDX_D><<<(unsigned)blocks, 256, 0, st>>>(x, n, q, scale);
+        quant_rows_kernel<KV8_IDX_D><<<(unsigned)blocks, 256, 0, st>>>(x, n, q, scale, nullptr, 0, nullptr);
     else
         return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_rows_scatter(const float *x, int64_t n, const int64_t *dst, int64_t cache_rows, uint8_t *q,
+                                      float *scale, int *err_word, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    const int64_t blocks = (n + 7) / 8;
+    quant_rows_kernel<kRow><<<(unsigned)blocks, 256, 0, st>>>(x, n, q, scale, dst, cache_rows, err_word);
     return cudaGetLastError();
 }
 

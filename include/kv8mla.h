@@ -210,6 +210,28 @@ KV8_API int mla_absorb_decode8_noalloc(const void *q_lat, const void *q_rope, in
                                        int P_req, int *err_word, float *out, void *stream);
 
 /* -----------------------------------------------------------------------------------------------
+ * mla_absorb_batch_decode8 -- one decode step for B sequences at once, each with its own cache and length
+ * ([KV8] second commit: a device-resident cache per sequence to which each step appends the new rows;
+ * the split-T partials and log-sum-exp merge as for one sequence).
+ *   Sequence b's cache is rows b*seq_stride_rows .. b*seq_stride_rows + T_max - 1 of kv8 / kv_scale; it
+ *   attends its first lens[b] rows (lens: device int32 [B], clamped to [0, T_max]; 0 rows give a zero
+ *   output).  q_lat [B][H][512], q_rope [B][H][64] of type q_dtype; out [B][H][512] f32.
+ *   B >= 1; H in [1, 128]; T_max in [1, KV8_MAX_ROWS]; seq_stride_rows >= T_max when B > 1.
+ *   workspace: >= mla_batch_decode8_workspace_bytes(B, H, T_max) bytes (partial sets [B][P][H] first, as
+ *   for one sequence, then the prepared queries).  err_word: optional (KV8_ERR_TIMEOUT).
+ * kv8_quant_rows_scatter -- kv8_quant_rows writing input row r to cache row dst_rows[r] (device int64 [n]),
+ *   e.g. one fresh row appended to each sequence; a destination outside [0, cache_rows) is skipped and sets
+ *   KV8_ERR_INDEX in *err_word (optional).
+ * --------------------------------------------------------------------------------------------- */
+KV8_API int mla_batch_decode8_workspace_bytes(int B, int H, int64_t T_max, size_t *bytes);
+KV8_API int mla_absorb_batch_decode8(const void *q_lat, const void *q_rope, int q_dtype, int B, int H,
+                                     const uint8_t *kv8, const float *kv_scale, int64_t T_max, int64_t seq_stride_rows,
+                                     const int32_t *lens, float sm_scale, void *workspace, size_t ws_bytes,
+                                     int *err_word, float *out, void *stream);
+KV8_API int kv8_quant_rows_scatter(const float *x, int64_t n, const int64_t *dst_rows, uint8_t *kv8,
+                                   float *kv_scale, int64_t cache_rows, int *err_word, void *stream);
+
+/* -----------------------------------------------------------------------------------------------
  * Absorb projections through kv_b_proj stored as fmt=8 ([FMT8] "feat: fmt=8 (fp8-e4m3) decode on
  * the kv_b absorb path, CPU and CUDA": raw e4m3 bytes plus one f32 scale per 128x128 block,
  * block-row-major; the absorbed attention of [KV8] first commit works in the 512-wide latent).
