@@ -13,6 +13,7 @@ Other workloads (--workload), each one step of its own hot path:
   proj_dec / proj_prefill   the absorb projections through an fmt=8 kv_b (q_nope -> q_lat, context ->
            head output) for 1 query / a 1024-query chunk of 128 heads
   indexer  the DSA lightning indexer: 8 queries x 64 index heads over 131072 e4m3 index keys each, top-2048
+  batch_dec  one decode step for 8 sequences with their own caches (up to 32768 rows each, ragged)
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload KEY]
 For N > 1 launch with torchrun; every rank runs an independent replica (one layer's attention does
@@ -658,13 +659,101 @@ class IndexerCase(Case):
         return (time.perf_counter() - t0) * self._scale
 
 
+class BatchDecodeCase(Case):
+    """One decode step for B sequences at once: the fresh row of each sequence appended to its own cache
+    (one scatter call), then the batched split-T partials and the merge."""
+    launches_per_step = 5  # scatter quant + prep + partial + merge (+ the partial's dependent launch)
+    kernel_calls = "mla_absorb_batch_decode8: query prep + attn_tc_kernel + lse_merge_kernel"
+    step_desc = "kv8_quant_rows_scatter(B fresh rows) + batched split-T decode + log-sum-exp merge"
+
+    def __init__(self, kv, torch, dev, w):
+        import synth
+        self.kv, self.torch, self.w = kv, torch, w
+        B, T, H = w.B, w.T, w.H
+        self.lens_list = synth.batch_lengths(w)
+        self.kv8 = torch.zeros((B * T, 576), dtype=torch.uint8, device=dev)
+        self.sc = torch.zeros(B * T, dtype=torch.float32, device=dev)
+        fresh, dst = [], []
+        for b in range(B):
+            n = self.lens_list[b]
+            x = torch.from_numpy(synth.rows_for(w, b, 0, n)).to(dev)
+            kv.kv8_quant_rows(x[:-1], self.kv8[b * T:b * T + n - 1], self.sc[b * T:b * T + n - 1])
+            fresh.append(x[-1:].clone())
+            dst.append(b * T + n - 1)
+            del x
+        self.fresh = torch.cat(fresh)
+        self.dst = torch.tensor(dst, dtype=torch.int64, device=dev)
+        self.lens = torch.tensor(self.lens_list, dtype=torch.int32, device=dev)
+        ql, qr = synth.queries_for(w, B)
+        self.q_lat, self.q_rope = _bf16(torch, dev, ql), _bf16(torch, dev, qr)
+        self.ws = torch.empty(kv.mla_batch_decode8_workspace_bytes(B, H, T) // 4, dtype=torch.float32, device=dev)
+        self.out = torch.empty((B, H, 512), dtype=torch.float32, device=dev)
+        self.pack = Packed(torch, dev, [self.q_lat, self.q_rope, self.fresh])
+        self.h_out = torch.empty((B, H, 512), dtype=torch.float32).pin_memory()
+        self.h2d = self.pack.nbytes
+        self.d2h = self.h_out.numel() * 4
+        rows = sum(self.lens_list)
+        self.alg_bytes = rows * ROW_BYTES + self.q_lat.numel() * 2 + self.q_rope.numel() * 2
+        self.alg_bytes_step = rows * ROW_BYTES + self.h2d + self.d2h
+        self.flops = float(FLOP_PER_ROW_HEAD) * H * rows
+
+    def _decode(self, q_lat, q_rope, stream):
+        w = self.w
+        self.kv.mla_absorb_batch_decode8(q_lat, q_rope, self.kv8, self.sc, w.T, w.T, self.lens, SM_SCALE(), self.ws,
+                                         self.out, stream=stream)
+
+    def step(self, stream, ev=None):
+        self.kv.kv8_quant_rows_scatter(self.fresh, self.dst, self.kv8, self.sc, stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        self._decode(self.q_lat, self.q_rope, stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def kernel_call(self, stream):
+        self._decode(self.q_lat, self.q_rope, stream)
+
+    def e2e_step(self, stream):
+        kv = self.kv
+        self.pack.upload(kv, stream)
+        q_lat, q_rope, fresh = self.pack.views
+        kv.kv8_quant_rows_scatter(fresh, self.dst, self.kv8, self.sc, stream=stream)
+        self._decode(q_lat, q_rope, stream)
+        kv.kv8_copy(self.h_out, self.out, stream=stream)
+
+    def config(self):
+        w = self.w
+        return {"B": w.B, "H": w.H, "T_max": w.T, "lengths": getattr(self, "lens_list", None)}
+
+    def oracle_setup(self, n_heads):
+        import oracle
+        import synth
+        w = self.w
+        self.lens_list = synth.batch_lengths(w)
+        ql, qr = synth.queries_for(w, w.B)
+        heads = np.linspace(0, w.H - 1, n_heads).astype(int)
+        self._o = []
+        for b in range(w.B):
+            q_o, s_o = oracle.quant_rows(synth.rows_for(w, b, 0, self.lens_list[b]))
+            self._o.append((np.ascontiguousarray(ql[b][heads]), np.ascontiguousarray(qr[b][heads]), q_o, s_o))
+        self._scale = w.H / n_heads
+        return f"{n_heads} of {w.H} heads of every sequence over its whole length, scaled by heads to the step"
+
+    def oracle_step(self) -> float:
+        import oracle
+        t0 = time.perf_counter()
+        for ql, qr, q_o, s_o in self._o:
+            oracle.attn_decode(ql, qr, q_o, s_o, SM_SCALE())
+        return (time.perf_counter() - t0) * self._scale
+
+
 CASES = {"dec262k": DecodeCase, "dec16k": DecodeCase, "dsa": SelectCase, "prefill": PrefillCase,
-         "proj_dec": ProjCase, "proj_prefill": ProjCase, "indexer": IndexerCase}
+         "proj_dec": ProjCase, "proj_prefill": ProjCase, "indexer": IndexerCase, "batch_dec": BatchDecodeCase}
 # the oracle's sample: heads for the attention workloads, query rows for the projections
 ORACLE_HEADS = {"dec262k": 32, "dec16k": 128, "dsa": 128, "prefill": 8, "proj_dec": 1, "proj_prefill": 64,
-                "indexer": 1}
+                "indexer": 1, "batch_dec": 16}
 REFERENCE_HEADS = {"dec262k": 8, "dec16k": 32, "dsa": 32, "prefill": 4, "proj_dec": 1, "proj_prefill": 16,
-                   "indexer": 1}
+                   "indexer": 1, "batch_dec": 4}
 
 
 def SM_SCALE():

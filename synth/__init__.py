@@ -18,6 +18,8 @@ Workloads (one query position = one decode step of one layer):
   7 proj_prefill  the same for S=1024 query rows
   8 indexer   B=8 queries x 64 index heads x 128 (bf16 N(0,1)), head weights N(0,1)/8; per query its own
               T=131072 index-key rows N(0,1)*10^U(-0.5,0.5) of width 128; top NS=2048
+  9 batch_dec B=8 sequences, sequence b of length 32768 - 997 b (its own cache of 32768 rows, rows drawn
+              as for dec16k with sequence index b), H=128, bf16 queries; its last row is the fresh row
 """
 from __future__ import annotations
 
@@ -61,6 +63,8 @@ WORKLOADS = {
     "proj_prefill": Workload("proj_prefill", 7, H=128, T=0, S=1024),
     # the DSA lightning indexer that chooses the selection: 64 index heads of width 128 per query
     "indexer": Workload("indexer", 8, H=64, T=131072, B=8, NS=2048, mag_lo=10 ** -0.5, mag_hi=10 ** 0.5),
+    # one decode step for a batch of sequences, each its own cache (ragged lengths, one fresh row each)
+    "batch_dec": Workload("batch_dec", 9, H=128, T=32768, B=8),
 }
 
 DESCRIPTIONS = {
@@ -75,6 +79,8 @@ DESCRIPTIONS = {
     "proj_prefill": "absorb projections for a prefill chunk: S=1024 queries x H=128 heads through an fmt=8 kv_b",
     "indexer": "DSA lightning indexer: B=8 queries, each scoring its own T=131072 e4m3 index keys (width 128) "
                "with 64 index heads, then top-2048",
+    "batch_dec": "batched decode: B=8 sequences, each its own cache of up to T=32768 rows (lengths 32768 - 997 b), "
+                 "H=128, bf16 queries, one fresh row appended to each sequence per step",
 }
 
 
@@ -216,3 +222,8 @@ def index_queries_for(w: Workload) -> np.ndarray:
 def index_weights_for(w: Workload) -> np.ndarray:
     """Per-query head weights [B][64] f32: N(0,1)/8 (either sign)."""
     return (normal_f32(rng_for(w, 8), (w.B, w.H)) / np.float32(8.0)).astype(np.float32)
+
+
+def batch_lengths(w: Workload) -> list[int]:
+    """Ragged sequence lengths of the batched-decode workload."""
+    return [w.T - 997 * b for b in range(w.B)]
