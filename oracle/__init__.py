@@ -67,6 +67,7 @@ def _load():
             "kv8o_attn_prefill": (None, [P, P, i32, i32, P, P, P, i64, f32, P]),
             "kv8o_q_absorb": (None, [P, i32, i32, P, P, P]),
             "kv8o_quant_rows_w": (None, [P, i64, i32, P, P]),
+            "kv8o_attn_mixed_decode": (None, [P, P, P, i32, P, P, P, i64, f32, P]),
             "kv8o_index_scores": (None, [P, P, P, i32, i32, i32, P, P, i64, i64, P]),
             "kv8o_topk": (None, [P, i64, i32, P]),
             "kv8o_out_project": (None, [P, i32, i32, P, P, P]),
@@ -279,6 +280,27 @@ def topk(scores, k: int) -> np.ndarray:
     kk = min(int(k), s.size)
     out = np.empty(kk, dtype=np.int32)
     _load().kv8o_topk(_ptr(s), s.size, int(k), _ptr(out))
+    return out
+
+
+MX_NOPE, MX_ROPE = 448, 64
+
+
+def attn_mixed_decode(q_nope, q_rope, k8, k_scale, k_rope, sm_scale) -> np.ndarray:
+    """Mixed-precision cache decode: q_nope [H][448] and q_rope [H][64] (f32 holding bf16 values); the cache's
+    k8 [T][448] e4m3 bytes, k_scale [T] f32, k_rope [T][64] (f32 holding bf16 values).  q_nope is quantized
+    per head by the row quantizer first.  Returns out [H][512] f32."""
+    qn = _f32(q_nope).reshape(-1, MX_NOPE)
+    H = qn.shape[0]
+    q8, qs = quant_rows_w(qn, MX_NOPE)
+    qr = _f32(q_rope).reshape(H, MX_ROPE)
+    k8 = np.ascontiguousarray(k8, dtype=np.uint8).reshape(-1, MX_NOPE)
+    T = k8.shape[0]
+    ks = _f32(k_scale).reshape(T)
+    kr = _f32(k_rope).reshape(T, MX_ROPE)
+    out = np.empty((H, MX_NOPE + MX_ROPE), dtype=np.float32)
+    _load().kv8o_attn_mixed_decode(_ptr(q8), _ptr(qs), _ptr(qr), H, _ptr(k8), _ptr(ks), _ptr(kr), T,
+                                   float(np.float32(sm_scale)), _ptr(out))
     return out
 
 

@@ -573,6 +573,58 @@ void kv8o_topk(const double *scores, int64_t n, int k, int32_t *idx)
     free(order);
 }
 
+/* ---------------------------------------------------------------------------------------------
+ * Mixed-precision cache decode ([B1] page, "B1 Mixed FP8/BF16 FMHA first pass": each KV row keeps its
+ * no-position part (448) as e4m3 bytes with a per-row f32 scale and its RoPE part (64) as bf16; the
+ * query's no-position part is quantized from bf16 to e4m3 just before the attention; head width 512).
+ * Our reading (K and V are the same 512-wide row):
+ *   q8 [H][448] u8 and q_scale [H]: the row quantizer above applied to each head's q_nope;
+ *   score[h][t] = sm_scale * ( q_scale[h] * k_scale[t] * sum_i e4m3(q8[h][i]) e4m3(k8[t][i])
+ *                              + sum_j q_rope[h][j] * k_rope[t][j] )
+ *   value_t     = [ k_scale[t] * e4m3(k8[t][i]) for i < 448 ,  k_rope[t][j] for j < 64 ]
+ *   out[h]      = sum_t softmax_t(score[h][t]) * value_t             (double; rounded once to f32)
+ * q_rope and k_rope are passed as f32 holding the bf16 values.
+ * ------------------------------------------------------------------------------------------- */
+#define KV8O_MX_NOPE 448
+#define KV8O_MX_ROPE 64
+#define KV8O_MX_D (KV8O_MX_NOPE + KV8O_MX_ROPE)
+
+void kv8o_attn_mixed_decode(const uint8_t *q8, const float *q_scale, const float *q_rope, int H, const uint8_t *k8,
+                            const float *k_scale, const float *k_rope, int64_t T, float sm_scale, float *out)
+{
+    lut_init();
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int h = 0; h < H; ++h) {
+        double *score = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+        double m = -INFINITY;
+        for (int64_t t = 0; t < T; ++t) {
+            double dn = 0.0, dr = 0.0;
+            for (int i = 0; i < KV8O_MX_NOPE; ++i)
+                dn += g_lut[q8[(int64_t)h * KV8O_MX_NOPE + i]] * g_lut[k8[t * KV8O_MX_NOPE + i]];
+            for (int j = 0; j < KV8O_MX_ROPE; ++j)
+                dr += (double)q_rope[(int64_t)h * KV8O_MX_ROPE + j] * (double)k_rope[t * KV8O_MX_ROPE + j];
+            score[t] = (double)sm_scale * ((double)q_scale[h] * (double)k_scale[t] * dn + dr);
+            if (score[t] > m)
+                m = score[t];
+        }
+        double acc[KV8O_MX_D], z = 0.0;
+        for (int i = 0; i < KV8O_MX_D; ++i)
+            acc[i] = 0.0;
+        for (int64_t t = 0; t < T; ++t) {
+            const double p = exp(score[t] - m);
+            z += p;
+            const double ks = (double)k_scale[t];
+            for (int i = 0; i < KV8O_MX_NOPE; ++i)
+                acc[i] += p * ks * g_lut[k8[t * KV8O_MX_NOPE + i]];
+            for (int j = 0; j < KV8O_MX_ROPE; ++j)
+                acc[KV8O_MX_NOPE + j] += p * (double)k_rope[t * KV8O_MX_ROPE + j];
+        }
+        for (int i = 0; i < KV8O_MX_D; ++i)
+            out[(int64_t)h * KV8O_MX_D + i] = z > 0.0 ? (float)(acc[i] / z) : 0.0f;
+        free(score);
+    }
+}
+
 int kv8o_num_threads(void)
 {
 #ifdef _OPENMP

@@ -18,6 +18,8 @@ Workloads (one query position = one decode step of one layer):
   7 proj_prefill  the same for S=1024 query rows
   8 indexer   B=8 queries x 64 index heads x 128 (bf16 N(0,1)), head weights N(0,1)/8; per query its own
               T=131072 index-key rows N(0,1)*10^U(-0.5,0.5) of width 128; top NS=2048
+  10 mixed_dec H=128, T=65536: rows of 448 no-position values N(0,1)*10^U(-1,1) (quantized in set-up) and 64
+              RoPE values N(0,1) rounded to bf16; queries N(0,1) rounded to bf16 (448 + 64 per head)
   9 batch_dec B=8 sequences, sequence b of length 32768 - 997 b (its own cache of 32768 rows, rows drawn
               as for dec16k with sequence index b), H=128, bf16 queries; its last row is the fresh row
 """
@@ -65,6 +67,8 @@ WORKLOADS = {
     "indexer": Workload("indexer", 8, H=64, T=131072, B=8, NS=2048, mag_lo=10 ** -0.5, mag_hi=10 ** 0.5),
     # one decode step for a batch of sequences, each its own cache (ragged lengths, one fresh row each)
     "batch_dec": Workload("batch_dec", 9, H=128, T=32768, B=8),
+    # decode over the mixed-precision cache: 448 e4m3 no-position values + row scale, 64 bf16 RoPE values
+    "mixed_dec": Workload("mixed_dec", 10, H=128, T=65536),
 }
 
 DESCRIPTIONS = {
@@ -79,6 +83,8 @@ DESCRIPTIONS = {
     "proj_prefill": "absorb projections for a prefill chunk: S=1024 queries x H=128 heads through an fmt=8 kv_b",
     "indexer": "DSA lightning indexer: B=8 queries, each scoring its own T=131072 e4m3 index keys (width 128) "
                "with 64 index heads, then top-2048",
+    "mixed_dec": "mixed-precision cache decode: H=128 heads over T=65536 rows of 448 e4m3 no-position values "
+                 "(per-row f32 scale) + 64 bf16 RoPE values; bf16 queries",
     "batch_dec": "batched decode: B=8 sequences, each its own cache of up to T=32768 rows (lengths 32768 - 997 b), "
                  "H=128, bf16 queries, one fresh row appended to each sequence per step",
 }
@@ -227,3 +233,32 @@ def index_weights_for(w: Workload) -> np.ndarray:
 def batch_lengths(w: Workload) -> list[int]:
     """Ragged sequence lengths of the batched-decode workload."""
     return [w.T - 997 * b for b in range(w.B)]
+
+
+MX_NOPE, MX_ROPE = 448, 64
+
+
+def mixed_rows_for(w: Workload, start: int = 0, count: int | None = None):
+    """(no-position values [count][448] f32, RoPE values [count][64] f32 holding bf16 values) of the
+    mixed-cache workload, drawn in blocks of 4096 rows so any sub-range reproduces."""
+    if count is None:
+        count = w.T - start
+    nope = np.empty((count, MX_NOPE), dtype=np.float32)
+    rope = np.empty((count, MX_ROPE), dtype=np.float32)
+    blk = 4096
+    for bi in range(start // blk, (start + count + blk - 1) // blk):
+        rng = np.random.default_rng([w.seed, 9, bi])
+        x = normal_f32(rng, (blk, MX_NOPE))
+        mag = 10.0 ** rng.uniform(np.log10(w.mag_lo), np.log10(w.mag_hi), blk)
+        x = (x * mag[:, None]).astype(np.float32)
+        r = to_bf16_values(normal_f32(rng, (blk, MX_ROPE)))
+        lo, hi = max(start, bi * blk), min(start + count, (bi + 1) * blk)
+        nope[lo - start:hi - start] = x[lo - bi * blk:hi - bi * blk]
+        rope[lo - start:hi - start] = r[lo - bi * blk:hi - bi * blk]
+    return nope, rope
+
+
+def mixed_queries_for(w: Workload):
+    """(q_nope [H][448], q_rope [H][64]): bf16-representable N(0,1)."""
+    q = to_bf16_values(normal_f32(rng_for(w, 10), (w.H, MX_NOPE + MX_ROPE)))
+    return np.ascontiguousarray(q[:, :MX_NOPE]), np.ascontiguousarray(q[:, MX_NOPE:])

@@ -612,3 +612,86 @@ def test_topk_ties_order_and_brute_force(oracle):
         order = sorted(range(n), key=lambda i: (-s[i], i))[:k]
         assert list(got) == sorted(order)
         assert np.all(np.diff(got) > 0)
+
+
+# ------------------------------------------------------------------------------------------------
+# mixed-precision cache (448 e4m3 no-position values + f32 row scale, 64 bf16 RoPE values per row)
+# ------------------------------------------------------------------------------------------------
+def _mixed_cache(oracle, T, seed, mag=(0.1, 10.0)):
+    rng = np.random.default_rng(seed)
+    nope = (rng.standard_normal((T, 448)) * 10.0 ** rng.uniform(np.log10(mag[0]), np.log10(mag[1]), (T, 1))).astype(np.float32)
+    k8, ks = oracle.quant_rows_w(nope, 448)
+    kr = torch.from_numpy(rng.standard_normal((T, 64)).astype(np.float32)).to(torch.bfloat16).float().numpy()
+    return rng, k8, ks, kr
+
+
+def _torch_q8(qn):
+    """Independent per-row quantization of the queries: torch's f32 amax / multiply / float8_e4m3fn."""
+    t = torch.from_numpy(qn)
+    amax = t.abs().amax(dim=1, keepdim=True)
+    q8 = (t * (torch.tensor(448.0) / amax)).to(torch.float8_e4m3fn)
+    return q8.to(torch.float64).numpy(), (amax[:, 0] / torch.tensor(448.0)).double().numpy()
+
+
+def test_mixed_quant_width_448_matches_torch(oracle):
+    rng = np.random.default_rng(50)
+    x = (rng.standard_normal((200, 448)) * 10.0 ** rng.uniform(-3, 3, (200, 1))).astype(np.float32)
+    q, s = oracle.quant_rows_w(x, 448)
+    d, sc = _torch_q8(x)
+    assert np.array_equal(torch.from_numpy(q).view(torch.float8_e4m3fn).to(torch.float64).numpy(), d)
+    assert np.array_equal(s.astype(np.float64), sc)
+
+
+def test_mixed_single_row_returns_the_row(oracle):
+    _, k8, ks, kr = _mixed_cache(oracle, 1, 51)
+    rng = np.random.default_rng(52)
+    out = oracle.attn_mixed_decode(rng.standard_normal((4, 448)).astype(np.float32),
+                                   rng.standard_normal((4, 64)).astype(np.float32), k8, ks, kr, 0.07)
+    dk = torch.from_numpy(k8).view(torch.float8_e4m3fn).to(torch.float64).numpy()[0] * np.float64(ks[0])
+    for h in range(4):
+        assert np.array_equal(out[h, :448], dk.astype(np.float32)) and np.array_equal(out[h, 448:], kr[0])
+
+
+def test_mixed_zero_query_is_the_mean(oracle):
+    T = 37
+    _, k8, ks, kr = _mixed_cache(oracle, T, 53)
+    out = oracle.attn_mixed_decode(np.zeros((2, 448), np.float32), np.zeros((2, 64), np.float32), k8, ks, kr, 0.07)
+    dk = torch.from_numpy(k8).view(torch.float8_e4m3fn).to(torch.float64).numpy() * ks[:, None].astype(np.float64)
+    want = np.concatenate([dk.mean(axis=0), kr.astype(np.float64).mean(axis=0)]).astype(np.float32)
+    np.testing.assert_allclose(out[0], want, rtol=1e-6, atol=1e-6 * np.abs(want).max())
+
+
+def test_mixed_two_rows_differing_in_rope_closed_form(oracle):
+    """Equal no-position parts, different RoPE parts: the weights are sigma(+-Delta) with Delta the
+    sm_scale-weighted RoPE dot difference (the RoPE part enters the score unscaled)."""
+    _, k8, ks, kr = _mixed_cache(oracle, 2, 54)
+    k8[1], ks[1] = k8[0], ks[0]
+    rng = np.random.default_rng(55)
+    qn = rng.standard_normal((3, 448)).astype(np.float32)
+    qr = torch.from_numpy(rng.standard_normal((3, 64)).astype(np.float32)).to(torch.bfloat16).float().numpy()
+    sm = 0.25
+    out = oracle.attn_mixed_decode(qn, qr, k8, ks, kr, sm)
+    delta = sm * (qr.astype(np.float64) @ (kr[0].astype(np.float64) - kr[1].astype(np.float64)))
+    w0 = 1.0 / (1.0 + np.exp(-delta))
+    dk = torch.from_numpy(k8[0].copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy() * np.float64(ks[0])
+    for h in range(3):
+        want_rope = w0[h] * kr[0] + (1 - w0[h]) * kr[1]
+        np.testing.assert_allclose(out[h, 448:], want_rope, rtol=1e-6, atol=1e-6)
+        np.testing.assert_allclose(out[h, :448], dk, rtol=1e-6, atol=1e-6 * np.abs(dk).max())
+
+
+def test_mixed_matches_a_double_softmax(oracle):
+    T, H = 300, 5
+    rng, k8, ks, kr = _mixed_cache(oracle, T, 56)
+    qn = torch.from_numpy(rng.standard_normal((H, 448)).astype(np.float32)).to(torch.bfloat16).float().numpy()
+    qr = torch.from_numpy(rng.standard_normal((H, 64)).astype(np.float32)).to(torch.bfloat16).float().numpy()
+    sm = float(np.float32(1.0 / np.sqrt(512.0)))
+    q8, qs = _torch_q8(qn)
+    dk = torch.from_numpy(k8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    s = sm * ((qs[:, None] * ks[None, :].astype(np.float64)) * (q8 @ dk.T) + qr.astype(np.float64) @ kr.T.astype(np.float64))
+    p = np.exp(s - s.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    vals = np.concatenate([dk * ks[:, None].astype(np.float64), kr.astype(np.float64)], axis=1)
+    want = p @ vals
+    got = oracle.attn_mixed_decode(qn, qr, k8, ks, kr, sm)
+    np.testing.assert_allclose(got, want, rtol=1e-6, atol=1e-6 * np.abs(want).max())
