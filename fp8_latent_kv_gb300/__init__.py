@@ -36,6 +36,8 @@ SIGNATURES = {
     "mla_q_absorb8": (_I, [_P, _I, _I, _I, _P, _P, _P, _I, _P]),
     "kv8_quant_rows_w": (_I, [_P, _I64, _I, _P, _P, _P]),
     "kv8_quant_rows_scatter": (_I, [_P, _I64, _P, _P, _P, _I64, _P, _P]),
+    "mla_mixed_decode8_workspace_bytes": (_I, [_I, _I64, _P]),
+    "mla_absorb_mixed_decode8": (_I, [_P, _P, _I, _I, _P, _P, _P, _I64, _F, _P, _SZ, _P, _P, _P]),
     "mla_batch_decode8_workspace_bytes": (_I, [_I, _I, _I64, _P]),
     "mla_absorb_batch_decode8": (_I, [_P, _P, _I, _I, _I, _P, _P, _I64, _I64, _P, _F, _P, _SZ, _P, _P, _P]),
     "dsa_index_workspace_bytes": (_I, [_I, _P]),
@@ -131,6 +133,23 @@ def mla_decode8_partial(q_lat, q_rope, kv8, kv_scale, T: int, sm_scale: float, w
     _check("mla_decode8_partial", load().mla_decode8_partial(
         _ptr(q_lat), _ptr(q_rope), _qdtype(q_lat), H, _ptr(kv8), _ptr(kv_scale), T, sm_scale, P_req,
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err_word), _stream(stream)))
+
+
+def mla_mixed_decode8_workspace_bytes(H: int, T: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check("mla_mixed_decode8_workspace_bytes", load().mla_mixed_decode8_workspace_bytes(H, T, ctypes.addressof(out)))
+    return out.value
+
+
+def mla_absorb_mixed_decode8(q_nope, q_rope, k8, k_scale, k_rope, sm_scale: float, workspace, out, err_word=None,
+                             stream=None) -> None:
+    """Mixed-cache decode: q_nope [H][448], q_rope [H][64] (f32 or bf16); k8 [T][448] uint8, k_scale [T] f32,
+    k_rope [T][64] bf16 -> out [H][512] f32."""
+    H = q_nope.shape[-2]
+    T = k8.shape[0]
+    _check("mla_absorb_mixed_decode8", load().mla_absorb_mixed_decode8(
+        _ptr(q_nope), _ptr(q_rope), _qdtype(q_nope), H, _ptr(k8), _ptr(k_scale), _ptr(k_rope), T, sm_scale,
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err_word), _ptr(out), _stream(stream)))
 
 
 def kv8_quant_rows_scatter(x, dst_rows, kv8, kv_scale, err_word=None, stream=None) -> None:

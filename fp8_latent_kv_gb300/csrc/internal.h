@@ -50,6 +50,10 @@ cudaError_t launch_q_absorb(const void *q_nope, int q_bf16, int S, int H, const 
                             void *q_lat, int out_bf16, cudaStream_t st);
 cudaError_t launch_out_project(const float *ctx, int S, int H, const uint8_t *w8, const float *w_scale, float *out,
                                cudaStream_t st);
+int mixed_partitions(int H, int64_t T);
+cudaError_t launch_attn_mixed(const void *q_nope, const void *q_rope, int q_bf16, int H, const uint8_t *k8,
+                              const float *k_scale, const void *k_rope, int64_t T, float sm_scale_log2, int P,
+                              float *ws, cudaStream_t st);
 cudaError_t launch_copy(void *dst, const void *src, size_t bytes, cudaStream_t st);
 cudaError_t launch_lse_merge(const float *ws, int B, int P, int H, float *out, cudaStream_t st);
 

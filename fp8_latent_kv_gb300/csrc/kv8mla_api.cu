@@ -107,6 +107,30 @@ const char *kv8_strerror(int code) {
     }
 }
 
+int mla_mixed_decode8_workspace_bytes(int H, int64_t T, size_t *bytes) {
+    if (H < 1 || H > KV8_MAX_HEADS || T < 1 || T > KV8_MAX_ROWS || !bytes) return KV8_EINVAL;
+    *bytes = decode_partial_bytes(mixed_partitions(H, T), H);
+    return KV8_OK;
+}
+
+int mla_absorb_mixed_decode8(const void *q_nope, const void *q_rope, int q_dtype, int H, const uint8_t *k8,
+                             const float *k_scale, const void *k_rope, int64_t T, float sm_scale, void *workspace,
+                             size_t ws_bytes, int *err_word, float *out, void *stream) {
+    size_t need = 0;
+    int rc = mla_mixed_decode8_workspace_bytes(H, T, &need);
+    if (rc != KV8_OK) return rc;
+    if (!valid_q(q_nope, q_rope, q_dtype) || !aligned(k8, 16) || !aligned(k_scale, 4) || !aligned(k_rope, 16) ||
+        !isfinite(sm_scale) || !aligned(workspace, 16) || !aligned(out, 16))
+        return KV8_EINVAL;
+    if (ws_bytes < need) return KV8_EWORKSPACE;
+    (void)err_word;  // no device-side condition can arise: the kernel's only waits are __syncthreads
+    const int P = mixed_partitions(H, T);
+    rc = status(launch_attn_mixed(q_nope, q_rope, q_dtype == KV8_BF16, H, k8, k_scale, k_rope, T, sm_scale * kLog2e, P,
+                                  static_cast<float *>(workspace), (cudaStream_t)stream));
+    if (rc != KV8_OK) return rc;
+    return mla_lse_merge8(workspace, 1, P, H, out, stream);
+}
+
 int kv8_quant_rows_scatter(const float *x, int64_t n, const int64_t *dst_rows, uint8_t *kv8, float *kv_scale,
                            int64_t cache_rows, int *err_word, void *stream) {
     if (n < 0 || cache_rows < 0) return KV8_EINVAL;
@@ -161,7 +185,7 @@ int mla_absorb_batch_decode8(const void *q_lat, const void *q_rope, int q_dtype,
 }
 
 int kv8_quant_rows_w(const float *x, int64_t n, int width, uint8_t *q, float *scale, void *stream) {
-    if (n < 0 || (width != KV8_ROW_BYTES && width != KV8_IDX_D)) return KV8_EINVAL;
+    if (n < 0 || (width != KV8_ROW_BYTES && width != KV8_IDX_D && width != KV8_MX_NOPE)) return KV8_EINVAL;
     if (n == 0) return KV8_OK;
     if (!aligned(x, 16) || !aligned(q, 16) || !aligned(scale, 4)) return KV8_EINVAL;
     return status(launch_quant_rows_w(x, n, width, q, scale, (cudaStream_t)stream));

@@ -85,6 +85,8 @@ cudaError_t launch_quant_rows_w(const float *x, int64_t n, int width, uint8_t *q
         quant_rows_kernel<kRow><<<(unsigned)blocks, 256, 0, st>>>(x, n, q, scale, nullptr, 0, nullptr);
     else if (width == KV8_IDX_D)
         quant_rows_kernel<KV8_IDX_D><<<(unsigned)blocks, 256, 0, st>>>(x, n, q, scale, nullptr, 0, nullptr);
+    else if (width == KV8_MX_NOPE)
+        quant_rows_kernel<KV8_MX_NOPE><<<(unsigned)blocks, 256, 0, st>>>(x, n, q, scale, nullptr, 0, nullptr);
     else
         return cudaErrorInvalidValue;
     return cudaGetLastError();

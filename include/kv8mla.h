@@ -64,6 +64,8 @@ extern "C" {
 #define KV8_KVB_BLOCK 128      /* fmt=8 scale block edge: one f32 scale per 128x128 weight block */
 #define KV8_IDX_D 128          /* DSA indexer: index key / index query head width */
 #define KV8_MAX_IDX_HEADS 128  /* DSA indexer: index heads per query (a multiple of 16) */
+#define KV8_MX_NOPE 448        /* mixed cache: no-position values per row (e4m3 + row scale) */
+#define KV8_MX_ROPE 64         /* mixed cache: RoPE values per row (bf16) */
 
 /* return codes */
 #define KV8_OK 0
@@ -104,7 +106,7 @@ KV8_API int kv8_encode_e4m3(const float *y, int64_t n, uint8_t *out, void *strea
 KV8_API int kv8_quant_rows(const float *x, int64_t n, uint8_t *kv8, float *kv_scale, void *stream);
 
 /* kv8_quant_rows_w -- the same row quantizer for rows of `width` elements: width = KV8_ROW_BYTES (cache
- * rows, as kv8_quant_rows) or KV8_IDX_D (DSA index keys).  x [n][width] f32 -> q [n][width] e4m3,
+ * rows, as kv8_quant_rows), KV8_IDX_D (DSA index keys) or KV8_MX_NOPE (mixed-cache no-position parts).  x [n][width] f32 -> q [n][width] e4m3,
  * scale [n] f32.  Any other width is KV8_EINVAL. */
 KV8_API int kv8_quant_rows_w(const float *x, int64_t n, int width, uint8_t *q, float *scale, void *stream);
 
@@ -208,6 +210,24 @@ KV8_API int mla_absorb_prefill8(const void *q_lat, const void *q_rope, int q_dty
 KV8_API int mla_absorb_decode8_noalloc(const void *q_lat, const void *q_rope, int q_dtype, int H,
                                        const uint8_t *kv8, const float *kv_scale, int64_t T, float sm_scale,
                                        int P_req, int *err_word, float *out, void *stream);
+
+/* -----------------------------------------------------------------------------------------------
+ * mla_absorb_mixed_decode8 -- decode over the mixed-precision cache ([B1] "B1 Mixed FP8/BF16 FMHA first
+ * pass": the no-position part of each KV row stored as e4m3 with a per-row f32 scale, the RoPE part as
+ * bf16, the query's no-position part quantized from bf16 to e4m3 before the attention; head width
+ * 512 = KV8_MX_NOPE + KV8_MX_ROPE; the row is both key and value).  For each head h:
+ *     (q8[h], q_scale[h]) = the row quantizer (amax/448) applied to q_nope[h]
+ *     score[h][t] = sm_scale * ( q_scale[h] * k_scale[t] * e4m3(q8[h]).e4m3(k8[t]) + q_rope[h].k_rope[t] )
+ *     out[h] = sum_t softmax_t(score[h]) * [ k_scale[t] * e4m3(k8[t]) , k_rope[t] ]        (512 f32)
+ *   q_nope [H][448], q_rope [H][64] of type q_dtype; k8 [T][448] e4m3 (kv8_quant_rows_w, width 448),
+ *   k_scale [T] f32, k_rope [T][64] bf16; out [H][512] f32.  H in [1, 128]; T in [1, KV8_MAX_ROWS].
+ *   workspace: >= mla_mixed_decode8_workspace_bytes(H, T) (split-T partial sets as for mla_decode8_partial;
+ *   merged by mla_lse_merge8 inside the call).  Runs on the CUDA cores (f32 arithmetic).
+ * --------------------------------------------------------------------------------------------- */
+KV8_API int mla_mixed_decode8_workspace_bytes(int H, int64_t T, size_t *bytes);
+KV8_API int mla_absorb_mixed_decode8(const void *q_nope, const void *q_rope, int q_dtype, int H, const uint8_t *k8,
+                                     const float *k_scale, const void *k_rope, int64_t T, float sm_scale,
+                                     void *workspace, size_t ws_bytes, int *err_word, float *out, void *stream);
 
 /* -----------------------------------------------------------------------------------------------
  * mla_absorb_batch_decode8 -- one decode step for B sequences at once, each with its own cache and length
