@@ -14,6 +14,7 @@ Other workloads (--workload), each one step of its own hot path:
            head output) for 1 query / a 1024-query chunk of 128 heads
   indexer  the DSA lightning indexer: 8 queries x 64 index heads over 131072 e4m3 index keys each, top-2048
   batch_dec  one decode step for 8 sequences with their own caches (up to 32768 rows each, ragged)
+  mixed_dec  one decode step over the mixed-precision cache (448 e4m3 + 64 bf16 per row), T = 65536
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload KEY]
 For N > 1 launch with torchrun; every rank runs an independent replica (one layer's attention does
@@ -747,13 +748,111 @@ class BatchDecodeCase(Case):
         return (time.perf_counter() - t0) * self._scale
 
 
+class MixedDecodeCase(Case):
+    """One decode step over the mixed-precision cache: the fresh row's no-position part quantized into the
+    cache and its bf16 RoPE part stored, then the decode (CUDA cores) and the merge."""
+    launches_per_step = 4  # quant (448) + RoPE copy + partial + merge
+    kernel_calls = "mla_absorb_mixed_decode8: attn_mixed_kernel + lse_merge_kernel"
+    step_desc = "kv8_quant_rows_w(fresh row, width 448) + RoPE copy + mixed-cache split-T decode + merge"
+    dtype = "e4m3+bf16 -> f32 (CUDA cores)"
+
+    def __init__(self, kv, torch, dev, w):
+        import synth
+        self.kv, self.torch, self.w = kv, torch, w
+        H, T = w.H, w.T
+        nope, rope = synth.mixed_rows_for(w)
+        self.k8 = torch.empty((T, 448), dtype=torch.uint8, device=dev)
+        self.ks = torch.empty(T, dtype=torch.float32, device=dev)
+        xn = torch.from_numpy(nope).to(dev)
+        kv.kv8_quant_rows_w(xn[:-1], self.k8[:-1], self.ks[:-1])
+        self.fresh_nope = xn[-1:].clone()
+        del xn
+        self.k_rope = torch.from_numpy(rope).to(dev).to(torch.bfloat16)
+        self.fresh_rope = self.k_rope[-1:].clone()
+        qn, qr = synth.mixed_queries_for(w)
+        self.qn, self.qr = _bf16(torch, dev, qn), _bf16(torch, dev, qr)
+        self.ws = torch.empty(kv.mla_mixed_decode8_workspace_bytes(H, T) // 4, dtype=torch.float32, device=dev)
+        self.out = torch.empty((H, 512), dtype=torch.float32, device=dev)
+        self.pack = Packed(torch, dev, [self.qn, self.qr, self.fresh_nope, self.fresh_rope])
+        self.h_out = torch.empty((H, 512), dtype=torch.float32).pin_memory()
+        self.h2d = self.pack.nbytes
+        self.d2h = self.h_out.numel() * 4
+        self.alg_bytes = T * (448 + 4 + 128) + self.qn.numel() * 2 + self.qr.numel() * 2
+        self.alg_bytes_step = self.alg_bytes + self.d2h
+        self.flops = 2.0 * H * T * (448 + 64 + 512)
+
+    def _decode(self, qn, qr, stream):
+        self.kv.mla_absorb_mixed_decode8(qn, qr, self.k8, self.ks, self.k_rope, SM_SCALE(), self.ws, self.out,
+                                         stream=stream)
+
+    def _append(self, fresh_nope, fresh_rope, stream):
+        T = self.w.T
+        self.kv.kv8_quant_rows_w(fresh_nope, self.k8[T - 1:], self.ks[T - 1:], stream=stream)
+        self.kv.kv8_copy(self.k_rope[T - 1:], fresh_rope, stream=stream)
+
+    def step(self, stream, ev=None):
+        self._append(self.fresh_nope, self.fresh_rope, stream)
+        if ev is not None:
+            ev[0].record(stream)
+        self._decode(self.qn, self.qr, stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def kernel_call(self, stream):
+        self._decode(self.qn, self.qr, stream)
+
+    def e2e_step(self, stream):
+        kv = self.kv
+        self.pack.upload(kv, stream)
+        qn, qr, fn, fr = self.pack.views
+        self._append(fn, fr, stream)
+        self._decode(qn, qr, stream)
+        kv.kv8_copy(self.h_out, self.out, stream=stream)
+
+    def config(self):
+        w = self.w
+        return {"H": w.H, "T": w.T, "row": "448 e4m3 + f32 scale + 64 bf16"}
+
+    def roofline(self, kern_s, peaks, key):
+        hbm_gbs = self.alg_bytes / kern_s / 1e9
+        tflops = self.flops / kern_s / 1e12
+        return {"bound": "alu", "achieved": tflops, "peak": SIMT_F32_PEAK_TFLOPS, "unit": "TFLOP/s",
+                "frac": tflops / SIMT_F32_PEAK_TFLOPS,
+                "peak_source": "152 SMs x 128 f32 lanes x 2 flop (FMA) x 2070 MHz (the maximum SM clock)",
+                "kernel": "attn_mixed_kernel (attn_mixed.cu) + lse_merge_kernel", "events_bracket": self.kernel_calls,
+                "traffic": traffic_per_launch(key, "attn_mixed_kernel", ["fp8_latent_kv_gb300/csrc/attn_mixed.cu"]),
+                "algorithmic_bytes": self.alg_bytes, "algorithmic_flops": self.flops, "kernel_us": kern_s * 1e6,
+                "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / peaks["hbm_gbs"], "hbm_peak_gbs": peaks["hbm_gbs"],
+                "tflops": tflops}
+
+    def oracle_setup(self, n_heads):
+        import oracle
+        import synth
+        w = self.w
+        nope, rope = synth.mixed_rows_for(w)
+        k8, ks = oracle.quant_rows_w(nope, 448)
+        qn, qr = synth.mixed_queries_for(w)
+        heads = np.linspace(0, w.H - 1, n_heads).astype(int)
+        self._o = (np.ascontiguousarray(qn[heads]), np.ascontiguousarray(qr[heads]), k8, ks, rope)
+        self._scale = w.H / n_heads
+        return f"{n_heads} of {w.H} heads over all T={w.T} rows, scaled by heads to the step"
+
+    def oracle_step(self) -> float:
+        import oracle
+        qn, qr, k8, ks, rope = self._o
+        t0 = time.perf_counter()
+        oracle.attn_mixed_decode(qn, qr, k8, ks, rope, SM_SCALE())
+        return (time.perf_counter() - t0) * self._scale
+
+
 CASES = {"dec262k": DecodeCase, "dec16k": DecodeCase, "dsa": SelectCase, "prefill": PrefillCase,
-         "proj_dec": ProjCase, "proj_prefill": ProjCase, "indexer": IndexerCase, "batch_dec": BatchDecodeCase}
+         "proj_dec": ProjCase, "proj_prefill": ProjCase, "indexer": IndexerCase, "batch_dec": BatchDecodeCase,
+         "mixed_dec": MixedDecodeCase}
 # the oracle's sample: heads for the attention workloads, query rows for the projections
 ORACLE_HEADS = {"dec262k": 32, "dec16k": 128, "dsa": 128, "prefill": 8, "proj_dec": 1, "proj_prefill": 64,
-                "indexer": 1, "batch_dec": 16}
+                "indexer": 1, "batch_dec": 16, "mixed_dec": 32}
 REFERENCE_HEADS = {"dec262k": 8, "dec16k": 32, "dsa": 32, "prefill": 4, "proj_dec": 1, "proj_prefill": 16,
-                   "indexer": 1, "batch_dec": 4}
+                   "indexer": 1, "batch_dec": 4, "mixed_dec": 8}
 
 
 def SM_SCALE():
