@@ -476,7 +476,7 @@ SIMT_F32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # 152 SMs x 128 f32 lanes 
 class ProjCase(Case):
     """The absorb projections through an fmt=8 kv_b: q_nope -> q_lat (bf16, the attention's query) and a
     context -> the head outputs, both on one stream.  A decode step (S = 1) reads every weight byte once
-    (HBM-bound); a prefill chunk (S = 1024) is f32 FMA work on the CUDA cores."""
+    on the CUDA cores; a prefill chunk (S = 1024) runs on the tensor cores; both are HBM-bound."""
     launches_per_step = 2
     kernel_calls = "mla_q_absorb8 + mla_out_project8"
 
@@ -532,21 +532,19 @@ class ProjCase(Case):
         return {"S": self.w.S, "H": self.w.H, "kv_b": "fmt=8: 128x256 rows x 512 e4m3 bytes, 128x128-block f32 scales"}
 
     def roofline(self, kern_s, peaks, key):
+        # both shapes sit below the ridge (S = 1: 2 flop per weight byte; S = 1024: ~68 flop per byte of
+        # activations in and out), so the bound is HBM; the tensor-core rate is reported beside it
         hbm_gbs = self.alg_bytes / kern_s / 1e9
         tflops = self.flops / kern_s / 1e12
-        common = {"kernel": "q_absorb + out_project (proj8.cu)", "events_bracket": self.kernel_calls,
-                  "traffic": traffic_per_launch(key, "proj8", ["fp8_latent_kv_gb300/csrc/proj8.cu"]),
-                  "algorithmic_bytes": self.alg_bytes, "algorithmic_flops": self.flops, "kernel_us": kern_s * 1e6,
-                  "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / peaks["hbm_gbs"], "hbm_peak_gbs": peaks["hbm_gbs"],
-                  "tflops": tflops}
-        if self.w.S <= 8:
-            return dict({"bound": "hbm", "achieved": hbm_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": hbm_gbs / peaks["hbm_gbs"], "peak_source": f"copy bandwidth ({peaks['source']})"},
-                        **common)
-        return dict({"bound": "alu", "achieved": tflops, "peak": SIMT_F32_PEAK_TFLOPS, "unit": "TFLOP/s",
-                     "frac": tflops / SIMT_F32_PEAK_TFLOPS,
-                     "peak_source": "152 SMs x 128 f32 lanes x 2 flop (FMA) x 2070 MHz (the maximum SM clock)"},
-                    **common)
+        kern = "q_absorb_small + out_project_small (proj8.cu, CUDA cores)" if self.w.S <= 8 else \
+            "q_absorb_tc_kernel + out_project_tc_kernel (proj8_tc.cu, tcgen05 kind::f16)"
+        return {"bound": "hbm", "achieved": hbm_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": hbm_gbs / peaks["hbm_gbs"], "peak_source": f"copy bandwidth ({peaks['source']})",
+                "kernel": kern, "events_bracket": self.kernel_calls,
+                "traffic": None, "algorithmic_bytes": self.alg_bytes, "algorithmic_flops": self.flops,
+                "kernel_us": kern_s * 1e6, "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / peaks["hbm_gbs"],
+                "hbm_peak_gbs": peaks["hbm_gbs"], "tflops": tflops,
+                "tensor_frac_of_bf16_peak": tflops / peaks["bf16_tflops"] if self.w.S > 8 else None}
 
     def oracle_setup(self, n_rows):
         import synth

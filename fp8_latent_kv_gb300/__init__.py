@@ -33,7 +33,7 @@ SIGNATURES = {
     "mla_absorb_sel8": (_I, [_P, _P, _I, _I, _I, _P, _P, _I64, _I64, _P, _I, _F, _P, _SZ, _P, _P, _P]),
     "mla_absorb_prefill8": (_I, [_P, _P, _I, _I, _I, _I64, _P, _P, _I64, _F, _P, _P, _P]),
     "mla_absorb_decode8_noalloc": (_I, [_P, _P, _I, _I, _P, _P, _I64, _F, _I, _P, _P, _P]),
-    "mla_q_absorb8": (_I, [_P, _I, _I, _I, _P, _P, _P, _I, _P]),
+    "mla_q_absorb8": (_I, [_P, _I, _I, _I, _P, _P, _P, _I, _P, _P]),
     "kv8_quant_rows_w": (_I, [_P, _I64, _I, _P, _P, _P]),
     "kv8_quant_rows_scatter": (_I, [_P, _I64, _P, _P, _P, _I64, _P, _P]),
     "mla_mixed_decode8_workspace_bytes": (_I, [_I, _I64, _P]),
@@ -42,7 +42,7 @@ SIGNATURES = {
     "mla_absorb_batch_decode8": (_I, [_P, _P, _I, _I, _I, _P, _P, _I64, _I64, _P, _F, _P, _SZ, _P, _P, _P]),
     "dsa_index_workspace_bytes": (_I, [_I, _P]),
     "dsa_index_topk8": (_I, [_P, _I, _P, _I, _I, _P, _P, _I64, _I64, _I, _P, _SZ, _P, _P, _P, _P]),
-    "mla_out_project8": (_I, [_P, _I, _I, _P, _P, _P, _P]),
+    "mla_out_project8": (_I, [_P, _I, _I, _P, _P, _P, _P, _P]),
     "kv8_copy": (_I, [_P, _P, _SZ, _P]),
     "kv8_strerror": (ctypes.c_char_p, [_I]),
 }
@@ -201,21 +201,21 @@ def dsa_index_topk8(q_idx, w, k8, k_scale, T: int, seq_stride_rows: int, NS: int
         _stream(stream)))
 
 
-def mla_q_absorb8(q_nope, w8, w_scale, q_lat, stream=None) -> None:
+def mla_q_absorb8(q_nope, w8, w_scale, q_lat, err_word=None, stream=None) -> None:
     """q_lat [S][H][512] (f32 or bf16 tensor) = q_nope [S][H][128] (f32 or bf16) through the key rows of
     the fmt=8 kv_b (w8 [H*256][512] uint8, w_scale [H*2][4] f32)."""
     H = q_nope.shape[-2]
     S = q_nope.numel() // (H * 128)
     _check("mla_q_absorb8", load().mla_q_absorb8(_ptr(q_nope), _qdtype(q_nope), S, H, _ptr(w8), _ptr(w_scale),
-                                                 _ptr(q_lat), _qdtype(q_lat), _stream(stream)))
+                                                 _ptr(q_lat), _qdtype(q_lat), _ptr(err_word), _stream(stream)))
 
 
-def mla_out_project8(ctx, w8, w_scale, out, stream=None) -> None:
+def mla_out_project8(ctx, w8, w_scale, out, err_word=None, stream=None) -> None:
     """out [S][H][128] f32 = ctx [S][H][512] f32 through the value rows of the fmt=8 kv_b."""
     H = ctx.shape[-2]
     S = ctx.numel() // (H * 512)
     _check("mla_out_project8", load().mla_out_project8(_ptr(ctx), S, H, _ptr(w8), _ptr(w_scale), _ptr(out),
-                                                       _stream(stream)))
+                                                       _ptr(err_word), _stream(stream)))
 
 
 def kv8_copy(dst, src, nbytes: int | None = None, stream=None) -> None:

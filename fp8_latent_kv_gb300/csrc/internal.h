@@ -47,9 +47,13 @@ cudaError_t launch_attn_simt(const AttnArgs &a, cudaStream_t st);
 cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t st);
 size_t tc_scratch_bytes(int B, int P);
 cudaError_t launch_q_absorb(const void *q_nope, int q_bf16, int S, int H, const uint8_t *w8, const float *w_scale,
-                            void *q_lat, int out_bf16, cudaStream_t st);
+                            void *q_lat, int out_bf16, int *err_word, cudaStream_t st);
 cudaError_t launch_out_project(const float *ctx, int S, int H, const uint8_t *w8, const float *w_scale, float *out,
-                               cudaStream_t st);
+                               int *err_word, cudaStream_t st);
+cudaError_t launch_q_absorb_tc(const void *q_nope, int q_bf16, int S, int H, const uint8_t *w8, const float *w_scale,
+                               void *q_lat, int out_bf16, int *err_word, cudaStream_t st);
+cudaError_t launch_out_project_tc(const float *ctx, int S, int H, const uint8_t *w8, const float *w_scale, float *out,
+                                  int *err_word, cudaStream_t st);
 int mixed_partitions(int H, int64_t T);
 cudaError_t launch_attn_mixed(const void *q_nope, const void *q_rope, int q_bf16, int H, const uint8_t *k8,
                               const float *k_scale, const void *k_rope, int64_t T, float sm_scale_log2, int P,

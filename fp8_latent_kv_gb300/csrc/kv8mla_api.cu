@@ -215,20 +215,20 @@ int dsa_index_topk8(const void *q_idx, int q_dtype, const float *w, int B, int H
 }
 
 int mla_q_absorb8(const void *q_nope, int q_dtype, int S, int H, const uint8_t *w8, const float *w_scale,
-                  void *q_lat, int out_dtype, void *stream) {
+                  void *q_lat, int out_dtype, int *err_word, void *stream) {
     if (S < 1 || S > KV8_MAX_ROWS || H < 1 || H > KV8_MAX_HEADS) return KV8_EINVAL;
     if (!aligned(q_nope, 16) || !aligned(w8, 16) || !aligned(w_scale, 4) || !aligned(q_lat, 16)) return KV8_EINVAL;
     if ((q_dtype != KV8_F32 && q_dtype != KV8_BF16) || (out_dtype != KV8_F32 && out_dtype != KV8_BF16))
         return KV8_EINVAL;
     return status(launch_q_absorb(q_nope, q_dtype == KV8_BF16, S, H, w8, w_scale, q_lat, out_dtype == KV8_BF16,
-                                  (cudaStream_t)stream));
+                                  err_word, (cudaStream_t)stream));
 }
 
 int mla_out_project8(const float *ctx, int S, int H, const uint8_t *w8, const float *w_scale, float *out,
-                     void *stream) {
+                     int *err_word, void *stream) {
     if (S < 1 || S > KV8_MAX_ROWS || H < 1 || H > KV8_MAX_HEADS) return KV8_EINVAL;
     if (!aligned(ctx, 16) || !aligned(w8, 16) || !aligned(w_scale, 4) || !aligned(out, 16)) return KV8_EINVAL;
-    return status(launch_out_project(ctx, S, H, w8, w_scale, out, (cudaStream_t)stream));
+    return status(launch_out_project(ctx, S, H, w8, w_scale, out, err_word, (cudaStream_t)stream));
 }
 
 int kv8_copy(void *dst, const void *src, size_t bytes, void *stream) {

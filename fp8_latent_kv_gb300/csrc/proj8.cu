@@ -10,9 +10,9 @@
 // sum); an output row of W_UV crosses four blocks, so each block's partial sum takes its own scale.
 // Weights are decoded exactly (e4m3 -> f16 -> f32) and products summed in f32.
 //
-// Two shapes each: a few query rows (decode: every weight byte is read once, coalesced, and used for
-// all rows) and many (prefill chunks: per head a shared-memory-tiled f32 product, the weight block
-// decoded once per CTA and reused by 64 rows).
+// This file holds the shape for a few query rows (decode: every weight byte is read once, coalesced,
+// and used for all rows, on the CUDA cores); more rows (prefill chunks) go to the tensor-core kernels of
+// proj8_tc.cu.
 #include "internal.h"
 
 namespace kv8 {
@@ -102,99 +102,6 @@ __global__ void __launch_bounds__(256) q_absorb_small(const void *__restrict__ q
 }
 
 // ------------------------------------------------------------------------------------------------
-// q absorb, many rows.  CTA (h, column block cb, 64-row tile): the 128x128 weight block decoded into
-// shared memory once, the tile's queries transposed beside it; thread (c4, sg) computes columns
-// 4c4..4c4+3 of rows 8sg..8sg+7.
-// ------------------------------------------------------------------------------------------------
-constexpr int kTileS = 64;
-struct QAbsorbSmem {
-    float w[kNope][kBlk];      // 64 KB: W_UK block, [j][c]
-    float qt[kNope][kTileS];   // 32 KB: queries, [j][s]
-};
-
-__global__ void __launch_bounds__(256) q_absorb_tiled(const void *__restrict__ q_nope, int q_bf16, int S, int H,
-                                                      const uint8_t *__restrict__ w8, const float *__restrict__ w_scale,
-                                                      void *__restrict__ q_lat, int out_bf16) {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    QAbsorbSmem &sm = *reinterpret_cast<QAbsorbSmem *>(smem_raw);
-    const int h = blockIdx.x, cb = blockIdx.y, s0 = blockIdx.z * kTileS, tid = threadIdx.x;
-    // weight block: 128 rows x 128 bytes, 16 bytes per thread per step
-    for (int i = tid; i < kNope * (kBlk / 16); i += 256) {
-        const int j = i >> 3, c16 = (i & 7) * 16;
-        const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(w8 + ((int64_t)h * kKvbRows + j) * kKL + cb * kBlk + c16));
-        *reinterpret_cast<float4 *>(&sm.w[j][c16 + 0]) = dec4(raw.x);
-        *reinterpret_cast<float4 *>(&sm.w[j][c16 + 4]) = dec4(raw.y);
-        *reinterpret_cast<float4 *>(&sm.w[j][c16 + 8]) = dec4(raw.z);
-        *reinterpret_cast<float4 *>(&sm.w[j][c16 + 12]) = dec4(raw.w);
-    }
-    // queries: item (s, j8) = 8 consecutive values of row s; consecutive threads take consecutive rows,
-    // so the transposed stores hit consecutive banks
-    for (int i = tid; i < kTileS * (kNope / 8); i += 256) {
-        const int s = i & (kTileS - 1), j8 = i / kTileS;
-        float v[8];
-        if (s0 + s < S) {
-            const int64_t base = ((int64_t)(s0 + s) * H + h) * kNope + 8 * j8;
-            if (q_bf16) {
-                const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(q_nope) + base));
-                const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u[k]));
-                    v[2 * k] = f.x;
-                    v[2 * k + 1] = f.y;
-                }
-            } else {
-                const float4 a = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(q_nope) + base));
-                const float4 b = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(q_nope) + base) + 1);
-                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-                v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-            }
-        } else {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) v[k] = 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) sm.qt[8 * j8 + k][s] = v[k];
-    }
-    __syncthreads();
-    const int c4 = tid & 31, sg = tid >> 5;
-    float acc[8][4];
-#pragma unroll
-    for (int a = 0; a < 8; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
-#pragma unroll 4
-    for (int j = 0; j < kNope; ++j) {
-        const float4 w = *reinterpret_cast<const float4 *>(&sm.w[j][4 * c4]);
-        const float4 qa = *reinterpret_cast<const float4 *>(&sm.qt[j][8 * sg]);
-        const float4 qb = *reinterpret_cast<const float4 *>(&sm.qt[j][8 * sg + 4]);
-        const float q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-#pragma unroll
-        for (int a = 0; a < 8; ++a) {
-            acc[a][0] = fmaf(q[a], w.x, acc[a][0]);
-            acc[a][1] = fmaf(q[a], w.y, acc[a][1]);
-            acc[a][2] = fmaf(q[a], w.z, acc[a][2]);
-            acc[a][3] = fmaf(q[a], w.w, acc[a][3]);
-        }
-    }
-    const float sc = __ldg(w_scale + (int64_t)(2 * h) * kNbc + cb);
-#pragma unroll
-    for (int a = 0; a < 8; ++a) {
-        const int s = s0 + 8 * sg + a;
-        if (s >= S) continue;
-        const int64_t o = ((int64_t)s * H + h) * kKL + cb * kBlk + 4 * c4;
-        if (out_bf16) {
-            __nv_bfloat162 *d = reinterpret_cast<__nv_bfloat162 *>(static_cast<__nv_bfloat16 *>(q_lat) + o);
-            d[0] = __floats2bfloat162_rn(acc[a][0] * sc, acc[a][1] * sc);
-            d[1] = __floats2bfloat162_rn(acc[a][2] * sc, acc[a][3] * sc);
-        } else {
-            *reinterpret_cast<float4 *>(static_cast<float *>(q_lat) + o) =
-                make_float4(acc[a][0] * sc, acc[a][1] * sc, acc[a][2] * sc, acc[a][3] * sc);
-        }
-    }
-}
-
-// ------------------------------------------------------------------------------------------------
 // out project, few rows.  CTA (h, 32 value rows): warp w takes rows 4w..4w+3 of them.  For a row, lane
 // l reads the 4 weight bytes at columns 128k + 4l (k = 0..3: one per scale block; each warp
 // instruction reads 128 contiguous bytes) and the matching context values (consecutive lanes,
@@ -247,138 +154,31 @@ __global__ void __launch_bounds__(256) out_project_small(const float *__restrict
     }
 }
 
-// ------------------------------------------------------------------------------------------------
-// out project, many rows.  CTA (h, 64-row tile); for each of the 4 column blocks: W_UV's 128x128
-// block decoded and transposed into shared memory ([c][v]) beside the tile's context ([c][s]);
-// thread (v4, sg) accumulates values 4v4..4v4+3 of rows 8sg..8sg+7 per block, then adds the block's
-// scaled sum.
-// ------------------------------------------------------------------------------------------------
-struct OutProjSmem {
-    float wt[kBlk][kVH];       // 64 KB: [c][v]
-    float xt[kBlk][kTileS];    // 32 KB: [c][s]
-};
-
-__global__ void __launch_bounds__(256) out_project_tiled(const float *__restrict__ ctx, int S, int H,
-                                                         const uint8_t *__restrict__ w8,
-                                                         const float *__restrict__ w_scale, float *__restrict__ out) {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    OutProjSmem &sm = *reinterpret_cast<OutProjSmem *>(smem_raw);
-    const int h = blockIdx.x, s0 = blockIdx.y * kTileS, tid = threadIdx.x;
-    const int v4 = tid & 31, sg = tid >> 5;
-    float acc[8][4];
-#pragma unroll
-    for (int a = 0; a < 8; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
-    for (int cb = 0; cb < kNbc; ++cb) {
-        if (cb > 0) __syncthreads();  // the previous block's operands are no longer read
-        // thread (v = tid & 127, half = tid >> 7): 64 bytes of row v, written transposed
-        {
-            const int v = tid & 127, c0 = (tid >> 7) * 64;
-            const uint4 *src = reinterpret_cast<const uint4 *>(w8 + ((int64_t)h * kKvbRows + kNope + v) * kKL + cb * kBlk + c0);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint4 raw = __ldg(src + q);
-                const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float4 f = dec4(u[k]);
-                    const int c = c0 + 16 * q + 4 * k;
-                    sm.wt[c + 0][v] = f.x;
-                    sm.wt[c + 1][v] = f.y;
-                    sm.wt[c + 2][v] = f.z;
-                    sm.wt[c + 3][v] = f.w;
-                }
-            }
-        }
-        for (int i = tid; i < kTileS * (kBlk / 4); i += 256) {
-            const int s = i & (kTileS - 1), c4 = i / kTileS;  // consecutive threads: consecutive rows
-            const float4 x = s0 + s < S ? __ldg(reinterpret_cast<const float4 *>(ctx + ((int64_t)(s0 + s) * H + h) * kKL + cb * kBlk) + c4)
-                                        : make_float4(0.f, 0.f, 0.f, 0.f);
-            sm.xt[4 * c4 + 0][s] = x.x;
-            sm.xt[4 * c4 + 1][s] = x.y;
-            sm.xt[4 * c4 + 2][s] = x.z;
-            sm.xt[4 * c4 + 3][s] = x.w;
-        }
-        __syncthreads();
-        float blk[8][4];
-#pragma unroll
-        for (int a = 0; a < 8; ++a)
-#pragma unroll
-            for (int b = 0; b < 4; ++b) blk[a][b] = 0.f;
-#pragma unroll 4
-        for (int c = 0; c < kBlk; ++c) {
-            const float4 w = *reinterpret_cast<const float4 *>(&sm.wt[c][4 * v4]);
-            const float4 xa = *reinterpret_cast<const float4 *>(&sm.xt[c][8 * sg]);
-            const float4 xb = *reinterpret_cast<const float4 *>(&sm.xt[c][8 * sg + 4]);
-            const float x[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-#pragma unroll
-            for (int a = 0; a < 8; ++a) {
-                blk[a][0] = fmaf(x[a], w.x, blk[a][0]);
-                blk[a][1] = fmaf(x[a], w.y, blk[a][1]);
-                blk[a][2] = fmaf(x[a], w.z, blk[a][2]);
-                blk[a][3] = fmaf(x[a], w.w, blk[a][3]);
-            }
-        }
-        const float sc = __ldg(w_scale + (int64_t)(2 * h + 1) * kNbc + cb);
-#pragma unroll
-        for (int a = 0; a < 8; ++a)
-#pragma unroll
-            for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(sc, blk[a][b], acc[a][b]);
-    }
-#pragma unroll
-    for (int a = 0; a < 8; ++a) {
-        const int s = s0 + 8 * sg + a;
-        if (s >= S) continue;
-        *reinterpret_cast<float4 *>(out + ((int64_t)s * H + h) * kVH + 4 * v4) =
-            make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
-    }
-}
-
-template <typename K>
-cudaError_t set_smem(K kernel, size_t bytes) {
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-}
-
 }  // namespace
 
 cudaError_t launch_q_absorb(const void *q_nope, int q_bf16, int S, int H, const uint8_t *w8, const float *w_scale,
-                            void *q_lat, int out_bf16, cudaStream_t st) {
-    if (S <= kSmallS) {
-        const dim3 grid((unsigned)H, (unsigned)kNbc);
-        if (S <= 1)
-            q_absorb_small<1><<<grid, 256, 0, st>>>(q_nope, q_bf16, S, H, w8, w_scale, q_lat, out_bf16);
-        else if (S <= 4)
-            q_absorb_small<4><<<grid, 256, 0, st>>>(q_nope, q_bf16, S, H, w8, w_scale, q_lat, out_bf16);
-        else
-            q_absorb_small<kSmallS><<<grid, 256, 0, st>>>(q_nope, q_bf16, S, H, w8, w_scale, q_lat, out_bf16);
-        return cudaGetLastError();
-    }
-    const size_t smem = sizeof(QAbsorbSmem);
-    cudaError_t e = set_smem(q_absorb_tiled, smem);
-    if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)H, (unsigned)kNbc, (unsigned)((S + kTileS - 1) / kTileS));
-    q_absorb_tiled<<<grid, 256, smem, st>>>(q_nope, q_bf16, S, H, w8, w_scale, q_lat, out_bf16);
+                            void *q_lat, int out_bf16, int *err_word, cudaStream_t st) {
+    if (S > kSmallS) return launch_q_absorb_tc(q_nope, q_bf16, S, H, w8, w_scale, q_lat, out_bf16, err_word, st);
+    const dim3 grid((unsigned)H, (unsigned)kNbc);
+    if (S <= 1)
+        q_absorb_small<1><<<grid, 256, 0, st>>>(q_nope, q_bf16, S, H, w8, w_scale, q_lat, out_bf16);
+    else if (S <= 4)
+        q_absorb_small<4><<<grid, 256, 0, st>>>(q_nope, q_bf16, S, H, w8, w_scale, q_lat, out_bf16);
+    else
+        q_absorb_small<kSmallS><<<grid, 256, 0, st>>>(q_nope, q_bf16, S, H, w8, w_scale, q_lat, out_bf16);
     return cudaGetLastError();
 }
 
 cudaError_t launch_out_project(const float *ctx, int S, int H, const uint8_t *w8, const float *w_scale, float *out,
-                               cudaStream_t st) {
-    if (S <= kSmallS) {
-        const dim3 grid((unsigned)H, (unsigned)(kVH / 32));
-        if (S <= 1)
-            out_project_small<1><<<grid, 256, 0, st>>>(ctx, S, H, w8, w_scale, out);
-        else if (S <= 4)
-            out_project_small<4><<<grid, 256, 0, st>>>(ctx, S, H, w8, w_scale, out);
-        else
-            out_project_small<kSmallS><<<grid, 256, 0, st>>>(ctx, S, H, w8, w_scale, out);
-        return cudaGetLastError();
-    }
-    const size_t smem = sizeof(OutProjSmem);
-    cudaError_t e = set_smem(out_project_tiled, smem);
-    if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)H, (unsigned)((S + kTileS - 1) / kTileS));
-    out_project_tiled<<<grid, 256, smem, st>>>(ctx, S, H, w8, w_scale, out);
+                               int *err_word, cudaStream_t st) {
+    if (S > kSmallS) return launch_out_project_tc(ctx, S, H, w8, w_scale, out, err_word, st);
+    const dim3 grid((unsigned)H, (unsigned)(kVH / 32));
+    if (S <= 1)
+        out_project_small<1><<<grid, 256, 0, st>>>(ctx, S, H, w8, w_scale, out);
+    else if (S <= 4)
+        out_project_small<4><<<grid, 256, 0, st>>>(ctx, S, H, w8, w_scale, out);
+    else
+        out_project_small<kSmallS><<<grid, 256, 0, st>>>(ctx, S, H, w8, w_scale, out);
     return cudaGetLastError();
 }
 

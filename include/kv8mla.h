@@ -264,13 +264,15 @@ KV8_API int kv8_quant_rows_scatter(const float *x, int64_t n, const int64_t *dst
  *   bf16 rounds the f32 sum to nearest even) -- the query the decode / selection / prefill calls take.
  * mla_out_project8: out[s][h][v] = sum_{c<512} W[256h + 128 + v][c] * ctx[s][h][c]     (v < 128)
  *   ctx [S][H][512] f32 (a normalised context, e.g. mla_lse_merge8's out); out [S][H][128] f32.
- * Sums in f32 over exactly decoded weights; the block scale is applied per 128-column block.
+ * Sums in f32 over exactly decoded weights; the block scale is applied per 128-column block.  Up to 8
+ * rows run on the CUDA cores (the weights read once); more on the tensor cores (kind::f16: every e4m3
+ * weight is a bf16; f32 activations as bf16 hi + lo pieces).  err_word: optional (KV8_ERR_TIMEOUT).
  * S in [1, KV8_MAX_ROWS]; H in [1, 128]; all buffers 16-byte aligned; outputs must not overlap inputs.
  * --------------------------------------------------------------------------------------------- */
 KV8_API int mla_q_absorb8(const void *q_nope, int q_dtype, int S, int H, const uint8_t *w8, const float *w_scale,
-                          void *q_lat, int out_dtype, void *stream);
+                          void *q_lat, int out_dtype, int *err_word, void *stream);
 KV8_API int mla_out_project8(const float *ctx, int S, int H, const uint8_t *w8, const float *w_scale, float *out,
-                             void *stream);
+                             int *err_word, void *stream);
 
 /* -----------------------------------------------------------------------------------------------
  * dsa_index_topk8 -- the DSA lightning indexer and its top-k ([B1] page, the commit adding
