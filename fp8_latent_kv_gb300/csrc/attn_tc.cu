@@ -868,6 +868,9 @@ __global__ void __launch_bounds__(kPrepBlock) tc_prep_kernel(PrepArgs a) {
     }
 }
 
+}  // namespace
+
+// The driver's tensor-map encoder, looked up once (null if the driver does not provide it).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -881,8 +884,6 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     });
     return fn;
 }
-
-}  // namespace
 
 // Launch the tensor-core kernel.  The grid covers B items x P partitions x the head halves.  Dense
 // rows are loaded as 128-row tiles; selected rows are gathered 4 at a time from a tensor map over all

@@ -23,7 +23,6 @@
 #include "sm100.cuh"
 
 #include <cudaTypedefs.h>
-#include <mutex>
 
 namespace kv8 {
 namespace {
@@ -432,26 +431,12 @@ __global__ void __launch_bounds__(kKThreads) topk_kernel(const float *__restrict
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 index_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        cudaDriverEntryPointQueryResult q;
-        void *p = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
 }  // namespace
 
 cudaError_t launch_index_scores(const void *q, int q_bf16, const float *w, int B, int HI, const uint8_t *k8,
                                 const float *k_scale, int64_t T, int64_t seq_stride_rows, float *scores,
                                 int *err_word, cudaStream_t st) {
-    PFN_cuTensorMapEncodeTiled_v12000 encode = index_map_encoder();
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
     const int64_t rows = (int64_t)(B - 1) * seq_stride_rows + T;
     if (rows > 0x7fffffffLL - kITile) return cudaErrorInvalidValue;  // tensor-map row coordinates are 32-bit

@@ -3,6 +3,8 @@
 
 #include "common.cuh"
 
+#include <cudaTypedefs.h>
+
 namespace kv8 {
 
 // One attention problem set: B batch items (decode: 1; selection: B sequences; prefill: S queries),
@@ -54,10 +56,14 @@ cudaError_t launch_q_absorb_tc(const void *q_nope, int q_bf16, int S, int H, con
                                void *q_lat, int out_bf16, int *err_word, cudaStream_t st);
 cudaError_t launch_out_project_tc(const float *ctx, int S, int H, const uint8_t *w8, const float *w_scale, float *out,
                                   int *err_word, cudaStream_t st);
+// the driver's cuTensorMapEncodeTiled, looked up once; null if unavailable
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 int mixed_partitions(int H, int64_t T);
 cudaError_t launch_attn_mixed(const void *q_nope, const void *q_rope, int q_bf16, int H, const uint8_t *k8,
                               const float *k_scale, const void *k_rope, int64_t T, float sm_scale_log2, int P,
-                              float *ws, cudaStream_t st);
+                              float *ws, void *scratch, int *err_word, cudaStream_t st);
+// staging for the mixed decode's query prep (query images, score factors, row-scale maxima)
+size_t mixed_scratch_bytes(int H, int P);
 cudaError_t launch_copy(void *dst, const void *src, size_t bytes, cudaStream_t st);
 cudaError_t launch_lse_merge(const float *ws, int B, int P, int H, float *out, cudaStream_t st);
 

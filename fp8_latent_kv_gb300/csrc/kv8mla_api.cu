@@ -109,7 +109,9 @@ const char *kv8_strerror(int code) {
 
 int mla_mixed_decode8_workspace_bytes(int H, int64_t T, size_t *bytes) {
     if (H < 1 || H > KV8_MAX_HEADS || T < 1 || T > KV8_MAX_ROWS || !bytes) return KV8_EINVAL;
-    *bytes = decode_partial_bytes(mixed_partitions(H, T), H);
+    // partial sets first (the documented layout), then staging for the query prep
+    const int P = mixed_partitions(H, T);
+    *bytes = decode_partial_bytes(P, H) + mixed_scratch_bytes(H, P);
     return KV8_OK;
 }
 
@@ -123,10 +125,11 @@ int mla_absorb_mixed_decode8(const void *q_nope, const void *q_rope, int q_dtype
         !isfinite(sm_scale) || !aligned(workspace, 16) || !aligned(out, 16))
         return KV8_EINVAL;
     if (ws_bytes < need) return KV8_EWORKSPACE;
-    (void)err_word;  // no device-side condition can arise: the kernel's only waits are __syncthreads
     const int P = mixed_partitions(H, T);
     rc = status(launch_attn_mixed(q_nope, q_rope, q_dtype == KV8_BF16, H, k8, k_scale, k_rope, T, sm_scale * kLog2e, P,
-                                  static_cast<float *>(workspace), (cudaStream_t)stream));
+                                  static_cast<float *>(workspace),
+                                  static_cast<uint8_t *>(workspace) + decode_partial_bytes(P, H), err_word,
+                                  (cudaStream_t)stream));
     if (rc != KV8_OK) return rc;
     return mla_lse_merge8(workspace, 1, P, H, out, stream);
 }

@@ -27,24 +27,6 @@ constexpr int kPT = 128;          // activation rows per tile (MMA M)
 constexpr int kPThreads = 256;
 constexpr uint32_t kKB = 64;      // bf16 elements per 128-byte swizzled row segment (one K block)
 
-// tcgen05.mma kind::f16 with bf16 A and B (both the same type), f32 D in TMEM.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
-    return (1u << 4)                     // D format: f32
-           | (1u << 7) | (1u << 10)      // A, B format: bf16
-           | ((uint32_t)(N >> 3) << 17)  // N / 8
-           | ((uint32_t)(M >> 4) << 24); // M / 16
-}
-
 __device__ __forceinline__ uint32_t bf16_bits(float x) {
     return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x));
 }

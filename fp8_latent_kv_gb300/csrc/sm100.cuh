@@ -1,6 +1,6 @@
 // sm100.cuh -- inline-PTX wrappers for the Blackwell (sm_100 family, here sm_103a) features the
 // tensor-core kernels use: mbarriers with bounded waits, TMA (cp.async.bulk[.tensor]), TMEM
-// allocation, tcgen05.mma (kind::f8f6f4), tcgen05.commit, tcgen05.ld/st, and the shared-memory /
+// allocation, tcgen05.mma (kind::f8f6f4, kind::f16), tcgen05.commit, tcgen05.ld/st, and the shared-memory /
 // instruction descriptors.  Written from the PTX ISA's descriptions of these instructions.
 #pragma once
 
@@ -182,6 +182,16 @@ __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 
+// tcgen05.mma kind::f16 with bf16 A and B (both the same type), f32 D in TMEM.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // The mbarrier receives one arrive once every tcgen05 operation issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -207,6 +217,16 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool a_mn, bool b_mn) {
     return (1u << 4)                              // D format: f32
            | (0u << 7) | (0u << 10)               // A, B format: e4m3
+           | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16)
+           | ((uint32_t)(N >> 3) << 17)           // N / 8
+           | ((uint32_t)(M >> 4) << 24);          // M / 16
+}
+
+// Instruction descriptor for kind::f16 with bf16 A and B and an f32 accumulator (K-major unless
+// a_mn / b_mn).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn = false, bool b_mn = false) {
+    return (1u << 4)                              // D format: f32
+           | (1u << 7) | (1u << 10)               // A, B format: bf16
            | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16)
            | ((uint32_t)(N >> 3) << 17)           // N / 8
            | ((uint32_t)(M >> 4) << 24);          // M / 16

@@ -221,8 +221,11 @@ KV8_API int mla_absorb_decode8_noalloc(const void *q_lat, const void *q_rope, in
  *     out[h] = sum_t softmax_t(score[h]) * [ k_scale[t] * e4m3(k8[t]) , k_rope[t] ]        (512 f32)
  *   q_nope [H][448], q_rope [H][64] of type q_dtype; k8 [T][448] e4m3 (kv8_quant_rows_w, width 448),
  *   k_scale [T] f32, k_rope [T][64] bf16; out [H][512] f32.  H in [1, 128]; T in [1, KV8_MAX_ROWS].
- *   workspace: >= mla_mixed_decode8_workspace_bytes(H, T) (split-T partial sets as for mla_decode8_partial;
- *   merged by mla_lse_merge8 inside the call).  Runs on the CUDA cores (f32 arithmetic).
+ *   workspace: >= mla_mixed_decode8_workspace_bytes(H, T) (split-T partial sets as for mla_decode8_partial,
+ *   merged by mla_lse_merge8 inside the call; then staging for the query prep).  k8 and k_rope 16-byte aligned.  err_word: optional
+ *   (KV8_ERR_TIMEOUT).  Runs on the tensor cores: the no-position product as e4m3 x e4m3 and the RoPE
+ *   product as bf16 x bf16 (an f32 RoPE query as bf16 hi + lo), f32 accumulation; the softmax weights
+ *   enter the value product as e4m3 hi + lo (no-position values) and bf16 (RoPE values).
  * --------------------------------------------------------------------------------------------- */
 KV8_API int mla_mixed_decode8_workspace_bytes(int H, int64_t T, size_t *bytes);
 KV8_API int mla_absorb_mixed_decode8(const void *q_nope, const void *q_rope, int q_dtype, int H, const uint8_t *k8,

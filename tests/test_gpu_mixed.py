@@ -4,7 +4,8 @@ vs the oracle.
 The cache's e4m3 bytes come from the oracle's quantizer (the GPU's width-448 quantizer is checked
 bit-exact separately).  Both sides quantize the query's no-position part the same way (the row
 quantizer), so the comparison is of the attention itself, at the attention tolerance.  Edge cases:
-T = 1 and T around the 64-row tile, H not a multiple of the 32-head block, f32 queries.
+T = 1 and T around the 128-row tile, several tiles per partition, H not a multiple of the 64-head
+half, f32 queries (the RoPE query then enters as bf16 hi + lo).
 """
 import numpy as np
 import pytest
@@ -23,7 +24,7 @@ def _cache(oracle, nope, rope):
         torch.from_numpy(rope).to(DEV).to(torch.bfloat16)
 
 
-def _run(lib, qn, qr, tk8, tks, tkr, bf16, sm=synth.SM_SCALE):
+def _run(lib, qn, qr, tk8, tks, tkr, bf16, sm=synth.SM_SCALE, err=None):
     H, T = qn.shape[0], tk8.shape[0]
     tq = torch.from_numpy(np.ascontiguousarray(qn)).to(DEV)
     tr = torch.from_numpy(np.ascontiguousarray(qr)).to(DEV)
@@ -31,7 +32,7 @@ def _run(lib, qn, qr, tk8, tks, tkr, bf16, sm=synth.SM_SCALE):
         tq, tr = tq.to(torch.bfloat16), tr.to(torch.bfloat16)
     ws = torch.empty(lib.mla_mixed_decode8_workspace_bytes(H, T) // 4, dtype=torch.float32, device=DEV)
     out = torch.empty((H, 512), dtype=torch.float32, device=DEV)
-    lib.mla_absorb_mixed_decode8(tq, tr, tk8, tks, tkr, sm, ws, out)
+    lib.mla_absorb_mixed_decode8(tq, tr, tk8, tks, tkr, sm, ws, out, err_word=err)
     torch.cuda.synchronize()
     return out.cpu().numpy()
 
@@ -50,7 +51,9 @@ def test_quant_rows_width_448_bit_exact(lib, oracle):
 
 
 @pytest.mark.parametrize("T,H,bf16", [(1, 128, True), (63, 5, True), (64, 128, True), (65, 33, False),
-                                      (1000, 128, True), (5000, 16, False)])
+                                      (127, 64, True), (128, 65, True), (129, 128, False), (257, 1, True),
+                                      (1000, 128, True), (5000, 16, False), (40000, 128, True),
+                                      (40000, 97, False)])
 def test_mixed_decode_parity(lib, oracle, T, H, bf16):
     rng = np.random.default_rng(T * 7 + H)
     nope = (rng.standard_normal((T, 448)) * 10.0 ** rng.uniform(-1, 1, (T, 1))).astype(np.float32)
@@ -72,3 +75,17 @@ def test_mixed_decode_workload_sampled_heads(lib, oracle):
     got = _run(lib, qn, qr, tk8, tks, tkr, True)
     heads = list(range(0, w.H, 9))
     parity(got[heads], oracle.attn_mixed_decode(qn[heads], qr[heads], k8, ks, rope, synth.SM_SCALE), "mixed_dec")
+
+
+def test_mixed_decode_error_word_stays_clear(lib, oracle):
+    rng = np.random.default_rng(61)
+    T, H = 3000, 128
+    nope = rng.standard_normal((T, 448)).astype(np.float32)
+    rope = synth.to_bf16_values(rng.standard_normal((T, 64)).astype(np.float32))
+    k8, ks, tk8, tks, tkr = _cache(oracle, nope, rope)
+    q = synth.to_bf16_values(rng.standard_normal((H, 512)).astype(np.float32))
+    qn, qr = np.ascontiguousarray(q[:, :448]), np.ascontiguousarray(q[:, 448:])
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = _run(lib, qn, qr, tk8, tks, tkr, True, err=err)
+    assert int(err.item()) == 0
+    parity(got, oracle.attn_mixed_decode(qn, qr, k8, ks, rope, synth.SM_SCALE), "err word run")
