@@ -656,26 +656,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // and before its accumulators are rescaled
                     if (ok) ok = mbar_wait(&ms.pv_done, (i - 1) & 1, &ms.abort_flag, a.err_word);
                     if (any_alpha) {
-                        // rescale this half's columns of the four context accumulators
+                        // rescale this half's columns of the four context accumulators, two per TMEM round trip
                         tc_fence_after_sync();
 #pragma unroll 1
-                        for (int c = 0; c < 4; ++c) {
-                            const uint32_t ta = tmem + lane_addr + 256u + 64u * c + 32u * hh;
-                            uint32_t o[32];
+                        for (int c2 = 0; c2 < 2; ++c2) {
+                            const uint32_t ta = tmem + lane_addr + 256u + 128u * c2 + 32u * hh;
+                            uint32_t o[64];
                             tmem_ld_32x32b_x16(ta, *reinterpret_cast<uint32_t(*)[16]>(o));
                             tmem_ld_32x32b_x16(ta + 16u, *reinterpret_cast<uint32_t(*)[16]>(o + 16));
+                            tmem_ld_32x32b_x16(ta + 64u, *reinterpret_cast<uint32_t(*)[16]>(o + 32));
+                            tmem_ld_32x32b_x16(ta + 80u, *reinterpret_cast<uint32_t(*)[16]>(o + 48));
                             tmem_wait_ld();
                             const float *al = ms.ph.tile.alpha[hh];
 #pragma unroll
                             for (int j4 = 0; j4 < 8; ++j4) {
                                 const float4 a4 = *reinterpret_cast<const float4 *>(al + 4 * j4);
-                                o[4 * j4 + 0] = __float_as_uint(__uint_as_float(o[4 * j4 + 0]) * a4.x);
-                                o[4 * j4 + 1] = __float_as_uint(__uint_as_float(o[4 * j4 + 1]) * a4.y);
-                                o[4 * j4 + 2] = __float_as_uint(__uint_as_float(o[4 * j4 + 2]) * a4.z);
-                                o[4 * j4 + 3] = __float_as_uint(__uint_as_float(o[4 * j4 + 3]) * a4.w);
+                                const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    o[4 * j4 + u] = __float_as_uint(__uint_as_float(o[4 * j4 + u]) * av[u]);
+                                    o[32 + 4 * j4 + u] = __float_as_uint(__uint_as_float(o[32 + 4 * j4 + u]) * av[u]);
+                                }
                             }
                             tmem_st_32x32b_x16(ta, *reinterpret_cast<const uint32_t(*)[16]>(o));
                             tmem_st_32x32b_x16(ta + 16u, *reinterpret_cast<const uint32_t(*)[16]>(o + 16));
+                            tmem_st_32x32b_x16(ta + 64u, *reinterpret_cast<const uint32_t(*)[16]>(o + 32));
+                            tmem_st_32x32b_x16(ta + 80u, *reinterpret_cast<const uint32_t(*)[16]>(o + 48));
                         }
                         tmem_wait_st();
                     }
