@@ -49,6 +49,13 @@ FLOP_PER_ROW_HEAD = 2 * 1088    # 576-wide score dot + 512-wide context accumula
 L2_FLUSH_BYTES = 256 << 20      # 2x the 129 MB L2
 TC_KERNEL_SOURCES = ["fp8_latent_kv_gb300/csrc/attn_tc.cu", "fp8_latent_kv_gb300/csrc/sm100.cuh"]
 TC_KERNEL = "attn_tc_kernel"
+# the sources each committed traffic summary is tied to (a kernel's .cu and the headers its device code uses)
+IDX_SOURCES = ["fp8_latent_kv_gb300/csrc/indexer.cu", "fp8_latent_kv_gb300/csrc/sm100.cuh",
+               "fp8_latent_kv_gb300/csrc/quant_row.cuh"]
+MIXED_SOURCES = ["fp8_latent_kv_gb300/csrc/attn_mixed.cu", "fp8_latent_kv_gb300/csrc/sm100.cuh",
+                 "fp8_latent_kv_gb300/csrc/quant_row.cuh"]
+PROJ_TC_SOURCES = ["fp8_latent_kv_gb300/csrc/proj8_tc.cu", "fp8_latent_kv_gb300/csrc/sm100.cuh"]
+PROJ_SMALL_SOURCES = ["fp8_latent_kv_gb300/csrc/proj8.cu"]
 MMA_PIECES = 2                  # hi + lo e4m3 pieces of the queries and of the weights: 2 MMAs per product
 
 
@@ -541,7 +548,10 @@ class ProjCase(Case):
         return {"bound": "hbm", "achieved": hbm_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": hbm_gbs / peaks["hbm_gbs"], "peak_source": f"copy bandwidth ({peaks['source']})",
                 "kernel": kern, "events_bracket": self.kernel_calls,
-                "traffic": None, "algorithmic_bytes": self.alg_bytes, "algorithmic_flops": self.flops,
+                # DRAM bytes of one launch of each of the two kernels (one step)
+                "traffic": traffic_per_launch(key, "proj8_small_kernels", PROJ_SMALL_SOURCES) if self.w.S <= 8
+                else traffic_per_launch(key, "proj8_tc_kernels", PROJ_TC_SOURCES),
+                "algorithmic_bytes": self.alg_bytes, "algorithmic_flops": self.flops,
                 "kernel_us": kern_s * 1e6, "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / peaks["hbm_gbs"],
                 "hbm_peak_gbs": peaks["hbm_gbs"], "tflops": tflops,
                 "tensor_frac_of_bf16_peak": tflops / peaks["bf16_tflops"] if self.w.S > 8 else None}
@@ -629,7 +639,7 @@ class IndexerCase(Case):
         return {"bound": "hbm", "achieved": hbm_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": hbm_gbs / peaks["hbm_gbs"], "peak_source": f"copy bandwidth ({peaks['source']})",
                 "kernel": "index_score_kernel + topk_kernel (indexer.cu)", "events_bracket": self.kernel_calls,
-                "traffic": traffic_per_launch(key, "index_score_kernel", ["fp8_latent_kv_gb300/csrc/indexer.cu"]),
+                "traffic": traffic_per_launch(key, "index_score_kernel", IDX_SOURCES),
                 "algorithmic_bytes": self.alg_bytes, "algorithmic_flops": self.flops, "kernel_us": kern_s * 1e6,
                 "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / peaks["hbm_gbs"], "hbm_peak_gbs": peaks["hbm_gbs"],
                 "tflops": tflops, "tensor_frac_of_fp8_peak": tflops / (2.0 * peaks["bf16_tflops"])}
@@ -820,7 +830,7 @@ class MixedDecodeCase(Case):
         return {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
                 "peak_source": f"fp8 = 2 x bf16 burst ({peaks['source']})",
                 "kernel": "attn_mixed_tc_kernel (attn_mixed.cu) + lse_merge_kernel", "events_bracket": self.kernel_calls,
-                "traffic": traffic_per_launch(key, "attn_mixed_tc_kernel", ["fp8_latent_kv_gb300/csrc/attn_mixed.cu"]),
+                "traffic": traffic_per_launch(key, "attn_mixed_tc_kernel", MIXED_SOURCES),
                 "algorithmic_bytes": self.alg_bytes, "algorithmic_flops": self.flops, "kernel_us": kern_s * 1e6,
                 "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / peaks["hbm_gbs"], "hbm_peak_gbs": peaks["hbm_gbs"],
                 "tflops": tflops}
