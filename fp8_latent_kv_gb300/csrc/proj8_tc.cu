@@ -80,16 +80,26 @@ __global__ void __launch_bounds__(kPThreads, 1) q_absorb_tc_kernel(const void *_
         tmem_alloc(&sm.tmem_base, 512);
         tmem_relinquish();
     }
-    // W_UK[h] (e4m3 [128 j][512 c]) -> b[j / 64][c][j % 64] as bf16: item (j, c4) = 4 consecutive c
-    for (int it = tid; it < kNope * (kKL / 4); it += kPThreads) {
-        const int j = it / (kKL / 4), c4 = it - j * (kKL / 4);
-        const uint32_t w = __ldg(reinterpret_cast<const uint32_t *>(w8 + ((int64_t)h * kKvbRows + j) * kKL) + c4);
-        const uint2 v = e4m3x4_to_bf16x4(w);
-        const uint16_t e[4] = {(uint16_t)(v.x & 0xFFFFu), (uint16_t)(v.x >> 16), (uint16_t)(v.y & 0xFFFFu),
-                               (uint16_t)(v.y >> 16)};
+    // W_UK[h] (e4m3 [128 j][512 c]) -> b[j / 64][c][j % 64] as bf16: item (j, c4) = 4 consecutive c;
+    // each thread's loads go out 16 at a time
+    static_assert(kNope * (kKL / 4) % (16 * kPThreads) == 0, "weight items split evenly");
+    for (int base = tid; base < kNope * (kKL / 4); base += 16 * kPThreads) {
+        uint32_t w[16];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-            *reinterpret_cast<uint16_t *>(&sm.b[0][0] + kmajor_off(4 * c4 + u, j, kKL)) = e[u];
+        for (int u = 0; u < 16; ++u) {
+            const int it = base + u * kPThreads, j = it / (kKL / 4), c4 = it - j * (kKL / 4);
+            w[u] = __ldg(reinterpret_cast<const uint32_t *>(w8 + ((int64_t)h * kKvbRows + j) * kKL) + c4);
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int it = base + u * kPThreads, j = it / (kKL / 4), c4 = it - j * (kKL / 4);
+            const uint2 v = e4m3x4_to_bf16x4(w[u]);
+            const uint16_t e[4] = {(uint16_t)(v.x & 0xFFFFu), (uint16_t)(v.x >> 16), (uint16_t)(v.y & 0xFFFFu),
+                                   (uint16_t)(v.y >> 16)};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                *reinterpret_cast<uint16_t *>(&sm.b[0][0] + kmajor_off(4 * c4 + k, j, kKL)) = e[k];
+        }
     }
     const int n_pieces = q_bf16 ? 1 : 2;
     tc_fence_before_sync();
@@ -100,33 +110,51 @@ __global__ void __launch_bounds__(kPThreads, 1) q_absorb_tc_kernel(const void *_
     const int q = warp & 3, col_half = warp >> 2;
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
     const int n_tiles = (S + kPT - 1) / kPT;
+    // A query tile is 128 rows x 16 items of 8 values; thread tid takes items tid + 256 u (u < 8).  The
+    // next tile's values are loaded into registers (raw: 8 bf16 = one uint4, or 8 f32 = two float4) while
+    // the current tile's MMAs and epilogue run.
+    constexpr int kQItems = kPT * (kNope / 8) / kPThreads;  // 8
+    static_assert(kPT * (kNope / 8) == kQItems * kPThreads, "query items split evenly");
+    uint4 raw[kQItems][2];
+    auto load_tile = [&](int ti) {
+#pragma unroll
+        for (int u = 0; u < kQItems; ++u) {
+            const int it = tid + u * kPThreads, r = it / (kNope / 8), j8 = it - r * (kNope / 8);
+            const int srow = ti * kPT + r;
+            raw[u][0] = raw[u][1] = make_uint4(0u, 0u, 0u, 0u);
+            if (ti < n_tiles && srow < S) {
+                const int64_t e = ((int64_t)srow * H + h) * kNope + 8 * j8;
+                if (q_bf16) {
+                    raw[u][0] = __ldg(reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(q_nope) + e));
+                } else {
+                    raw[u][0] = __ldg(reinterpret_cast<const uint4 *>(static_cast<const float *>(q_nope) + e));
+                    raw[u][1] = __ldg(reinterpret_cast<const uint4 *>(static_cast<const float *>(q_nope) + e) + 1);
+                }
+            }
+        }
+    };
+    load_tile(0);
     bool ok = true;
     for (int ti = 0; ti < n_tiles && ok; ++ti) {
         const int s0 = ti * kPT;
         // ---- query tile -> a[piece][K block]: item (row, j8) = 8 consecutive j of one row
-        for (int it = tid; it < kPT * (kNope / 8); it += kPThreads) {
-            const int r = it / (kNope / 8), j8 = it - r * (kNope / 8);
-            float v[8];
-            if (s0 + r < S) {
-                const int64_t e = ((int64_t)(s0 + r) * H + h) * kNope + 8 * j8;
-                if (q_bf16) {
-                    const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(q_nope) + e));
-                    const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u[k]));
-                        v[2 * k] = f.x;
-                        v[2 * k + 1] = f.y;
-                    }
-                } else {
-                    const float4 x0 = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(q_nope) + e));
-                    const float4 x1 = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(q_nope) + e) + 1);
-                    v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
-                    v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
+        for (int u = 0; u < kQItems; ++u) {
+            const int it = tid + u * kPThreads, r = it / (kNope / 8), j8 = it - r * (kNope / 8);
+            float v[8];
+            if (q_bf16) {
+                const uint32_t w4[4] = {raw[u][0].x, raw[u][0].y, raw[u][0].z, raw[u][0].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w4[k]));
+                    v[2 * k] = f.x;
+                    v[2 * k + 1] = f.y;
                 }
             } else {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) v[k] = 0.f;
+                v[0] = __uint_as_float(raw[u][0].x); v[1] = __uint_as_float(raw[u][0].y);
+                v[2] = __uint_as_float(raw[u][0].z); v[3] = __uint_as_float(raw[u][0].w);
+                v[4] = __uint_as_float(raw[u][1].x); v[5] = __uint_as_float(raw[u][1].y);
+                v[6] = __uint_as_float(raw[u][1].z); v[7] = __uint_as_float(raw[u][1].w);
             }
             uint32_t hi[4], lo[4];
 #pragma unroll
@@ -141,6 +169,7 @@ __global__ void __launch_bounds__(kPThreads, 1) q_absorb_tc_kernel(const void *_
             *reinterpret_cast<uint4 *>(&sm.a[0][0][0] + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
             if (n_pieces == 2) *reinterpret_cast<uint4 *>(&sm.a[1][0][0] + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
+        load_tile(ti + 1);  // in flight during this tile's MMAs and epilogue
         fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncthreads();
@@ -165,34 +194,33 @@ __global__ void __launch_bounds__(kPThreads, 1) q_absorb_tc_kernel(const void *_
         tc_fence_after_sync();
         // ---- epilogue: thread (row r, column half) -> 256 outputs, scaled per 128-column block
         const int r = q * 32 + lane, s = s0 + r;
-        for (int c0 = col_half * 256; c0 < col_half * 256 + 256 && ok; c0 += 32) {
-            uint32_t v0[16], v1[16];
-            tmem_ld_32x32b_x16(tmem + lane_addr + (uint32_t)c0, v0);
-            tmem_ld_32x32b_x16(tmem + lane_addr + (uint32_t)c0 + 16u, v1);
+        for (int c0 = col_half * 256; c0 < col_half * 256 + 256 && ok; c0 += 64) {
+            uint32_t v[4][16];  // 64 columns (one scale block), one TMEM round trip
+#pragma unroll
+            for (int g = 0; g < 4; ++g) tmem_ld_32x32b_x16(tmem + lane_addr + (uint32_t)(c0 + 16 * g), v[g]);
             tmem_wait_ld();
             const float sc = __ldg(w_scale + (int64_t)(2 * h) * kNbc + c0 / kBlk);
             if (s < S) {
                 const int64_t o = ((int64_t)s * H + h) * kKL + c0;
                 if (out_bf16) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        pk[k] = bf16_bits(__uint_as_float(v0[2 * k]) * sc) | (bf16_bits(__uint_as_float(v0[2 * k + 1]) * sc) << 16);
-                        pk[8 + k] = bf16_bits(__uint_as_float(v1[2 * k]) * sc) | (bf16_bits(__uint_as_float(v1[2 * k + 1]) * sc) << 16);
-                    }
                     uint4 *d = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(q_lat) + o);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) d[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                    for (int g = 0; g < 4; ++g) {
+                        uint32_t pk[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            pk[k] = bf16_bits(__uint_as_float(v[g][2 * k]) * sc) | (bf16_bits(__uint_as_float(v[g][2 * k + 1]) * sc) << 16);
+                        d[2 * g] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        d[2 * g + 1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    }
                 } else {
                     float4 *d = reinterpret_cast<float4 *>(static_cast<float *>(q_lat) + o);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        d[k] = make_float4(__uint_as_float(v0[4 * k]) * sc, __uint_as_float(v0[4 * k + 1]) * sc,
-                                           __uint_as_float(v0[4 * k + 2]) * sc, __uint_as_float(v0[4 * k + 3]) * sc);
+                    for (int g = 0; g < 4; ++g)
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        d[4 + k] = make_float4(__uint_as_float(v1[4 * k]) * sc, __uint_as_float(v1[4 * k + 1]) * sc,
-                                               __uint_as_float(v1[4 * k + 2]) * sc, __uint_as_float(v1[4 * k + 3]) * sc);
+                        for (int k = 0; k < 4; ++k)
+                            d[4 * g + k] = make_float4(__uint_as_float(v[g][4 * k]) * sc, __uint_as_float(v[g][4 * k + 1]) * sc,
+                                                       __uint_as_float(v[g][4 * k + 2]) * sc, __uint_as_float(v[g][4 * k + 3]) * sc);
                 }
             }
         }
@@ -236,12 +264,22 @@ __global__ void __launch_bounds__(kPThreads, 1) out_project_tc_kernel(const floa
         tmem_alloc(&sm.tmem_base, 512);
         tmem_relinquish();
     }
-    // W_UV[h] (e4m3 [128 v][512 c]) -> b[c / 64][v][c % 64] as bf16: item (v, c8) = 8 consecutive c
-    for (int it = tid; it < kVH * (kKL / 8); it += kPThreads) {
-        const int v = it / (kKL / 8), c8 = it - v * (kKL / 8);
-        const uint2 w = __ldg(reinterpret_cast<const uint2 *>(w8 + ((int64_t)h * kKvbRows + kNope + v) * kKL) + c8);
-        const uint2 lo = e4m3x4_to_bf16x4(w.x), hi = e4m3x4_to_bf16x4(w.y);
-        *reinterpret_cast<uint4 *>(&sm.b[0][0] + kmajor_off(v, 8 * c8, kVH)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    // W_UV[h] (e4m3 [128 v][512 c]) -> b[c / 64][v][c % 64] as bf16: item (v, c8) = 8 consecutive c; each
+    // thread's loads go out 16 at a time
+    static_assert(kVH * (kKL / 8) % (16 * kPThreads) == 0, "weight items split evenly");
+    for (int base = tid; base < kVH * (kKL / 8); base += 16 * kPThreads) {
+        uint2 w[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int it = base + u * kPThreads, v = it / (kKL / 8), c8 = it - v * (kKL / 8);
+            w[u] = __ldg(reinterpret_cast<const uint2 *>(w8 + ((int64_t)h * kKvbRows + kNope + v) * kKL) + c8);
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int it = base + u * kPThreads, v = it / (kKL / 8), c8 = it - v * (kKL / 8);
+            const uint2 lo = e4m3x4_to_bf16x4(w[u].x), hi = e4m3x4_to_bf16x4(w[u].y);
+            *reinterpret_cast<uint4 *>(&sm.b[0][0] + kmajor_off(v, 8 * c8, kVH)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -254,24 +292,37 @@ __global__ void __launch_bounds__(kPThreads, 1) out_project_tc_kernel(const floa
     float sc[kNbc];
 #pragma unroll
     for (int k = 0; k < kNbc; ++k) sc[k] = __ldg(w_scale + (int64_t)(2 * h + 1) * kNbc + k);
+    // A stage is one scale block (128 columns) of a 128-row context tile: 128 rows x 16 items of 8 f32;
+    // thread tid takes items tid + 256 u (u < 8).  The next stage's values are loaded into registers
+    // while the current stage's MMAs (and, after a tile's last block, its epilogue) run.
+    constexpr int kOItems = kPT * (kBlk / 8) / kPThreads;  // 8
+    static_assert(kPT * (kBlk / 8) == kOItems * kPThreads, "context items split evenly");
+    float4 raw[kOItems][2];
+    auto load_stage = [&](int ti, int cb) {
+#pragma unroll
+        for (int u = 0; u < kOItems; ++u) {
+            const int it = tid + u * kPThreads, r = it / (kBlk / 8), c8 = it - r * (kBlk / 8);
+            const int srow = ti * kPT + r;
+            raw[u][0] = raw[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (ti < n_tiles && srow < S) {
+                const float4 *src = reinterpret_cast<const float4 *>(ctx + ((int64_t)srow * H + h) * kKL + cb * kBlk + 8 * c8);
+                raw[u][0] = __ldg(src);
+                raw[u][1] = __ldg(src + 1);
+            }
+        }
+    };
+    load_stage(0, 0);
     bool ok = true;
     uint32_t phase = 0;
     for (int ti = 0; ti < n_tiles && ok; ++ti) {
         const int s0 = ti * kPT;
         for (int cb = 0; cb < kNbc && ok; ++cb) {
             // ---- context columns 128cb.. of the tile -> bf16 hi + lo: item (row, c8)
-            for (int it = tid; it < kPT * (kBlk / 8); it += kPThreads) {
-                const int r = it / (kBlk / 8), c8 = it - r * (kBlk / 8);
-                float v[8];
-                if (s0 + r < S) {
-                    const float4 *src = reinterpret_cast<const float4 *>(ctx + ((int64_t)(s0 + r) * H + h) * kKL + cb * kBlk + 8 * c8);
-                    const float4 x0 = __ldg(src), x1 = __ldg(src + 1);
-                    v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
-                    v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
-                } else {
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) v[k] = 0.f;
-                }
+            for (int u = 0; u < kOItems; ++u) {
+                const int it = tid + u * kPThreads, r = it / (kBlk / 8), c8 = it - r * (kBlk / 8);
+                const float v[8] = {raw[u][0].x, raw[u][0].y, raw[u][0].z, raw[u][0].w,
+                                    raw[u][1].x, raw[u][1].y, raw[u][1].z, raw[u][1].w};
                 uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
@@ -285,6 +336,10 @@ __global__ void __launch_bounds__(kPThreads, 1) out_project_tc_kernel(const floa
                 *reinterpret_cast<uint4 *>(&sm.a[0][0][0] + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                 *reinterpret_cast<uint4 *>(&sm.a[1][0][0] + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
+            if (cb + 1 < kNbc)
+                load_stage(ti, cb + 1);
+            else
+                load_stage(ti + 1, 0);
             fence_proxy_async_smem();
             tc_fence_before_sync();
             __syncthreads();
@@ -313,14 +368,14 @@ __global__ void __launch_bounds__(kPThreads, 1) out_project_tc_kernel(const floa
             float accv[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k) accv[k] = 0.f;
+            uint32_t d[kNbc][16];  // the four scale blocks' accumulators, one TMEM round trip
 #pragma unroll
-            for (int cb = 0; cb < kNbc; ++cb) {
-                uint32_t d[16];
-                tmem_ld_32x32b_x16(tmem + lane_addr + (uint32_t)(cb * 128 + v0), d);
-                tmem_wait_ld();
+            for (int cb = 0; cb < kNbc; ++cb) tmem_ld_32x32b_x16(tmem + lane_addr + (uint32_t)(cb * 128 + v0), d[cb]);
+            tmem_wait_ld();
 #pragma unroll
-                for (int k = 0; k < 16; ++k) accv[k] = fmaf(sc[cb], __uint_as_float(d[k]), accv[k]);
-            }
+            for (int cb = 0; cb < kNbc; ++cb)
+#pragma unroll
+                for (int k = 0; k < 16; ++k) accv[k] = fmaf(sc[cb], __uint_as_float(d[cb][k]), accv[k]);
             if (s < S) {
                 float4 *dst = reinterpret_cast<float4 *>(out + ((int64_t)s * H + h) * kVH + v0);
 #pragma unroll
