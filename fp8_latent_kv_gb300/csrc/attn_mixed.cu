@@ -589,21 +589,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < n_acc; ++c) {
                     const float mul = c < 4 ? out_mul : 1.f;
                     const int dd = c < 4 ? 128 * c + r : kMxNope + r;
-#pragma unroll 1
-                    for (int k = 0; k < 2; ++k) {
-                        uint32_t o[16];
-                        if (n_tiles > 0) {
-                            tmem_ld_32x32b_x16(tmem + lane_addr + kColO + 64u * c + 32u * hh + 16u * k, o);
-                            tmem_wait_ld();
-                        } else {
+                    uint32_t o[32];  // this half's 32 heads of accumulator c, one TMEM round trip
+                    if (n_tiles > 0) {
+                        tmem_ld_32x32b_x16(tmem + lane_addr + kColO + 64u * c + 32u * hh, *reinterpret_cast<uint32_t(*)[16]>(o));
+                        tmem_ld_32x32b_x16(tmem + lane_addr + kColO + 64u * c + 32u * hh + 16u,
+                                           *reinterpret_cast<uint32_t(*)[16]>(o + 16));
+                        tmem_wait_ld();
+                    } else {
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) o[j] = 0u;
-                        }
+                        for (int j = 0; j < 32; ++j) o[j] = 0u;
+                    }
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int hg = half * kHeads + 32 * hh + 16 * k + j;
-                            if (hg < a.H) pv.cl[((int64_t)part * a.H + hg) * kKL + dd] = __uint_as_float(o[j]) * mul;
-                        }
+                    for (int j = 0; j < 32; ++j) {
+                        const int hg = half * kHeads + 32 * hh + j;
+                        if (hg < a.H) pv.cl[((int64_t)part * a.H + hg) * kKL + dd] = __uint_as_float(o[j]) * mul;
                     }
                 }
                 if (q == 0) {
