@@ -726,27 +726,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float out_mul = ms.out_mul;
                 const int hbase = half * kHeadsPerCta + 32 * hh;
                 PartialView pv(a.ws, a.B, a.P, a.H);
-                // the 8 column chunks of this thread's row (16 heads each)
+                // this thread's row (dims 128c + r) of the four accumulators, 32 heads per TMEM round trip;
+                // partial sets (relative to the running max) or the normalised output
+                float *const dst = a.ws ? pv.cl + ((int64_t)b * a.P + part) * a.H * kKL : a.out + (int64_t)b * a.H * kKL;
 #pragma unroll 1
-                for (int ch = 0; ch < 8; ++ch) {
-                    uint32_t o[16];
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t o[32];
                     if (n_tiles > 0) {
-                        tmem_ld_32x32b_x16(tmem + lane_addr + 256u + 64u * (ch >> 1) + 32u * hh + 16u * (ch & 1), o);
+                        const uint32_t ta = tmem + lane_addr + 256u + 64u * c + 32u * hh;
+                        tmem_ld_32x32b_x16(ta, *reinterpret_cast<uint32_t(*)[16]>(o));
+                        tmem_ld_32x32b_x16(ta + 16u, *reinterpret_cast<uint32_t(*)[16]>(o + 16));
                         tmem_wait_ld();
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) o[j] = 0u;
+                        for (int j = 0; j < 32; ++j) o[j] = 0u;
                     }
-                    const int dd = 128 * (ch >> 1) + r;
+                    float *const col = dst + 128 * c + r;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int hl = 32 * hh + 16 * (ch & 1) + j;  // head within the CTA
+                    for (int j = 0; j < 32; ++j) {
+                        const int hl = 32 * hh + j;  // head within the CTA
                         const int hg = half * kHeadsPerCta + hl;
-                        if (hg >= a.H) continue;
-                        if (a.ws)
-                            pv.cl[(((int64_t)b * a.P + part) * a.H + hg) * kKL + dd] = __uint_as_float(o[j]) * out_mul;
-                        else
-                            a.out[((int64_t)b * a.H + hg) * kKL + dd] = __uint_as_float(o[j]) * ms.ph.fin.zinv[hl];
+                        if (hg < a.H) col[(int64_t)hg * kKL] = __uint_as_float(o[j]) * (a.ws ? out_mul : ms.ph.fin.zinv[hl]);
                     }
                 }
                 if (a.ws && q == 0) {
