@@ -544,16 +544,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 if (ok) ok = mbar_wait(&ms.s_full[bb], (i >> 1) & 1, &ms.abort_flag, a.err_word);
                 tc_fence_after_sync();
-                float sc_[32];  // S = hi piece + lo piece
-#pragma unroll
-                for (int k2 = 0; k2 < 2; ++k2) {
-                    uint32_t shi[16], slo[16];
-                    const uint32_t ta = tmem + lane_addr + (uint32_t)bb * 128u + 32u * hh + 16u * k2;
-                    tmem_ld_32x32b_x16(ta, shi);
-                    tmem_ld_32x32b_x16(ta + 64u, slo);
+                float sc_[32];  // S = hi piece + lo piece, one TMEM round trip
+                {
+                    uint32_t shi[2][16], slo[2][16];
+                    const uint32_t ta = tmem + lane_addr + (uint32_t)bb * 128u + 32u * hh;
+                    tmem_ld_32x32b_x16(ta, shi[0]);
+                    tmem_ld_32x32b_x16(ta + 16u, shi[1]);
+                    tmem_ld_32x32b_x16(ta + 64u, slo[0]);
+                    tmem_ld_32x32b_x16(ta + 80u, slo[1]);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) sc_[16 * k2 + j] = __uint_as_float(shi[j]) + __uint_as_float(slo[j]);
+                    for (int j = 0; j < 32; ++j) sc_[j] = __uint_as_float(shi[j >> 4][j & 15]) + __uint_as_float(slo[j >> 4][j & 15]);
                 }
                 tc_fence_before_sync();
                 mbar_arrive(&ms.s_free[bb]);
