@@ -122,48 +122,6 @@ struct MxArgs {
     const float *smax;
 };
 
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-
-__device__ __forceinline__ void named_sync(int id, int count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-// Named barrier over `count` threads that also ORs a predicate across them.
-__device__ __forceinline__ bool bar_red_or(int id, int count, bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %1, 0;\n\t"
-        "bar.red.or.pred po, %2, %3, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)v), "r"(id), "r"(count)
-        : "memory");
-    return r != 0;
-}
-
-// 2^x by the hardware approximation (MUFU.EX2; subnormal results flush to 0, 2^-inf = 0)
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// Split two weights into e4m3 hi + lo pieces through f16x2: w is first rounded to f16 (11 bits, finer
-// than the 8 bits hi + lo keep), then hi = e4m3(w), lo = e4m3(w - hi) with the residual exact in f16.
-__device__ __forceinline__ void split_pair_h(float a, float b, uint32_t &hi, uint32_t &lo) {
-    uint32_t w16, h16, r16;
-    uint16_t h8, l8;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(w16) : "f"(b), "f"(a));
-    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(h8) : "r"(w16));
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h16) : "h"(h8));
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r16) : "r"(w16), "r"(h16));
-    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l8) : "r"(r16));
-    hi = h8;
-    lo = l8;
-}
-
 __device__ __forceinline__ uint32_t bf16x2_bits(float a, float b) {  // a in the low half
     const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<const uint32_t *>(&v);

@@ -114,13 +114,6 @@ struct TcArgs {
     const float *smax;
 };
 
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-
-__device__ __forceinline__ void named_sync(int id, int count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 // e4m3 pair encode (RNE, saturating): returns byte(a) | byte(b) << 8.
 __device__ __forceinline__ uint32_t enc_pair(float a, float b) {
     uint16_t v;
@@ -139,41 +132,6 @@ __device__ __forceinline__ void split_pair(float a, float b, uint32_t &hi, uint3
     hi = enc_pair(a, b);
     const float2 h = dec_pair(hi);
     lo = enc_pair(a - h.x, b - h.y);
-}
-
-// The same split through f16x2 (5 instructions per pair): w is first rounded to f16 (11 bits, finer
-// than the 8 bits hi + lo keep), then hi = e4m3(w), lo = e4m3(w - hi) with the residual exact in f16.
-__device__ __forceinline__ void split_pair_h(float a, float b, uint32_t &hi, uint32_t &lo) {
-    uint32_t w16, h16, r16;
-    uint16_t h8, l8;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(w16) : "f"(b), "f"(a));
-    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(h8) : "r"(w16));
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h16) : "h"(h8));
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r16) : "r"(w16), "r"(h16));
-    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l8) : "r"(r16));
-    hi = h8;
-    lo = l8;
-}
-
-// Named barrier over `count` threads that also ORs a predicate across them.
-__device__ __forceinline__ bool bar_red_or(int id, int count, bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %1, 0;\n\t"
-        "bar.red.or.pred po, %2, %3, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)v), "r"(id), "r"(count)
-        : "memory");
-    return r != 0;
-}
-
-// 2^x by the hardware approximation (MUFU.EX2; subnormal results flush to 0, 2^-inf = 0)
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
 }
 
 // 10 warps: a sub-partition holding 3 warps caps a thread at 168 registers (16K registers each).

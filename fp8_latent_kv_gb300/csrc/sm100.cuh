@@ -1,7 +1,8 @@
 // sm100.cuh -- inline-PTX wrappers for the Blackwell (sm_100 family, here sm_103a) features the
 // tensor-core kernels use: mbarriers with bounded waits, TMA (cp.async.bulk[.tensor]), TMEM
-// allocation, tcgen05.mma (kind::f8f6f4, kind::f16), tcgen05.commit, tcgen05.ld/st, and the shared-memory /
-// instruction descriptors.  Written from the PTX ISA's descriptions of these instructions.
+// allocation, tcgen05.mma (kind::f8f6f4, kind::f16), tcgen05.commit, tcgen05.ld/st, the shared-memory /
+// instruction descriptors, named barriers and programmatic-launch controls, and the softmax's ex2 and
+// e4m3 hi/lo weight split.  Written from the PTX ISA's descriptions of these instructions.
 #pragma once
 
 #include <cuda.h>
@@ -240,6 +241,52 @@ __host__ __device__ constexpr uint32_t sw128_offset(uint32_t row, uint32_t byte)
 }
 __host__ __device__ constexpr uint32_t sw64_offset(uint32_t row, uint32_t byte) {
     return row * 64u + ((((byte >> 4) ^ ((row >> 1) & 3u)) & 3u) << 4) + (byte & 15u);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Named barriers, programmatic dependent launch, and the softmax's arithmetic helpers
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ void named_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Named barrier over `count` threads that also ORs a predicate across them.
+__device__ __forceinline__ bool bar_red_or(int id, int count, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+// 2^x by the hardware approximation (MUFU.EX2; subnormal results flush to 0, 2^-inf = 0)
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Split two softmax weights into e4m3 hi + lo pieces through f16x2 (5 instructions per pair): w is first
+// rounded to f16 (11 bits, finer than the 8 bits hi + lo keep), then hi = e4m3(w), lo = e4m3(w - hi) with
+// the residual exact in f16.
+__device__ __forceinline__ void split_pair_h(float a, float b, uint32_t &hi, uint32_t &lo) {
+    uint32_t w16, h16, r16;
+    uint16_t h8, l8;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(w16) : "f"(b), "f"(a));
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(h8) : "r"(w16));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h16) : "h"(h8));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r16) : "r"(w16), "r"(h16));
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l8) : "r"(r16));
+    hi = h8;
+    lo = l8;
 }
 
 }  // namespace sm100
