@@ -33,7 +33,7 @@ constexpr int kIdxD = KV8_IDX_D;  // 128 bytes per key row and per query head
 constexpr int kITile = 128;       // key rows per tile (MMA M)
 constexpr int kIStages = 12;
 constexpr int kIAcc = 4;          // TMEM accumulator buffers
-constexpr int kIThreads = 192;    // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kIThreads = 320;    // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue (two groups of four)
 constexpr uint32_t kIStageBytes = kITile * kIdxD;  // 16 KB
 
 struct IdxSmem {
@@ -57,10 +57,6 @@ struct IdxArgs {
     int *err_word;
 };
 
-__device__ __forceinline__ void named_barrier_sync(int id, int count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 __global__ void __launch_bounds__(kIThreads, 1) index_score_kernel(const __grid_constant__ CUtensorMap map_k, IdxArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     IdxSmem &sm = *reinterpret_cast<IdxSmem *>(smem);
@@ -76,14 +72,14 @@ __global__ void __launch_bounds__(kIThreads, 1) index_score_kernel(const __grid_
     const int HI = a.HI;
     const int64_t row_base = (int64_t)b * a.seq_stride_rows;
 
-    // The epilogue warps load their query head rows and weights first, before any key tile is
-    // requested: issued behind the key stream they would wait for it.  Lane j holds the weight of the
+    // The first epilogue group's warps load the query head rows and weights first, before any key tile
+    // is requested: issued behind the key stream they would wait for it.  Lane j holds the weight of the
     // warp's j-th head row; lane l holds elements 4l..4l+3 of each row.
     constexpr int kRowsPerWarp = KV8_MAX_IDX_HEADS / 4;
     static_assert(kRowsPerWarp <= 32, "one head weight per lane");
     float4 v[kRowsPerWarp];
     float w_lane = 0.f;
-    if (warp >= 2) {
+    if (warp >= 2 && warp < 6) {
         const int hw = warp - 2 + 4 * lane;
         if (lane < kRowsPerWarp && hw < a.HI) w_lane = __ldg(a.w + (int64_t)b * a.HI + hw);
 #pragma unroll
@@ -117,7 +113,7 @@ __global__ void __launch_bounds__(kIThreads, 1) index_score_kernel(const __grid_
             mbar_init(&sm.dempty[k], 128);
         }
         mbar_init(&sm.final_bar, 1);
-        mbar_init(&sm.qready, 128);  // the four epilogue warps have written the query image
+        mbar_init(&sm.qready, 128);  // the first epilogue group has written the query image and weights
         sm.abort_flag = 0;
         fence_barrier_init();
     }
@@ -176,9 +172,13 @@ __global__ void __launch_bounds__(kIThreads, 1) index_score_kernel(const __grid_
         __syncwarp();
     } else {
         // ================================ epilogue ================================
-        // first the query image (its rows were loaded at the top of the kernel): warp w quantizes head
-        // rows w-2, w+2, ... (lane l takes elements 4l..4l+3) with the row quantizer's f32 steps
-        {
+        // Two groups of four warps take alternate tiles (group g: tiles g, g + 2, ...; its accumulators
+        // are buffers g and g + 2), so one group reads back a tile while the other waits for the next.
+        // First the query image (its rows were loaded at the top of the kernel): warp w of the first group
+        // quantizes head rows w-2, w+2, ... (lane l takes elements 4l..4l+3) with the row quantizer's f32
+        // steps; the second group waits for it.
+        const int grp = (warp - 2) >> 2;
+        if (grp == 0) {
 #pragma unroll
             for (int j = 0; j < kRowsPerWarp; ++j) {
                 const int h = warp - 2 + 4 * j;
@@ -196,23 +196,23 @@ __global__ void __launch_bounds__(kIThreads, 1) index_score_kernel(const __grid_
                 if (lane == 0) sm.wq[h] = wj * qs;
             }
             fence_proxy_async_smem();  // the MMAs read the image through the async proxy
-            named_barrier_sync(1, 128);  // wq complete for every epilogue thread
+            named_sync(1, 128);  // wq complete for this group's threads
             mbar_arrive(&sm.qready);
         }
+        bool ok = grp == 0 || n_tiles <= 1 || mbar_wait(&sm.qready, 0, &sm.abort_flag, a.err_word);
         const int q = warp & 3;  // TMEM lane quadrant
         const int r = q * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-        bool ok = true;
         // the row's key scale, loaded one tile ahead so its latency hides behind the previous tile
         auto kscale = [&](int i) -> float {
             const int64_t t = (i0 + i) * kITile + r;
             return (i < n_tiles && t < a.T) ? __ldg(a.k_scale + row_base + t) : 0.f;
         };
-        float ks_next = kscale(0);
-        for (int i = 0; i < n_tiles && ok; ++i) {
+        float ks_next = kscale(grp);
+        for (int i = grp; i < n_tiles && ok; i += 2) {
             const int buf = i % kIAcc;
             const float ks = ks_next;
-            ks_next = kscale(i + 1);
+            ks_next = kscale(i + 2);
             ok = mbar_wait(&sm.dfull[buf], (i / kIAcc) & 1, &sm.abort_flag, a.err_word);
             if (!ok) break;
             tc_fence_after_sync();
