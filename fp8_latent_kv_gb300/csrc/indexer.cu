@@ -252,7 +252,8 @@ __global__ void __launch_bounds__(kIThreads, 1) index_score_kernel(const __grid_
 
 // ------------------------------------------------------------------------------------------------
 // top-k: C CTAs per query (a cooperative launch: all CTAs resident), CTA c owning positions
-// [c*T/C, (c+1)*T/C).  Each radix pass: a warp-aggregated shared histogram of the CTA's candidates,
+// [c*T/C, (c+1)*T/C).  Each radix pass: a shared histogram of the CTA's candidates (plain shared atomics:
+// grouping equal bins with __match_any_sync first was slower),
 // added once into the query's global histogram; a barrier of the query's C CTAs; every CTA then finds
 // the pass's bin from the global histogram.  The final pass counts keys above / equal to the k-th key
 // per CTA, and after a last barrier each CTA writes its selected positions at their global offsets.
@@ -328,7 +329,7 @@ __global__ void __launch_bounds__(kKThreads) topk_kernel(const float *__restrict
     __shared__ uint32_t sh_bin, sh_need;
     __shared__ int abort_sh;
     __shared__ uint32_t keys_sh[kKCache];
-    const int tid = threadIdx.x, lane = tid & 31;
+    const int tid = threadIdx.x;
     const int b = blockIdx.x / C, c = blockIdx.x - b * C;
     const float *s = scores + (int64_t)b * T;
     int32_t *out = idx + (int64_t)b * NS;
@@ -356,10 +357,7 @@ __global__ void __launch_bounds__(kKThreads) topk_kernel(const float *__restrict
             const bool in = t < c1;
             const uint32_t key = in ? key_at(t) : 0u;
             const bool cand = in && (key & mask) == prefix;
-            const uint32_t bin = cand ? (key >> shift) & (nb - 1) : 0xFFFFFFFFu;
-            // lanes with the same bin add once (the leader adds the group's count)
-            const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-            if (cand && (__ffs(peers) - 1) == lane) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+            if (cand) atomicAdd(&hist[(key >> shift) & (nb - 1)], 1u);
         }
         __syncthreads();
         for (int i = tid; i < (int)nb; i += kKThreads)
