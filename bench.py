@@ -477,9 +477,6 @@ class PrefillCase(Case):
         return (time.perf_counter() - t0) * self._scale
 
 
-SIMT_F32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # 152 SMs x 128 f32 lanes x FMA x 2070 MHz = 80.5
-
-
 class ProjCase(Case):
     """The absorb projections through an fmt=8 kv_b: q_nope -> q_lat (bf16, the attention's query) and a
     context -> the head outputs, both on one stream.  A decode step (S = 1) reads every weight byte once

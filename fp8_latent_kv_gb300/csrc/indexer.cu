@@ -252,10 +252,10 @@ __global__ void __launch_bounds__(kIThreads, 1) index_score_kernel(const __grid_
 
 // ------------------------------------------------------------------------------------------------
 // top-k: C CTAs per query (a cooperative launch: all CTAs resident), CTA c owning positions
-// [c*T/C, (c+1)*T/C).  Each radix pass: a shared histogram of the CTA's candidates (plain shared atomics:
-// grouping equal bins with __match_any_sync first was slower),
-// added once into the query's global histogram; a barrier of the query's C CTAs; every CTA then finds
-// the pass's bin from the global histogram.  The final pass counts keys above / equal to the k-th key
+// [c*T/C, (c+1)*T/C).  Each radix pass: a shared histogram of the CTA's candidates (plain shared
+// atomics; grouping equal bins with __match_any_sync first was slower), added once into the query's
+// global histogram; a barrier of the query's C CTAs; every CTA then finds the pass's bin from the global
+// histogram.  The final pass counts keys above / equal to the k-th key
 // per CTA, and after a last barrier each CTA writes its selected positions at their global offsets.
 // ------------------------------------------------------------------------------------------------
 constexpr int kKThreads = 512;
