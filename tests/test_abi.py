@@ -118,3 +118,83 @@ def test_validation_rejects_before_launch(lib):
     assert lib.kv8_quant_rows(None, 0, None, None, None) == kv.KV8_OK  # nothing to do
     assert lib.kv8_encode_e4m3(mis, 5, fake, None) == EINVAL
     assert lib.mla_lse_merge8(fake, 1, 0, 16, fake, None) == EINVAL
+
+
+def test_validation_of_the_later_calls(lib):
+    """Batched, mixed-cache, projection, indexer, scatter and copy calls reject bad scalars, alignment and
+    workspace before any CUDA call."""
+    fake = 0x100000
+    mis4, mis2 = fake + 4, fake + 2  # 4-byte but not 8/16-byte aligned; 2-byte aligned
+    EINVAL, EWS, OK = kv.KV8_EINVAL, kv.KV8_EWORKSPACE, kv.KV8_OK
+    BF, F32 = kv.KV8_BF16, kv.KV8_F32
+    sz = ctypes.c_size_t(0)
+    # quantizers
+    assert lib.kv8_quant_rows_w(fake, 3, 100, fake, fake, None) == EINVAL      # unsupported width
+    assert lib.kv8_quant_rows_w(fake, -1, 128, fake, fake, None) == EINVAL
+    assert lib.kv8_quant_rows_w(None, 0, 448, None, None, None) == OK         # nothing to do
+    assert lib.kv8_quant_rows_w(mis4, 3, 128, fake, fake, None) == EINVAL
+    assert lib.kv8_quant_rows_scatter(fake, -1, fake, fake, fake, 10, None, None) == EINVAL
+    assert lib.kv8_quant_rows_scatter(fake, 2, fake, fake, fake, -1, None, None) == EINVAL
+    assert lib.kv8_quant_rows_scatter(None, 0, None, None, None, 10, None, None) == OK
+    assert lib.kv8_quant_rows_scatter(fake, 2, mis4, fake, fake, 10, None, None) == EINVAL  # int64 rows need 8 B
+    # batched decode
+    assert lib.mla_batch_decode8_workspace_bytes(0, 16, 100, ctypes.addressof(sz)) == EINVAL
+    assert lib.mla_batch_decode8_workspace_bytes(2, 129, 100, ctypes.addressof(sz)) == EINVAL
+    assert lib.mla_batch_decode8_workspace_bytes(2, 16, 0, ctypes.addressof(sz)) == EINVAL
+    assert lib.mla_batch_decode8_workspace_bytes(2, 16, 100, None) == EINVAL
+
+    def bat(**kw):
+        a = dict(ql=fake, qr=fake, dt=BF, B=2, H=16, kv8=fake, sc=fake, T=100, stride=100, lens=fake, sm=0.07,
+                 ws=fake, wsb=1 << 30, err=None, out=fake)
+        a.update(kw)
+        return lib.mla_absorb_batch_decode8(a["ql"], a["qr"], a["dt"], a["B"], a["H"], a["kv8"], a["sc"], a["T"],
+                                            a["stride"], a["lens"], a["sm"], a["ws"], a["wsb"], a["err"], a["out"],
+                                            None)
+    assert bat(stride=99) == EINVAL       # caches of two sequences would overlap
+    assert bat(lens=mis2) == EINVAL
+    assert bat(dt=7) == EINVAL
+    assert bat(sm=float("nan")) == EINVAL
+    assert bat(wsb=64) == EWS
+    # mixed-precision cache
+    assert lib.mla_mixed_decode8_workspace_bytes(0, 100, ctypes.addressof(sz)) == EINVAL
+    assert lib.mla_mixed_decode8_workspace_bytes(16, 0, ctypes.addressof(sz)) == EINVAL
+
+    def mix(**kw):
+        a = dict(qn=fake, qr=fake, dt=BF, H=16, k8=fake, ks=fake, kr=fake, T=100, sm=0.07, ws=fake, wsb=1 << 30,
+                 err=None, out=fake)
+        a.update(kw)
+        return lib.mla_absorb_mixed_decode8(a["qn"], a["qr"], a["dt"], a["H"], a["k8"], a["ks"], a["kr"], a["T"],
+                                            a["sm"], a["ws"], a["wsb"], a["err"], a["out"], None)
+    assert mix(k8=mis4) == EINVAL
+    assert mix(kr=mis4) == EINVAL
+    assert mix(H=129) == EINVAL
+    assert mix(sm=float("inf")) == EINVAL
+    assert mix(wsb=64) == EWS
+    # absorb projections
+    assert lib.mla_q_absorb8(fake, BF, 0, 16, fake, fake, fake, BF, None, None) == EINVAL
+    assert lib.mla_q_absorb8(fake, BF, 4, 129, fake, fake, fake, BF, None, None) == EINVAL
+    assert lib.mla_q_absorb8(fake, BF, 4, 16, fake, fake, fake, 7, None, None) == EINVAL
+    assert lib.mla_q_absorb8(fake, BF, 4, 16, fake, fake, mis4, F32, None, None) == EINVAL
+    assert lib.mla_out_project8(fake, 0, 16, fake, fake, fake, None, None) == EINVAL
+    assert lib.mla_out_project8(fake, 4, 16, fake, fake, mis4, None, None) == EINVAL
+    # DSA indexer
+    assert lib.dsa_index_workspace_bytes(0, ctypes.addressof(sz)) == EINVAL
+
+    def idx(**kw):
+        a = dict(q=fake, dt=BF, w=fake, B=2, HI=64, k8=fake, ks=fake, T=1000, stride=1000, NS=64, ws=fake,
+                 wsb=1 << 30, sc=fake, idx=fake)
+        a.update(kw)
+        return lib.dsa_index_topk8(a["q"], a["dt"], a["w"], a["B"], a["HI"], a["k8"], a["ks"], a["T"], a["stride"],
+                                   a["NS"], a["ws"], a["wsb"], a["sc"], a["idx"], None, None)
+    assert idx(HI=8) == EINVAL            # fewer than 16 heads
+    assert idx(HI=40) == EINVAL           # not a multiple of 16
+    assert idx(NS=0) == EINVAL
+    assert idx(NS=4097) == EINVAL
+    assert idx(T=0) == EINVAL
+    assert idx(dt=7) == EINVAL
+    assert idx(k8=mis4) == EINVAL
+    assert idx(wsb=64) == EWS
+    # copies: nothing to copy, a null pointer, overlapping ranges
+    assert lib.kv8_copy(None, None, 0, None) == OK
+    assert lib.kv8_copy(None, fake, 16, None) == EINVAL
+    assert lib.kv8_copy(fake, fake + 8, 16, None) == EINVAL
