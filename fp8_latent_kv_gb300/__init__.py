@@ -44,6 +44,7 @@ SIGNATURES = {
     "dsa_index_topk8": (_I, [_P, _I, _P, _I, _I, _P, _P, _I64, _I64, _I, _P, _SZ, _P, _P, _P, _P]),
     "mla_out_project8": (_I, [_P, _I, _I, _P, _P, _P, _P, _P]),
     "kv8_copy": (_I, [_P, _P, _SZ, _P]),
+    "kv8_wait_selftest": (_I, [ctypes.c_uint64, _P, _P, _P]),
     "kv8_strerror": (ctypes.c_char_p, [_I]),
 }
 
@@ -216,6 +217,12 @@ def mla_out_project8(ctx, w8, w_scale, out, err_word=None, stream=None) -> None:
     S = ctx.numel() // (H * 512)
     _check("mla_out_project8", load().mla_out_project8(_ptr(ctx), S, H, _ptr(w8), _ptr(w_scale), _ptr(out),
                                                        _ptr(err_word), _stream(stream)))
+
+
+def kv8_wait_selftest(limit_ns: int, err_word, wait_status, stream=None) -> None:
+    """Diagnostic: a bounded wait that nothing completes; sets KV8_ERR_TIMEOUT in err_word and 2 in wait_status
+    (both int32 device tensors) after limit_ns."""
+    _check("kv8_wait_selftest", load().kv8_wait_selftest(limit_ns, _ptr(err_word), _ptr(wait_status), _stream(stream)))
 
 
 def kv8_copy(dst, src, nbytes: int | None = None, stream=None) -> None:

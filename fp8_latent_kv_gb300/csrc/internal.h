@@ -56,6 +56,8 @@ cudaError_t launch_q_absorb_tc(const void *q_nope, int q_bf16, int S, int H, con
                                void *q_lat, int out_bf16, int *err_word, cudaStream_t st);
 cudaError_t launch_out_project_tc(const float *ctx, int S, int H, const uint8_t *w8, const float *w_scale, float *out,
                                   int *err_word, cudaStream_t st);
+// diagnostic: one CTA's bounded wait on an mbarrier nothing completes (see kv8_wait_selftest)
+cudaError_t launch_wait_selftest(uint64_t limit_ns, int *err_word, int *status, cudaStream_t st);
 // the driver's cuTensorMapEncodeTiled, looked up once; null if unavailable
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 int mixed_partitions(int H, int64_t T);

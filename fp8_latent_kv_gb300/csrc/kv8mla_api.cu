@@ -245,6 +245,12 @@ int kv8_copy(void *dst, const void *src, size_t bytes, void *stream) {
     return status(launch_copy(dd, ds, bytes, (cudaStream_t)stream));
 }
 
+int kv8_wait_selftest(uint64_t limit_ns, int *err_word, int *wait_status, void *stream) {
+    if (limit_ns < 1000ull || limit_ns > 1000000000ull || !aligned(err_word, 4) || !aligned(wait_status, 4))
+        return KV8_EINVAL;
+    return status(launch_wait_selftest(limit_ns, err_word, wait_status, (cudaStream_t)stream));
+}
+
 int kv8_encode_e4m3(const float *y, int64_t n, uint8_t *out, void *stream) {
     if (n < 0) return KV8_EINVAL;
     if (n == 0) return KV8_OK;

@@ -316,6 +316,15 @@ KV8_API int dsa_index_topk8(const void *q_idx, int q_dtype, const float *w, int 
  * --------------------------------------------------------------------------------------------- */
 KV8_API int kv8_copy(void *dst, const void *src, size_t bytes, void *stream);
 
+/* -----------------------------------------------------------------------------------------------
+ * kv8_wait_selftest -- diagnostic of the timeout path.  One CTA waits on an mbarrier that nothing
+ * completes, through the same bounded wait the library's tensor-core kernels use for their TMA, MMA and
+ * softmax hand-offs.  After limit_ns (in [1000, 1e9] ns) the wait gives up: KV8_ERR_TIMEOUT is OR-ed into
+ * *err_word, *wait_status is set to 2 (1 would mean the wait completed) and the kernel returns normally,
+ * leaving the context usable.  err_word and wait_status: device ints (required).
+ * --------------------------------------------------------------------------------------------- */
+KV8_API int kv8_wait_selftest(uint64_t limit_ns, int *err_word, int *wait_status, void *stream);
+
 /* Name of a return code (static string). */
 KV8_API const char *kv8_strerror(int code);
 
