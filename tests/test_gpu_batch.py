@@ -4,7 +4,8 @@ fresh row per sequence, vs the oracle.
 Each sequence's output must match the oracle's single-sequence decode over that sequence's own rows;
 the appended rows must be bit-exact.  Edge cases: ragged lengths (1, T_max, in between), a length 0
 (zero output), a length above T_max (clamped), H = 65 and 16, f32 queries (CUDA-core path), a scatter
-destination outside the cache (skipped and reported).
+destination outside the cache (skipped and reported); very unequal lengths, all lengths zero, and 70 and 80
+sequences (one partition each; 80 sequences take more than one wave of CTAs).
 """
 import numpy as np
 import pytest
@@ -74,6 +75,34 @@ def test_batch_decode_empty_and_clamped_lengths(lib, oracle):
         lo = b * stride
         parity(got[b], oracle.attn_decode(q[b, :, :512], q[b, :, 512:], q_o[lo:lo + n], s_o[lo:lo + n], synth.SM_SCALE),
                f"sequence {b}")
+
+
+@pytest.mark.parametrize("B,T_max,lens_kind", [(5, 3000, "unequal"), (4, 600, "zeros"), (70, 256, "ragged"),
+                                               (80, 200, "ragged")])
+def test_batch_decode_many_and_unequal_sequences(lib, oracle, B, T_max, lens_kind):
+    H, stride = 128, T_max
+    rng, rows, q_o, s_o = _setup(oracle, B, T_max, stride, 43 + B)
+    if lens_kind == "unequal":
+        lens = [T_max, 1, 0, 17, T_max // 3]
+    elif lens_kind == "zeros":
+        lens = [0] * B
+    else:
+        lens = [int(x) for x in rng.integers(0, T_max + 1, B)]
+        lens[0] = T_max
+    q = synth.to_bf16_values(rng.standard_normal((B, H, 576)).astype(np.float32))
+    got = _decode(lib, q[..., :512].copy(), q[..., 512:].copy(), torch.from_numpy(q_o).to(DEV),
+                  torch.from_numpy(s_o).to(DEV), T_max, stride, lens, True)
+    heads = [0, 77, 127]
+    for b in range(B):
+        n = min(lens[b], T_max)
+        if n == 0:
+            assert not got[b].any()
+            continue
+        if B > 8 and b % 7:
+            continue  # many sequences: a sample of them against the oracle
+        lo = b * stride
+        ref = oracle.attn_decode(q[b, heads, :512], q[b, heads, 512:], q_o[lo:lo + n], s_o[lo:lo + n], synth.SM_SCALE)
+        parity(got[b][heads], ref, f"sequence {b} of {B} (len {n})")
 
 
 def test_scatter_out_of_range_destination_is_skipped(lib, oracle):
