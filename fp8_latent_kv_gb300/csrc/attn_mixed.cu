@@ -597,7 +597,10 @@ struct MxPrepArgs {
 constexpr int kMxPrepThreads = 256;  // 8 warps, one head each
 
 __global__ void __launch_bounds__(kMxPrepThreads) mixed_prep_kernel(MxPrepArgs a) {
-    grid_launch_dependents();  // the decode kernel may start its row loads while this runs
+    // launched as a programmatic dependent of whatever came before on the stream: nothing is read until
+    // that grid has completed; then the decode kernel may start its row loads while this runs
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if ((int)blockIdx.x < a.n_groups) {
         const int hg = (int)blockIdx.x * (kMxPrepThreads / 32) + warp;
@@ -745,7 +748,16 @@ cudaError_t launch_attn_mixed(const void *q_nope, const void *q_rope, int q_bf16
     cudaError_t e =
         cudaFuncSetAttribute(attn_mixed_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    mixed_prep_kernel<<<(unsigned)(pa.n_groups + P), kMxPrepThreads, 0, st>>>(pa);
+    cudaLaunchConfig_t pcfg = {};
+    pcfg.gridDim = dim3((unsigned)(pa.n_groups + P));
+    pcfg.blockDim = dim3(kMxPrepThreads);
+    pcfg.stream = st;
+    cudaLaunchAttribute pattr[1];
+    pattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pattr[0].val.programmaticStreamSerializationAllowed = 1;
+    pcfg.attrs = pattr;
+    pcfg.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&pcfg, mixed_prep_kernel, pa)) != cudaSuccess) return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(P * a.n_half));

@@ -748,7 +748,10 @@ constexpr int kPrepHeads = 8;                   // heads per query-prep block
 constexpr int kPrepBlock = kPrepHeads * 36;     // one thread per (head, 16-element chunk)
 
 __global__ void __launch_bounds__(kPrepBlock) tc_prep_kernel(PrepArgs a) {
-    grid_launch_dependents();  // the partial kernel may start its row loads while this runs
+    // launched as a programmatic dependent of whatever came before on the stream: nothing is read until
+    // that grid has completed; then the partial kernel may start its row loads while this runs
+    grid_dependency_wait();
+    grid_launch_dependents();
     __shared__ float red[kPrepBlock / 32];
     __shared__ int qmax_bits[kPrepHeads];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, bid = blockIdx.x;
@@ -918,7 +921,16 @@ cudaError_t launch_attn_tc(const AttnArgs &x, cudaStream_t st) {
         a.qimg = pa.img;
         a.c_head = pa.c_head;
         a.smax = pa.smax;
-        tc_prep_kernel<<<(unsigned)((int64_t)a.B * (n_heads_pad / kPrepHeads + a.P)), kPrepBlock, 0, st>>>(pa);
+        cudaLaunchConfig_t pcfg = {};
+        pcfg.gridDim = dim3((unsigned)((int64_t)a.B * (n_heads_pad / kPrepHeads + a.P)));
+        pcfg.blockDim = dim3(kPrepBlock);
+        pcfg.stream = st;
+        cudaLaunchAttribute pattr[1];
+        pattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        pattr[0].val.programmaticStreamSerializationAllowed = 1;
+        pcfg.attrs = pattr;
+        pcfg.numAttrs = 1;
+        if ((e = cudaLaunchKernelEx(&pcfg, tc_prep_kernel, pa)) != cudaSuccess) return e;
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)grid);

@@ -5,6 +5,7 @@
 // outputs are small (a query, a fresh row, one context); a kernel moves them with less fixed cost
 // than a copy-engine transfer.
 #include "internal.h"
+#include "sm100.cuh"
 
 namespace kv8 {
 namespace {
@@ -14,6 +15,7 @@ constexpr int kCopyUnroll = 4;  // 16-byte loads in flight per thread (the host 
 
 __global__ void __launch_bounds__(kCopyThreads) copy16_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
                                                               int64_t n16) {
+    sm100::grid_launch_dependents();  // a programmatic dependent waits for this grid before it reads
     const int64_t stride = (int64_t)gridDim.x * kCopyThreads;
     for (int64_t i0 = (int64_t)blockIdx.x * kCopyThreads + threadIdx.x; i0 < n16; i0 += stride * kCopyUnroll) {
         uint4 v[kCopyUnroll];
@@ -32,6 +34,7 @@ __global__ void __launch_bounds__(kCopyThreads) copy16_kernel(const uint4 *__res
 
 __global__ void __launch_bounds__(kCopyThreads) copy1_kernel(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst,
                                                              int64_t n) {
+    sm100::grid_launch_dependents();
     const int64_t stride = (int64_t)gridDim.x * kCopyThreads;
     for (int64_t i = (int64_t)blockIdx.x * kCopyThreads + threadIdx.x; i < n; i += stride) dst[i] = src[i];
 }

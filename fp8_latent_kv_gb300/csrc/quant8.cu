@@ -12,6 +12,7 @@
 // cvt.rn.satfinite.e4m3x2.f32 (RNE, saturating, sign-preserving) with NaN inputs forced to 0x00.
 #include "internal.h"
 #include "quant_row.cuh"
+#include "sm100.cuh"
 
 namespace kv8 {
 
@@ -23,6 +24,9 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const float *__restrict
                                                           uint8_t *__restrict__ q, float *__restrict__ scale,
                                                           const int64_t *__restrict__ dst, int64_t cache_rows,
                                                           int *err_word) {
+    // a programmatic dependent (the next call's query prep) may launch now; it waits for this grid
+    // before it reads anything
+    sm100::grid_launch_dependents();
     constexpr int kF4 = W / 4, kPer = (kF4 + 31) / 32;
     const int lane = threadIdx.x & 31;
     const int64_t in_row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
