@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(kPThreads, 1) q_absorb_tc_kernel(const void *_
             }
             mma_commit(&sm.mma_bar);
         }
-        // one verdict for the whole block: every thread must take the same path through the barriers
+        // one decision for the whole block: every thread must take the same path through the barriers
         ok = __syncthreads_and(commit_wait(&sm.mma_bar, (uint32_t)(ti & 1), err_word)) != 0;
         tc_fence_after_sync();
         // ---- epilogue: thread (row r, column half) -> 256 outputs, scaled per 128-column block
@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(kPThreads, 1) out_project_tc_kernel(const floa
                         }
                 mma_commit(&sm.mma_bar);
             }
-            // one verdict for the whole block (the barrier also frees the A tile for the next block)
+            // one decision for the whole block (the barrier also frees the A tile for the next block)
             ok = __syncthreads_and(commit_wait(&sm.mma_bar, phase, err_word)) != 0;
             phase ^= 1u;
             tc_fence_after_sync();
