@@ -36,10 +36,26 @@ constexpr int kIAcc = 4;          // TMEM accumulator buffers
 constexpr int kIThreads = 320;    // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue (two groups of four)
 constexpr uint32_t kIStageBytes = kITile * kIdxD;  // 16 KB
 
+// top-k workspace layout and key order (the score kernel also builds the first radix pass's histogram)
+constexpr int kKThreads = 512;
+constexpr int kKBins = 2048;
+constexpr int kKMaxC = 152;
+constexpr int kKCache = 8192;  // a CTA's scores staged in shared memory when its range is this short
+// per-query workspace (u32): three pass histograms, per-CTA (above, equal) counts, barrier counter
+constexpr int kKWsHist = 3 * kKBins;
+constexpr int kKWsPerItem = kKWsHist + 2 * kKMaxC + 32;
+
+// order-preserving key: larger float -> larger unsigned key (-0 sorts just below +0)
+__device__ __forceinline__ uint32_t fkey(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 struct IdxSmem {
     alignas(1024) uint8_t stage[kIStages][kIStageBytes];
     alignas(1024) uint8_t qimg[KV8_MAX_IDX_HEADS * kIdxD];  // B operand: HI rows of 128 bytes, 128B-swizzled
     alignas(16) float wq[KV8_MAX_IDX_HEADS];                // w[h] * q_scale[h]
+    uint32_t hist0[kKBins];                                 // the CTA's keys by their top 11 bits (radix pass 0)
     uint64_t full[kIStages], empty[kIStages], dfull[kIAcc], dempty[kIAcc], final_bar, qready;
     uint32_t tmem_base;
     int abort_flag;
@@ -54,6 +70,7 @@ struct IdxArgs {
     int64_t T, seq_stride_rows;
     int ctas_per_item;
     float *scores;        // [B][T]
+    uint32_t *hist0;      // top-k workspace: each item's pass-0 histogram gets this kernel's counts, or null
     int *err_word;
 };
 
@@ -121,6 +138,7 @@ __global__ void __launch_bounds__(kIThreads, 1) index_score_kernel(const __grid_
         tmem_alloc(&sm.tmem_base, ncols);
         tmem_relinquish();
     }
+    for (int i = tid; i < kKBins; i += kIThreads) sm.hist0[i] = 0u;
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -242,36 +260,29 @@ __global__ void __launch_bounds__(kIThreads, 1) index_score_kernel(const __grid_
             tc_fence_before_sync();
             mbar_arrive(&sm.dempty[buf]);
             const int64_t t = (i0 + i) * kITile + r;
-            if (t < a.T) a.scores[(int64_t)b * a.T + t] = ks * acc;
+            if (t < a.T) {
+                const float sv = ks * acc;
+                a.scores[(int64_t)b * a.T + t] = sv;
+                atomicAdd(&sm.hist0[fkey(sv) >> 21], 1u);  // the top-k's first radix digit
+            }
         }
     }
     tc_fence_before_sync();
     __syncthreads();
+    if (a.hist0)
+        for (int i = tid; i < kKBins; i += kIThreads)
+            if (sm.hist0[i]) atomicAdd(&a.hist0[(int64_t)b * kKWsPerItem + i], sm.hist0[i]);
     if (warp == 1) tmem_dealloc(tmem, ncols);
 }
 
 // ------------------------------------------------------------------------------------------------
 // top-k: C CTAs per query (a cooperative launch: all CTAs resident), CTA c owning positions
-// [c*T/C, (c+1)*T/C).  Each radix pass: a shared histogram of the CTA's candidates (plain shared
-// atomics; grouping equal bins with __match_any_sync first was slower), added once into the query's
-// global histogram; a barrier of the query's C CTAs; every CTA then finds the pass's bin from the global
-// histogram.  The final pass counts keys above / equal to the k-th key
+// [c*T/C, (c+1)*T/C).  Pass 0's histogram (the keys' top 11 bits) comes complete from the score kernel.
+// Passes 1 and 2: a shared histogram of the CTA's candidates (plain shared atomics; grouping equal bins
+// with __match_any_sync first was slower), added once into the query's global histogram; a barrier of the
+// query's C CTAs.  After each pass every CTA finds the pass's bin from the global histogram.  The final pass counts keys above / equal to the k-th key
 // per CTA, and after a last barrier each CTA writes its selected positions at their global offsets.
 // ------------------------------------------------------------------------------------------------
-constexpr int kKThreads = 512;
-constexpr int kKBins = 2048;
-constexpr int kKMaxC = 152;
-constexpr int kKCache = 8192;  // a CTA's scores staged in shared memory when its range is this short
-// per-query workspace (u32): three pass histograms, per-CTA (above, equal) counts, barrier counter
-constexpr int kKWsHist = 3 * kKBins;
-constexpr int kKWsPerItem = kKWsHist + 2 * kKMaxC + 32;
-
-// order-preserving key: larger float -> larger unsigned key (-0 sorts just below +0)
-__device__ __forceinline__ uint32_t fkey(float f) {
-    const uint32_t u = __float_as_uint(f);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
 // Block-wide exclusive scan of one value per thread; returns the prefix, *total gets the sum.
 __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *warp_sums, uint32_t *total) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
@@ -350,19 +361,22 @@ __global__ void __launch_bounds__(kKThreads) topk_kernel(const float *__restrict
     for (int p = 0; p < 3; ++p) {
         const int shift = shifts[p];
         const uint32_t nb = 1u << widths[p];
-        for (int i = tid; i < kKBins; i += kKThreads) hist[i] = 0;
-        __syncthreads();
-        for (int64_t t0 = c0; t0 < c1; t0 += kKThreads) {
-            const int64_t t = t0 + tid;
-            const bool in = t < c1;
-            const uint32_t key = in ? key_at(t) : 0u;
-            const bool cand = in && (key & mask) == prefix;
-            if (cand) atomicAdd(&hist[(key >> shift) & (nb - 1)], 1u);
+        // pass 0's histogram was built by the score kernel (complete: it ran before this grid)
+        if (p > 0) {
+            for (int i = tid; i < kKBins; i += kKThreads) hist[i] = 0;
+            __syncthreads();
+            for (int64_t t0 = c0; t0 < c1; t0 += kKThreads) {
+                const int64_t t = t0 + tid;
+                const bool in = t < c1;
+                const uint32_t key = in ? key_at(t) : 0u;
+                const bool cand = in && (key & mask) == prefix;
+                if (cand) atomicAdd(&hist[(key >> shift) & (nb - 1)], 1u);
+            }
+            __syncthreads();
+            for (int i = tid; i < (int)nb; i += kKThreads)
+                if (hist[i]) atomicAdd(&ghist[p * kKBins + i], hist[i]);
+            if (!query_barrier(gbar, (uint32_t)p * (uint32_t)C, err_word, &abort_sh)) return;
         }
-        __syncthreads();
-        for (int i = tid; i < (int)nb; i += kKThreads)
-            if (hist[i]) atomicAdd(&ghist[p * kKBins + i], hist[i]);
-        if (!query_barrier(gbar, (uint32_t)(p + 1) * (uint32_t)C, err_word, &abort_sh)) return;
         // the bin where the count from the top reaches `need`: thread j holds 4 bins in descending order
         uint32_t cnt[4], sum = 0;
 #pragma unroll
@@ -406,7 +420,7 @@ __global__ void __launch_bounds__(kKThreads) topk_kernel(const float *__restrict
         gcnt[2 * c] = cta_gt;
         gcnt[2 * c + 1] = cta_eq;
     }
-    if (!query_barrier(gbar, 4u * (uint32_t)C, err_word, &abort_sh)) return;
+    if (!query_barrier(gbar, 3u * (uint32_t)C, err_word, &abort_sh)) return;
     uint32_t gt_prev = 0, eq_prev = 0;  // over the query's earlier CTAs
     for (int cc = 0; cc < c; ++cc) {
         gt_prev += __ldcg(&gcnt[2 * cc]);
@@ -433,7 +447,7 @@ __global__ void __launch_bounds__(kKThreads) topk_kernel(const float *__restrict
 
 cudaError_t launch_index_scores(const void *q, int q_bf16, const float *w, int B, int HI, const uint8_t *k8,
                                 const float *k_scale, int64_t T, int64_t seq_stride_rows, float *scores,
-                                int *err_word, cudaStream_t st) {
+                                void *topk_ws, int *err_word, cudaStream_t st) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
     const int64_t rows = (int64_t)(B - 1) * seq_stride_rows + T;
@@ -457,6 +471,7 @@ cudaError_t launch_index_scores(const void *q, int q_bf16, const float *w, int B
     a.seq_stride_rows = seq_stride_rows;
     a.ctas_per_item = B >= 152 ? 1 : 152 / B;  // one wave of CTAs (one per SM of a 152-SM part)
     a.scores = scores;
+    a.hist0 = static_cast<uint32_t *>(topk_ws);
     a.err_word = err_word;
     const size_t smem = sizeof(IdxSmem);
     cudaError_t e = cudaFuncSetAttribute(index_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -467,10 +482,13 @@ cudaError_t launch_index_scores(const void *q, int q_bf16, const float *w, int B
 
 size_t topk_workspace_bytes(int B) { return (size_t)B * kKWsPerItem * sizeof(uint32_t); }
 
+cudaError_t reset_topk_workspace(void *ws, int B, cudaStream_t st) {
+    return cudaMemsetAsync(ws, 0, topk_workspace_bytes(B), st);
+}
+
 cudaError_t launch_topk(const float *scores, int B, int64_t T, int NS, int32_t *idx, void *ws, int *err_word,
                         cudaStream_t st) {
-    cudaError_t e = cudaMemsetAsync(ws, 0, topk_workspace_bytes(B), st);
-    if (e != cudaSuccess) return e;
+    cudaError_t e;
     const int C = B >= kKMaxC ? 1 : kKMaxC / B;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(B * C));

@@ -36,10 +36,12 @@ cudaError_t launch_quant_rows(const float *x, int64_t n, uint8_t *q, float *scal
 cudaError_t launch_quant_rows_scatter(const float *x, int64_t n, const int64_t *dst, int64_t cache_rows, uint8_t *q,
                                       float *scale, int *err_word, cudaStream_t st);
 cudaError_t launch_quant_rows_w(const float *x, int64_t n, int width, uint8_t *q, float *scale, cudaStream_t st);
+// the scores also fill each item's pass-0 top-k histogram in topk_ws (zeroed first by reset_topk_workspace)
 cudaError_t launch_index_scores(const void *q, int q_bf16, const float *w, int B, int HI, const uint8_t *k8,
                                 const float *k_scale, int64_t T, int64_t seq_stride_rows, float *scores,
-                                int *err_word, cudaStream_t st);
+                                void *topk_ws, int *err_word, cudaStream_t st);
 size_t topk_workspace_bytes(int B);
+cudaError_t reset_topk_workspace(void *ws, int B, cudaStream_t st);
 cudaError_t launch_topk(const float *scores, int B, int64_t T, int NS, int32_t *idx, void *ws, int *err_word,
                         cudaStream_t st);
 cudaError_t launch_encode(const float *y, int64_t n, uint8_t *out, cudaStream_t st);

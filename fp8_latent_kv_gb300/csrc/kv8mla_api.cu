@@ -211,8 +211,10 @@ int dsa_index_topk8(const void *q_idx, int q_dtype, const float *w, int B, int H
         !aligned(k_scale, 4) || !aligned(scores, 16) || !aligned(idx, 16) || !aligned(workspace, 16))
         return KV8_EINVAL;
     if (ws_bytes < topk_workspace_bytes(B)) return KV8_EWORKSPACE;
-    cudaError_t e = launch_index_scores(q_idx, q_dtype == KV8_BF16, w, B, HI, k8, k_scale, T, seq_stride_rows, scores,
-                                        err_word, (cudaStream_t)stream);
+    cudaError_t e = reset_topk_workspace(workspace, B, (cudaStream_t)stream);
+    if (e == cudaSuccess)
+        e = launch_index_scores(q_idx, q_dtype == KV8_BF16, w, B, HI, k8, k_scale, T, seq_stride_rows, scores, workspace,
+                                err_word, (cudaStream_t)stream);
     if (e != cudaSuccess) return KV8_ECUDA;
     return status(launch_topk(scores, B, T, NS, idx, workspace, err_word, (cudaStream_t)stream));
 }
