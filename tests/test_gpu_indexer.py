@@ -152,3 +152,28 @@ def test_indexer_then_selected_attention(lib, oracle):
     ref, n_bad = oracle.attn_select(ql, qr, q_o, s_o, T, T, idx, synth.SM_SCALE)
     assert n_bad == 0
     parity(out.cpu().numpy(), ref, "attention over the indexer's selection")
+
+
+def test_workspace_reused_and_dirty(lib, oracle):
+    """The call zeroes its workspace itself (histograms, counts, barrier counters): a workspace that holds
+    garbage, or the previous call's state, gives the same scores and the same selection."""
+    rng = np.random.default_rng(35)
+    B, HI, T, NS = 3, 64, 5000, 300
+    rows = (rng.standard_normal((B * T, 128)) * 10.0 ** rng.uniform(-1, 1, (B * T, 1))).astype(np.float32)
+    k8, ks, tk8, tks = _keys(oracle, rows)
+    q = _qtensor(synth.to_bf16_values(rng.standard_normal((B, HI, 128)).astype(np.float32)), True)
+    w = torch.from_numpy(rng.standard_normal((B, HI)).astype(np.float32)).to(DEV)
+    ws = torch.full((lib.dsa_index_workspace_bytes(B) // 4,), 0x5A5A5A5A, dtype=torch.int32, device=DEV)
+    outs = []
+    for _ in range(3):
+        scores = torch.empty((B, T), dtype=torch.float32, device=DEV)
+        idx = torch.full((B, NS), -7, dtype=torch.int32, device=DEV)
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        lib.dsa_index_topk8(q, w, tk8, tks, T, T, NS, ws, scores, idx, err_word=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        outs.append((scores.cpu().numpy(), idx.cpu().numpy()))
+    for s_, i_ in outs[1:]:
+        assert np.array_equal(s_, outs[0][0]) and np.array_equal(i_, outs[0][1])
+    for b in range(B):
+        assert np.array_equal(outs[0][1][b], oracle.topk(outs[0][0][b], NS))
