@@ -48,9 +48,13 @@ using namespace sm100;
 
 constexpr int kTile = 128;             // rows per tile
 constexpr int kHeadsPerCta = 64;
-constexpr int kThreads = 320;          // 10 warps
-constexpr int kSoftmaxThreads = 256;   // warps 2..9
-constexpr int kPrepThreads = 288;      // warps 1..9
+constexpr int kHG = 16;                // heads per softmax group (four warps, one per TMEM lane quadrant)
+constexpr int kNG = kHeadsPerCta / kHG;  // softmax groups
+constexpr int kThreads = 64 + 128 * kNG; // warp 0 TMA, warp 1 MMA, then the softmax groups
+constexpr int kSoftmaxThreads = 128 * kNG;
+constexpr int kPrepThreads = 288;      // warps 1..9: the in-kernel query prep's workers
+constexpr int kPrepAll = kThreads - 32;  // warps 1..: every thread that waits for the prologue
+static_assert(kHG == 16 || kHG == 32, "a softmax thread's heads: one or two 16-column TMEM loads");
 constexpr uint32_t kImg = 73728;       // 4 x 16 KB (SW128, 128 B per row) + 8 KB (SW64, 64 B per row)
 constexpr uint32_t kRcOff = 65536;     // rope block inside an image / stage
 constexpr uint32_t OFF_Q = 0, OFF_ST0 = kImg, OFF_ST1 = 2 * kImg, OFF_PLO = 3 * kImg, OFF_MISC = 3 * kImg + 8192;
@@ -70,8 +74,8 @@ struct Misc {
             float wred[2][16];                 // prologue: per-warp maxima
         } pro;
         struct {
-            float alpha[2][32];                // tile loop, per head half: rescale factors 2^(m_old - m_new)
-            float delta[2][32];                // and the reference shifts m_ref_old - m_ref_new
+            float alpha[kNG][kHG];             // tile loop, per softmax group: rescale factors 2^(m_old - m_new)
+            float delta[kNG][kHG];             // and the reference shifts m_ref_old - m_ref_new
         } tile;
         struct {
             float zsum[kHeadsPerCta];          // epilogue: row sums per head
@@ -272,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ======================= prologue: query image, row-scale max =======================
-        const int pt = tid - 32;  // 0..287
+        const int pt = tid - 32;  // 0..kPrepAll-1; the query-prep workers are pt < kPrepThreads
         float smax = 0.f;
         if (a.qimg) {
             // decode: the prep kernel wrote the query image (loaded by the producer) and the factors
@@ -283,20 +287,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             // prefill: each CTA prepares its own 64 heads (the image is reused for all its tiles)
             constexpr int kItems = kHeadsPerCta * 36 / kPrepThreads;  // 8 chunks of 16 query elements
             static_assert(kHeadsPerCta * 36 == kItems * kPrepThreads, "query chunks split evenly");
-            uint4 qv[kItems][2];
-#pragma unroll
-            for (int k = 0; k < kItems; ++k) {
+            const bool worker = pt < kPrepThreads;
+            // query chunk k of this thread (16 bf16 values as two uint4), zeros for a padding head; loaded
+            // before the barrier for the maxima and again after it for the split (not held across it)
+            auto load_chunk = [&](int k, uint4 &u0, uint4 &u1) {
                 const int it = pt + k * kPrepThreads, h = it / 36, ch = it - h * 36;
                 const int hg = half * kHeadsPerCta + h;
-                qv[k][0] = qv[k][1] = make_uint4(0u, 0u, 0u, 0u);
-                if (hg < a.H) {
+                u0 = u1 = make_uint4(0u, 0u, 0u, 0u);
+                if (worker && hg < a.H) {
                     const __nv_bfloat16 *src = ch < 32 ? a.q_lat + ((int64_t)b * a.H + hg) * kKL + ch * 16
                                                        : a.q_rope + ((int64_t)b * a.H + hg) * kKR + (ch - 32) * 16;
-                    qv[k][0] = __ldg(reinterpret_cast<const uint4 *>(src));
-                    qv[k][1] = __ldg(reinterpret_cast<const uint4 *>(src) + 1);
+                    u0 = __ldg(reinterpret_cast<const uint4 *>(src));
+                    u1 = __ldg(reinterpret_cast<const uint4 *>(src) + 1);
+                }
+            };
+            static_assert(kItems % 4 == 0, "query chunks in rounds of four");
+#pragma unroll 1
+            for (int k0 = 0; k0 < kItems; k0 += 4) {
+                uint4 qv[4][2];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) load_chunk(k0 + u, qv[u][0], qv[u][1]);
+#pragma unroll
+                for (int u = 0; u < 4 && worker; ++u) {
+                    const int k = u;
+                    const int it = pt + (k0 + u) * kPrepThreads, h = it / 36;
+                    const uint32_t w[8] = {qv[k][0].x, qv[k][0].y, qv[k][0].z, qv[k][0].w,
+                                           qv[k][1].x, qv[k][1].y, qv[k][1].z, qv[k][1].w};
+                    float mx = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
+                        mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+                    }
+                    atomicMax(&ms.ph.pro.qmax_bits[h], __float_as_int(mx));  // non-negative floats order like ints
                 }
             }
-            for (int64_t t = t0 + pt; t < t1; t += 8 * kPrepThreads) {
+            for (int64_t t = t0 + pt; worker && t < t1; t += 8 * kPrepThreads) {
                 float v[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
@@ -306,35 +332,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int u = 0; u < 8; ++u) smax = fmaxf(smax, fabsf(v[u]));
             }
-#pragma unroll
-            for (int k = 0; k < kItems; ++k) {
-                const int it = pt + k * kPrepThreads, h = it / 36;
-                const uint32_t w[8] = {qv[k][0].x, qv[k][0].y, qv[k][0].z, qv[k][0].w,
-                                       qv[k][1].x, qv[k][1].y, qv[k][1].z, qv[k][1].w};
-                float mx = 0.f;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
-                    mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
-                }
-                atomicMax(&ms.ph.pro.qmax_bits[h], __float_as_int(mx));  // non-negative floats order like ints
-            }
             smax = warp_max(smax);
-            if (lane == 0) ms.ph.pro.wred[1][warp - 1] = smax;
-            named_sync(1, kPrepThreads);
+            if (lane == 0 && pt < kPrepThreads) ms.ph.pro.wred[1][warp - 1] = smax;
+            named_sync(1, kPrepAll);
             smax = 0.f;
             for (int k = 0; k < 9; ++k) smax = fmaxf(smax, ms.ph.pro.wred[1][k]);
             // q_h * 2^e_h lies in [128, 256): every bf16 value splits exactly into e4m3 hi + lo (down to
             // the e4m3 subnormal step); the score is rescaled by 2^-e_h.
-#pragma unroll
-            for (int k = 0; k < kItems; ++k) {
+#pragma unroll 2
+            for (int k = 0; k < kItems && worker; ++k) {
                 const int it = pt + k * kPrepThreads, h = it / 36, ch = it - h * 36;
+                uint4 u0, u1;
+                load_chunk(k, u0, u1);
                 const float qmax = __int_as_float(ms.ph.pro.qmax_bits[h]);
                 int E = 0;
                 if (qmax > 0.f) frexpf(qmax, &E);
                 const int sh = qmax > 0.f ? 8 - E : 0;  // values are scaled, not a 2^sh factor: it may overflow
-                const uint32_t w[8] = {qv[k][0].x, qv[k][0].y, qv[k][0].z, qv[k][0].w,
-                                       qv[k][1].x, qv[k][1].y, qv[k][1].z, qv[k][1].w};
+                const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
                 uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
                 for (int e2 = 0; e2 < 8; ++e2) {
@@ -376,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ms.out_mul = s_ref / kWScale;
         }
         fence_proxy_async_smem();
-        named_sync(1, kPrepThreads);
+        named_sync(1, kPrepAll);
 
         if (warp == 1) {
             // ================================ MMA issuer ================================
@@ -463,19 +477,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
         } else {
             // ============================ softmax + epilogue ============================
-            // Each thread owns one tile row (TMEM lane) and the 32 heads of its head half.  The four
-            // warps of a head half decide and rescale together through named barrier 2 + hh.  A wait
-            // that gives up clears `ok`; the thread then skips its remaining waits but still reaches
-            // every named barrier of every tile, so the other warps never wait for it.
+            // Each thread owns one tile row (TMEM lane) and the kHG heads of its softmax group.  The four
+            // warps of a group decide and rescale together through named barrier 2 + grp.  A wait that
+            // gives up clears `ok`; the thread then skips its remaining waits but still reaches every named
+            // barrier of every tile, so the other warps never wait for it.
+            constexpr int kV4 = kHG / 4, kLd = kHG / 16;  // float4s / 16-column TMEM loads per head set
             const int q = warp & 3;               // TMEM lane quadrant
-            const int hh = (warp - 2) >> 2;       // which 32 of the CTA's 64 heads
+            const int grp = (warp - 2) >> 2;      // which kHG of the CTA's 64 heads
+            const int h0 = kHG * grp;             // the group's first head (within the CTA)
             const int r = q * 32 + lane;          // row within the tile = TMEM lane
             const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-            const int bar_id = 2 + hh;
+            const int bar_id = 2 + grp;
             const float w_mul = ms.w_mul;
-            float z[32];
+            float z[kHG];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) z[j] = 0.f;
+            for (int j = 0; j < kHG; ++j) z[j] = 0.f;
             // scale of the row at list position pos, or -1 if that row is masked (past the end, or an
             // index outside [0, T), which is also reported)
             bool bad_index = false;
@@ -489,10 +505,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 return __ldg(a.kv_scale + seq_base + ri);
             };
+            // butterfly transpose-reduction of kHG values over the warp: at step k each lane keeps the half
+            // of its heads selected by lane bit k and combines the other half from lane ^ k; after log2(kHG)
+            // steps lane l holds head (l % kHG) over the lanes that differ in the low bits, and the last
+            // steps combine the lanes that differ in the high bits
+            auto warp_reduce_heads = [&](float (&v)[kHG], bool take_max) -> float {
+#pragma unroll
+                for (int k = kHG / 2; k >= 1; k >>= 1) {
+                    const bool upper = (lane & k) != 0;
+#pragma unroll
+                    for (int j = 0; j < k; ++j) {
+                        const float send = upper ? v[j] : v[j + k];
+                        const float keep = upper ? v[j + k] : v[j];
+                        const float other = __shfl_xor_sync(0xffffffffu, send, k);
+                        v[j] = take_max ? fmaxf(keep, other) : keep + other;
+                    }
+                }
+                float x = v[0];
+#pragma unroll
+                for (int o = kHG; o < 32; o <<= 1) {
+                    const float other = __shfl_xor_sync(0xffffffffu, x, o);
+                    x = take_max ? fmaxf(x, other) : x + other;
+                }
+                return x;
+            };
             float sc_next = n_tiles > 0 ? row_scale(t0 + r) : -1.f;
             bool ok = true;
             bool seen = false;  // some valid row has been scored: every head's running max is finite
-            int cur = 0;        // which copy of ms.m_run / ms.m_ref is current (uniform across the half)
+            int cur = 0;        // which copy of ms.m_run / ms.m_ref is current (uniform across the group)
             for (int i = 0; i < n_tiles; ++i) {
                 const int bb = i & 1;
                 const int64_t t = t0 + (int64_t)i * kTile + r;
@@ -502,29 +542,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 if (ok) ok = mbar_wait(&ms.s_full[bb], (i >> 1) & 1, &ms.abort_flag, a.err_word);
                 tc_fence_after_sync();
-                float sc_[32];  // S = hi piece + lo piece, one TMEM round trip
+                float sc_[kHG];  // S = hi piece + lo piece, one TMEM round trip
                 {
-                    uint32_t shi[2][16], slo[2][16];
-                    const uint32_t ta = tmem + lane_addr + (uint32_t)bb * 128u + 32u * hh;
-                    tmem_ld_32x32b_x16(ta, shi[0]);
-                    tmem_ld_32x32b_x16(ta + 16u, shi[1]);
-                    tmem_ld_32x32b_x16(ta + 64u, slo[0]);
-                    tmem_ld_32x32b_x16(ta + 80u, slo[1]);
+                    uint32_t shi[kLd][16], slo[kLd][16];
+                    const uint32_t ta = tmem + lane_addr + (uint32_t)bb * 128u + (uint32_t)h0;
+#pragma unroll
+                    for (int u = 0; u < kLd; ++u) {
+                        tmem_ld_32x32b_x16(ta + 16u * u, shi[u]);
+                        tmem_ld_32x32b_x16(ta + 64u + 16u * u, slo[u]);
+                    }
                     tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) sc_[j] = __uint_as_float(shi[j >> 4][j & 15]) + __uint_as_float(slo[j >> 4][j & 15]);
+                    for (int j = 0; j < kHG; ++j) sc_[j] = __uint_as_float(shi[j >> 4][j & 15]) + __uint_as_float(slo[j >> 4][j & 15]);
                 }
                 tc_fence_before_sync();
                 mbar_arrive(&ms.s_free[bb]);
 
                 // d = s - ref with s = S * sm_scale*log2(e)*2^-e_h * s_t (one FMA per score); ref is the
                 // running max, or 0 before any valid row
-                float d[32];
+                float d[kHG];
                 float dmax = -INFINITY;
-                const float *mref = &ms.m_ref[cur][32 * hh];
+                const float *mref = &ms.m_ref[cur][h0];
 #pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    const float4 c4 = *reinterpret_cast<const float4 *>(&ms.c_head[32 * hh + 4 * j4]);
+                for (int j4 = 0; j4 < kV4; ++j4) {
+                    const float4 c4 = *reinterpret_cast<const float4 *>(&ms.c_head[h0 + 4 * j4]);
                     const float4 r4 = *reinterpret_cast<const float4 *>(mref + 4 * j4);
                     d[4 * j4 + 0] = fmaf(sc_[4 * j4 + 0], c4.x * sc_t, -r4.x);
                     d[4 * j4 + 1] = fmaf(sc_[4 * j4 + 1], c4.y * sc_t, -r4.y);
@@ -534,32 +575,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!valid) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) d[j] = -INFINITY;
+                    for (int j = 0; j < kHG; ++j) d[j] = -INFINITY;
                     dmax = -INFINITY;
                 }
-                // lazy rescale: the half takes the slow path when some score exceeds its head's running
+                // lazy rescale: the group takes the slow path when some score exceeds its head's running
                 // max by more than kTau, or while no valid row has been seen
                 const bool slow = bar_red_or(bar_id, 128, dmax > kTau || !seen);
                 bool any_alpha = false;
                 if (slow) {
-                    // tile max per head over this warp's 32 rows: butterfly transpose-reduction.  At
-                    // step k each lane keeps the half of its heads selected by lane bit k and takes the
-                    // max with the other half from lane ^ k; after 5 steps lane l holds head l's max.
-                    float v[32];
+                    float v[kHG];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = d[j];
-#pragma unroll
-                    for (int k = 16; k >= 1; k >>= 1) {
-                        const bool upper = (lane & k) != 0;
-#pragma unroll
-                        for (int j = 0; j < k; ++j) {
-                            const float send = upper ? v[j] : v[j + k];
-                            const float keep = upper ? v[j + k] : v[j];
-                            v[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, k));
-                        }
-                    }
-                    const int hj = 32 * hh + lane;  // lane l now speaks for head l of the half
-                    ms.red[q][hj] = v[0];
+                    for (int j = 0; j < kHG; ++j) v[j] = d[j];
+                    const float vmax = warp_reduce_heads(v, true);  // this warp's 32 rows, head lane % kHG
+                    const int hl = lane & (kHG - 1);
+                    const int hj = h0 + hl;
+                    if (lane < kHG) ms.red[q][hj] = vmax;
                     named_sync(bar_id, 128);
                     const float ref_o = ms.m_ref[cur][hj], mo = ms.m_run[cur][hj];
                     const float tmax = fmaxf(fmaxf(ms.red[0][hj], ms.red[1][hj]), fmaxf(ms.red[2][hj], ms.red[3][hj])) + ref_o;
@@ -567,17 +597,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float al = (mo == -INFINITY || mn == mo) ? 1.f : ex2_approx(mo - mn);
                     const float ref_n = mn == -INFINITY ? 0.f : mn;
                     // the four quadrant warps write the same values
-                    ms.m_run[cur ^ 1][hj] = mn;
-                    ms.m_ref[cur ^ 1][hj] = ref_n;
-                    ms.ph.tile.alpha[hh][lane] = al;
-                    ms.ph.tile.delta[hh][lane] = ref_o - ref_n;
+                    if (lane < kHG) {
+                        ms.m_run[cur ^ 1][hj] = mn;
+                        ms.m_ref[cur ^ 1][hj] = ref_n;
+                        ms.ph.tile.alpha[grp][hl] = al;
+                        ms.ph.tile.delta[grp][hl] = ref_o - ref_n;
+                    }
                     seen = __shfl_sync(0xffffffffu, mn, 0) != -INFINITY;  // the same for every head
                     any_alpha = __any_sync(0xffffffffu, al != 1.f);
                     __syncwarp();
 #pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4) {
-                        const float4 a4 = *reinterpret_cast<const float4 *>(&ms.ph.tile.alpha[hh][4 * j4]);
-                        const float4 e4 = *reinterpret_cast<const float4 *>(&ms.ph.tile.delta[hh][4 * j4]);
+                    for (int j4 = 0; j4 < kV4; ++j4) {
+                        const float4 a4 = *reinterpret_cast<const float4 *>(&ms.ph.tile.alpha[grp][4 * j4]);
+                        const float4 e4 = *reinterpret_cast<const float4 *>(&ms.ph.tile.delta[grp][4 * j4]);
                         d[4 * j4 + 0] += e4.x;
                         d[4 * j4 + 1] += e4.y;
                         d[4 * j4 + 2] += e4.z;
@@ -591,9 +623,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // weights: p = 2^d (row sum z), w = p * s_t * kWScale / s_ref, split e4m3 hi + lo
                 const float g = valid ? sc_t * w_mul : 0.f;
-                uint32_t whi[8], wlo[8];
+                uint32_t whi[kV4], wlo[kV4];
 #pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
+                for (int j4 = 0; j4 < kV4; ++j4) {
                     const float p0 = ex2_approx(d[4 * j4 + 0]), p1 = ex2_approx(d[4 * j4 + 1]);
                     const float p2 = ex2_approx(d[4 * j4 + 2]), p3 = ex2_approx(d[4 * j4 + 3]);
                     z[4 * j4 + 0] += p0;
@@ -607,48 +639,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                     wlo[j4] = l01 | (l23 << 16);
                 }
                 uint8_t *phi = smem + (bb ? OFF_ST1 : OFF_ST0) + kRcOff;  // the rope block, read by the score already
-                *reinterpret_cast<uint4 *>(phi + sw64_offset(r, 32 * hh)) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
-                *reinterpret_cast<uint4 *>(phi + sw64_offset(r, 32 * hh + 16)) =
-                    make_uint4(whi[4], whi[5], whi[6], whi[7]);
+#pragma unroll
+                for (int u = 0; u < kV4 / 4; ++u)
+                    *reinterpret_cast<uint4 *>(phi + sw64_offset(r, h0 + 16 * u)) =
+                        make_uint4(whi[4 * u], whi[4 * u + 1], whi[4 * u + 2], whi[4 * u + 3]);
                 if (i >= 1) {
                     // the previous context product must be done before its weights' lo buffer is reused
                     // and before its accumulators are rescaled
                     if (ok) ok = mbar_wait(&ms.pv_done, (i - 1) & 1, &ms.abort_flag, a.err_word);
                     if (any_alpha) {
-                        // rescale this half's columns of the four context accumulators, two per TMEM round trip
+                        // rescale this group's columns of the four context accumulators, 32 columns per
+                        // TMEM round trip
                         tc_fence_after_sync();
+                        constexpr int kPerTrip = 32 / kHG;  // accumulators per round trip
 #pragma unroll 1
-                        for (int c2 = 0; c2 < 2; ++c2) {
-                            const uint32_t ta = tmem + lane_addr + 256u + 128u * c2 + 32u * hh;
-                            uint32_t o[64];
-                            tmem_ld_32x32b_x16(ta, *reinterpret_cast<uint32_t(*)[16]>(o));
-                            tmem_ld_32x32b_x16(ta + 16u, *reinterpret_cast<uint32_t(*)[16]>(o + 16));
-                            tmem_ld_32x32b_x16(ta + 64u, *reinterpret_cast<uint32_t(*)[16]>(o + 32));
-                            tmem_ld_32x32b_x16(ta + 80u, *reinterpret_cast<uint32_t(*)[16]>(o + 48));
-                            tmem_wait_ld();
-                            const float *al = ms.ph.tile.alpha[hh];
+                        for (int c0 = 0; c0 < 4; c0 += kPerTrip) {
+                            uint32_t o[kPerTrip][kHG];
 #pragma unroll
-                            for (int j4 = 0; j4 < 8; ++j4) {
+                            for (int c = 0; c < kPerTrip; ++c)
+#pragma unroll
+                                for (int u = 0; u < kLd; ++u)
+                                    tmem_ld_32x32b_x16(tmem + lane_addr + 256u + 64u * (c0 + c) + (uint32_t)h0 + 16u * u,
+                                                       *reinterpret_cast<uint32_t(*)[16]>(&o[c][16 * u]));
+                            tmem_wait_ld();
+                            const float *al = ms.ph.tile.alpha[grp];
+#pragma unroll
+                            for (int j4 = 0; j4 < kV4; ++j4) {
                                 const float4 a4 = *reinterpret_cast<const float4 *>(al + 4 * j4);
                                 const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
-                                for (int u = 0; u < 4; ++u) {
-                                    o[4 * j4 + u] = __float_as_uint(__uint_as_float(o[4 * j4 + u]) * av[u]);
-                                    o[32 + 4 * j4 + u] = __float_as_uint(__uint_as_float(o[32 + 4 * j4 + u]) * av[u]);
-                                }
+                                for (int c = 0; c < kPerTrip; ++c)
+#pragma unroll
+                                    for (int u4 = 0; u4 < 4; ++u4)
+                                        o[c][4 * j4 + u4] = __float_as_uint(__uint_as_float(o[c][4 * j4 + u4]) * av[u4]);
                             }
-                            tmem_st_32x32b_x16(ta, *reinterpret_cast<const uint32_t(*)[16]>(o));
-                            tmem_st_32x32b_x16(ta + 16u, *reinterpret_cast<const uint32_t(*)[16]>(o + 16));
-                            tmem_st_32x32b_x16(ta + 64u, *reinterpret_cast<const uint32_t(*)[16]>(o + 32));
-                            tmem_st_32x32b_x16(ta + 80u, *reinterpret_cast<const uint32_t(*)[16]>(o + 48));
+#pragma unroll
+                            for (int c = 0; c < kPerTrip; ++c)
+#pragma unroll
+                                for (int u = 0; u < kLd; ++u)
+                                    tmem_st_32x32b_x16(tmem + lane_addr + 256u + 64u * (c0 + c) + (uint32_t)h0 + 16u * u,
+                                                       *reinterpret_cast<const uint32_t(*)[16]>(&o[c][16 * u]));
                         }
                         tmem_wait_st();
                     }
                 }
                 uint8_t *plo = smem + OFF_PLO;
-                *reinterpret_cast<uint4 *>(plo + sw64_offset(r, 32 * hh)) = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
-                *reinterpret_cast<uint4 *>(plo + sw64_offset(r, 32 * hh + 16)) =
-                    make_uint4(wlo[4], wlo[5], wlo[6], wlo[7]);
+#pragma unroll
+                for (int u = 0; u < kV4 / 4; ++u)
+                    *reinterpret_cast<uint4 *>(plo + sw64_offset(r, h0 + 16 * u)) =
+                        make_uint4(wlo[4 * u], wlo[4 * u + 1], wlo[4 * u + 2], wlo[4 * u + 3]);
                 fence_proxy_async_smem();
                 tc_fence_before_sync();
                 mbar_arrive(&ms.p_full);
@@ -656,26 +695,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // ================================ epilogue ================================
             grid_launch_dependents();
-            if (hh == 0 && __any_sync(0xffffffffu, bad_index) && lane == 0 && a.err_word)
+            if (grp == 0 && __any_sync(0xffffffffu, bad_index) && lane == 0 && a.err_word)
                 atomicOr(a.err_word, (int)KV8_ERR_INDEX);
             if (ok && n_tiles > 0) ok = mbar_wait(&ms.pv_done, (n_tiles - 1) & 1, &ms.abort_flag, a.err_word);
             tc_fence_after_sync();
-            // row sums per head over the warp's 32 rows: butterfly transpose-reduction (as for the max,
-            // lane l ends with head l's sum), then over the 4 quadrants
-#pragma unroll
-            for (int k = 16; k >= 1; k >>= 1) {
-                const bool upper = (lane & k) != 0;
-#pragma unroll
-                for (int j = 0; j < k; ++j) {
-                    const float send = upper ? z[j] : z[j + k];
-                    const float keep = upper ? z[j + k] : z[j];
-                    z[j] = keep + __shfl_xor_sync(0xffffffffu, send, k);
-                }
+            // row sums per head: over the warp's 32 rows (the butterfly), then over the 4 quadrants
+            {
+                const float zw = warp_reduce_heads(z, false);
+                if (lane < kHG) ms.red[q][h0 + lane] = zw;
             }
-            ms.red[q][32 * hh + lane] = z[0];
             named_sync(bar_id, 128);
-            if (q == 0) {
-                const int h = 32 * hh + lane;
+            if (q == 0 && lane < kHG) {
+                const int h = h0 + lane;
                 const float zz = ms.red[0][h] + ms.red[1][h] + ms.red[2][h] + ms.red[3][h];
                 ms.ph.fin.zsum[h] = zz;
                 ms.ph.fin.zinv[h] = zz > 0.f ? ms.out_mul / zz : 0.f;
@@ -683,37 +714,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_sync(bar_id, 128);
             if (ok) {
                 const float out_mul = ms.out_mul;
-                const int hbase = half * kHeadsPerCta + 32 * hh;
                 PartialView pv(a.ws, a.B, a.P, a.H);
-                // this thread's row (dims 128c + r) of the four accumulators, 32 heads per TMEM round trip;
-                // partial sets (relative to the running max) or the normalised output
+                // this thread's row (dims 128c + r) of the four accumulators, 32 columns per TMEM round
+                // trip; partial sets (relative to the running max) or the normalised output
                 float *const dst = a.ws ? pv.cl + ((int64_t)b * a.P + part) * a.H * kKL : a.out + (int64_t)b * a.H * kKL;
+                constexpr int kPerTrip = 32 / kHG;
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t o[32];
+                for (int c0 = 0; c0 < 4; c0 += kPerTrip) {
+                    uint32_t o[kPerTrip][kHG];
                     if (n_tiles > 0) {
-                        const uint32_t ta = tmem + lane_addr + 256u + 64u * c + 32u * hh;
-                        tmem_ld_32x32b_x16(ta, *reinterpret_cast<uint32_t(*)[16]>(o));
-                        tmem_ld_32x32b_x16(ta + 16u, *reinterpret_cast<uint32_t(*)[16]>(o + 16));
+#pragma unroll
+                        for (int c = 0; c < kPerTrip; ++c)
+#pragma unroll
+                            for (int u = 0; u < kLd; ++u)
+                                tmem_ld_32x32b_x16(tmem + lane_addr + 256u + 64u * (c0 + c) + (uint32_t)h0 + 16u * u,
+                                                   *reinterpret_cast<uint32_t(*)[16]>(&o[c][16 * u]));
                         tmem_wait_ld();
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) o[j] = 0u;
-                    }
-                    float *const col = dst + 128 * c + r;
+                        for (int c = 0; c < kPerTrip; ++c)
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int hl = 32 * hh + j;  // head within the CTA
-                        const int hg = half * kHeadsPerCta + hl;
-                        if (hg < a.H) col[(int64_t)hg * kKL] = __uint_as_float(o[j]) * (a.ws ? out_mul : ms.ph.fin.zinv[hl]);
+                            for (int j = 0; j < kHG; ++j) o[c][j] = 0u;
+                    }
+#pragma unroll
+                    for (int c = 0; c < kPerTrip; ++c) {
+                        float *const col = dst + 128 * (c0 + c) + r;
+#pragma unroll
+                        for (int j = 0; j < kHG; ++j) {
+                            const int hl = h0 + j;  // head within the CTA
+                            const int hg = half * kHeadsPerCta + hl;
+                            if (hg < a.H) col[(int64_t)hg * kKL] = __uint_as_float(o[c][j]) * (a.ws ? out_mul : ms.ph.fin.zinv[hl]);
+                        }
                     }
                 }
-                if (a.ws && q == 0) {
-                    const int hg = hbase + lane;
+                if (a.ws && q == 0 && lane < kHG) {
+                    const int hg = half * kHeadsPerCta + h0 + lane;
                     if (hg < a.H) {
                         const int64_t pidx = ((int64_t)b * a.P + part) * a.H + hg;
-                        pv.m[pidx] = n_tiles > 0 ? ms.m_run[cur][32 * hh + lane] : -INFINITY;  // -inf: no valid row
-                        pv.z[pidx] = ms.ph.fin.zsum[32 * hh + lane];
+                        pv.m[pidx] = n_tiles > 0 ? ms.m_run[cur][h0 + lane] : -INFINITY;  // -inf: no valid row
+                        pv.z[pidx] = ms.ph.fin.zsum[h0 + lane];
                     }
                 }
             }
