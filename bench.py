@@ -155,10 +155,16 @@ def measured_peaks() -> dict:
 
 
 def sources_digest(paths) -> str:
+    """Digest of the code in the given sources: comments and whitespace are left out, so a traffic summary
+    stays tied to the code it measured and not to its commentary."""
+    import re
     h = hashlib.sha256()
     for p in paths:
-        with open(os.path.join(ROOT, p), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, p), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update(re.sub(r"\s+", "", text).encode())
     return h.hexdigest()[:16]
 
 

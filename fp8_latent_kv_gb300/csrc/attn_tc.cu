@@ -24,7 +24,8 @@
 // Rows reach shared memory by TMA: dense (and causal) ranges as 128-row tiles, selected rows (DSA) four
 // at a time with tile::gather4 from a tensor map over all items' caches.
 //
-// Warps: 0 = TMA producer, 1 = MMA issuer (and TMEM owner), 2..9 = softmax / epilogue.
+// Warps: 0 = TMA producer, 1 = MMA issuer (and TMEM owner), 2..17 = softmax / epilogue in four groups of
+// four warps (one per TMEM lane quadrant), each group owning 16 of the CTA's 64 heads.
 // Shared memory (231 KB): query image 72 KB, two 72 KB row stages (the weights' hi piece reuses the
 // stage's rope block once the score has read it), weights' lo piece 8 KB, barriers and scratch.
 // TMEM (512 columns): two 128-column score buffers (hi / lo query pieces side by side), four 64-column
@@ -138,7 +139,7 @@ __device__ __forceinline__ void split_pair(float a, float b, uint32_t &hi, uint3
     lo = enc_pair(a - h.x, b - h.y);
 }
 
-// 10 warps: a sub-partition holding 3 warps caps a thread at 168 registers (16K registers each).
+// 18 warps: a sub-partition holding 5 warps caps a thread at 96 registers (16K registers each).
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap map_lc, const __grid_constant__ CUtensorMap map_rc, TcArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
