@@ -288,7 +288,7 @@ KV8_API int mla_out_project8(const float *ctx, int S, int H, const uint8_t *w8, 
  *   k8 [rows][128] e4m3 and k_scale [rows] f32 as written by kv8_quant_rows_w(width = KV8_IDX_D).
  *   scores [B][T] f32 (written: I); idx [B][NS] int32 (written): the min(NS, T) positions with the
  *   largest scores, the smaller position first among equal scores, in ascending position order -- the
- *   selection list mla_absorb_sel8 takes.
+ *   selection list mla_absorb_sel8 takes.  When NS > T, idx[b][T..NS-1] is left as it was.
  *   HI a multiple of 16 in [16, KV8_MAX_IDX_HEADS]; T in [1, KV8_MAX_ROWS]; NS in [1, KV8_MAX_SELECT];
  *   seq_stride_rows >= 0 and (B-1)*seq_stride_rows + T < 2^31 - 128; buffers 16-byte aligned.
  *   workspace: >= dsa_index_workspace_bytes(B) bytes (the top-k's histograms and the barrier counters of
