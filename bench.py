@@ -866,6 +866,17 @@ ORACLE_HEADS = {"dec262k": 32, "dec16k": 128, "dsa": 128, "prefill": 8, "proj_de
                 "indexer": 1, "batch_dec": 16, "mixed_dec": 32}
 REFERENCE_HEADS = {"dec262k": 8, "dec16k": 32, "dsa": 32, "prefill": 4, "proj_dec": 1, "proj_prefill": 16,
                    "indexer": 1, "batch_dec": 4, "mixed_dec": 8}
+# workloads whose oracle sample is a set of heads (the oracle runs one thread per head, or per (query,
+# head)): the reference arm samples at least as many heads as the oracle has threads, so its per-head
+# rate is that of a full host
+HEAD_SAMPLED = {"dec262k", "dec16k", "dsa", "prefill", "batch_dec", "mixed_dec"}
+
+
+def reference_sample(key: str, w, threads: int) -> int:
+    n = REFERENCE_HEADS[key]
+    if key in HEAD_SAMPLED:
+        n = min(w.H, max(n, threads))
+    return n
 
 
 def SM_SCALE():
@@ -883,11 +894,46 @@ def metric_for(key: str) -> str:
 # --------------------------------------------------------------------------------------------------
 # CPU baseline: the oracle as it stands, on a bounded sample of the workload
 # --------------------------------------------------------------------------------------------------
-def cpu_baseline(case: Case, n_heads: int) -> dict:
+def cpu_baseline(case: Case, n_heads: int, key: str = "") -> dict:
     import oracle
     sample = case.oracle_setup(n_heads)
     t_us = case.oracle_step() * 1e6
-    return {"value": t_us, "unit": case.unit, "cores": oracle.num_threads(), "kind": "oracle", "sample": sample}
+    out = {"value": t_us, "unit": case.unit, "cores": oracle.num_threads(), "kind": "oracle", "sample": sample}
+    if key in ("dec262k", "dec16k"):
+        out["single_thread"] = single_thread_decode_baselines()
+    return out
+
+
+# heads timed single-threaded per decode workload (scaled by heads to the whole step)
+SINGLE_THREAD_HEADS = {"tiny": 16, "dec16k": 8, "dec262k": 1}
+
+
+def single_thread_decode_baselines() -> dict:
+    """The oracle on ONE host thread for the three decode workloads (tiny, dec16k, dec262k), each on a
+    bounded sample of heads over all rows, scaled by heads to one layer-step."""
+    import oracle
+    import synth
+    threads = oracle.num_threads()
+    res = {}
+    try:
+        for key, nh in SINGLE_THREAD_HEADS.items():
+            w = synth.WORKLOADS[key]
+            rows = synth.rows_for(w)
+            oracle.set_num_threads(threads)      # set-up (the cache bytes) on all threads, untimed
+            q_o, s_o = oracle.quant_rows(rows)
+            oracle.set_num_threads(1)
+            ql, qr = synth.queries_for(w, 1)
+            heads = np.linspace(0, w.H - 1, nh).astype(int)
+            qls, qrs = np.ascontiguousarray(ql[0][heads]), np.ascontiguousarray(qr[0][heads])
+            t0 = time.perf_counter()
+            oracle.quant_rows(rows[-1:])
+            oracle.attn_decode(qls, qrs, q_o, s_o, synth.SM_SCALE)
+            dt = (time.perf_counter() - t0) * w.H / nh
+            res[key] = {"value": dt * 1e6, "unit": "us/layer-step", "cores": 1,
+                        "sample": f"{nh} of {w.H} heads over all T={w.T} rows, scaled x{w.H / nh:g}"}
+    finally:
+        oracle.set_num_threads(threads)
+    return res
 
 
 def host_case(key: str):
@@ -914,7 +960,7 @@ def run_reference(args, rank, world):
     oracle.build()
     key = args.workload
     case = host_case(key)
-    sample = case.oracle_setup(REFERENCE_HEADS[key])
+    sample = case.oracle_setup(reference_sample(key, case.w, oracle.num_threads()))
     for _ in range(args.warmup):
         case.oracle_step()
     t0 = time.perf_counter()
@@ -1013,6 +1059,49 @@ def run_ours(args, rank, world, local_rank):
     ms_per_step = reduce_max(statistics.mean(step_ms), dev)
     kern_ms_mean = reduce_max(statistics.mean(kern_ms), dev)
 
+    # ---- the same steps without the L2 flush (a workload whose rows fit in L2 then reads them from L2)
+    warm_ms = []
+    for k in range(args.steps):
+        e0, e1 = E(), E()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g_step.replay()
+            e1.record(stream)
+        e1.synchronize()
+        warm_ms.append(e0.elapsed_time(e1))
+    warm_ms_mean = reduce_max(statistics.mean(warm_ms), dev)
+
+    # ---- clock soak: >= 1 s of back-to-back step replays with the clocks sampled throughout
+    soak = None
+    if rank == 0 and not args.no_soak:
+        # replays are enqueued in batches until at least 1.1 s of GPU time has passed
+        batch = max(10, int(0.1 / max(ms_per_step * 1e-3, 1e-6)) + 1)
+        sampler = ClockSampler(local_rank)
+        sampler.start()
+        s0, s1 = E(), E()
+        n_soak = 0
+        with torch.cuda.stream(stream):
+            s0.record(stream)
+            while True:
+                for _ in range(batch):
+                    g_step.replay()
+                n_soak += batch
+                s1.record(stream)
+                s1.synchronize()
+                if s0.elapsed_time(s1) >= 1100.0:
+                    break
+        s1.synchronize()
+        sclk = sampler.stop()
+        soak_ms = s0.elapsed_time(s1)
+        us_soak = soak_ms * 1e3 / n_soak
+        soak = {"seconds": soak_ms / 1e3, "steps": n_soak, "us_per_step": us_soak,
+                "sm_mhz_median": sclk.get("sm_mhz"), "sm_max_mhz": sclk.get("sm_max_mhz"),
+                "reasons": sclk.get("reasons"), "samples": sclk.get("samples"),
+                "power_w_max": sclk.get("power_w_max"),
+                "cycles_per_step": us_soak * sclk["sm_mhz"] if sclk.get("sm_mhz") else None,
+                "how": "step graph replayed back to back (no L2 flush) for >= 1 s; cycles = us x median SM MHz"}
+    barrier()
+
     # ---- end to end through the C ABI with host buffers: inputs in, output out, every step; as a
     # replayed graph of the same calls, and as direct calls (each paying the host's launch cost)
     def timed(fn):
@@ -1037,7 +1126,7 @@ def run_ours(args, rank, world, local_rank):
     roof = case.roofline(kern_ms_mean / 1e3, peaks, key)
 
     n_heads = ORACLE_HEADS[key]
-    base = cpu_baseline(case, n_heads) if (world == 1 and not args.no_cpu_baseline) else None
+    base = cpu_baseline(case, n_heads, key) if (world == 1 and not args.no_cpu_baseline) else None
     value = whole_job_us_per_step(ms_per_step, world)
     cfg = {"workload": synth.DESCRIPTIONS[key]}
     cfg.update(case.config())
@@ -1057,6 +1146,9 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": case.launches_per_step * args.steps,
         "roofline": roof,
         "clocks": {k: clk.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples", "power_w_max")},
+        "warm_l2": {"value": whole_job_us_per_step(warm_ms_mean, world), "unit": case.unit,
+                    "how": "the same step replays without the L2 flush before each step"},
+        "clock_soak": soak,
         "wall_s_timed_region": wall_s,
     }
     if base is not None:
@@ -1071,6 +1163,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
+    ap.add_argument("--no-soak", action="store_true", help="skip the 1 s clock soak (profiling runs)")
     ap.add_argument("--workload", choices=sorted(CASES), default="dec262k",
                     help="dec262k (default: the headline decode step), dec16k, dsa or prefill")
     args = ap.parse_args(argv)

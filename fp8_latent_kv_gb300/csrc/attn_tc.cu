@@ -490,9 +490,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
             const int bar_id = 2 + grp;
             const float w_mul = ms.w_mul;
-            float z[kHG];
+            constexpr int kP = kHG / 2;  // head pairs (f32x2 lanes)
+            uint64_t z2[kP];             // row sums per head pair, relative to the heads' references
 #pragma unroll
-            for (int j = 0; j < kHG; ++j) z[j] = 0.f;
+            for (int j = 0; j < kP; ++j) z2[j] = f2_pack(0.f, 0.f);
             // scale of the row at list position pos, or -1 if that row is masked (past the end, or an
             // index outside [0, T), which is also reported)
             bool bad_index = false;
@@ -543,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 if (ok) ok = mbar_wait(&ms.s_full[bb], (i >> 1) & 1, &ms.abort_flag, a.err_word);
                 tc_fence_after_sync();
-                float sc_[kHG];  // S = hi piece + lo piece, one TMEM round trip
+                uint64_t s2[kP];  // S = hi piece + lo piece (one TMEM round trip), head pairs packed
                 {
                     uint32_t shi[kLd][16], slo[kLd][16];
                     const uint32_t ta = tmem + lane_addr + (uint32_t)bb * 128u + (uint32_t)h0;
@@ -554,29 +555,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < kHG; ++j) sc_[j] = __uint_as_float(shi[j >> 4][j & 15]) + __uint_as_float(slo[j >> 4][j & 15]);
+                    for (int j = 0; j < kP; ++j) {
+                        const int a0 = 2 * j, a1 = 2 * j + 1;
+                        s2[j] = f2_add(f2_pack(__uint_as_float(shi[a0 >> 4][a0 & 15]), __uint_as_float(shi[a1 >> 4][a1 & 15])),
+                                       f2_pack(__uint_as_float(slo[a0 >> 4][a0 & 15]), __uint_as_float(slo[a1 >> 4][a1 & 15])));
+                    }
                 }
                 tc_fence_before_sync();
                 mbar_arrive(&ms.s_free[bb]);
 
-                // d = s - ref with s = S * sm_scale*log2(e)*2^-e_h * s_t (one FMA per score); ref is the
-                // running max, or 0 before any valid row
-                float d[kHG];
+                // d = s - ref with s = S * sm_scale*log2(e)*2^-e_h * s_t (the factor is rounded once, then
+                // one fused multiply-add per score); ref is the running max, or 0 before any valid row
+                uint64_t d2[kP];
                 float dmax = -INFINITY;
-                const float *mref = &ms.m_ref[cur][h0];
+                {
+                    const float *mref = &ms.m_ref[cur][h0];
+                    const uint64_t st2 = f2_pack(sc_t, sc_t);
 #pragma unroll
-                for (int j4 = 0; j4 < kV4; ++j4) {
-                    const float4 c4 = *reinterpret_cast<const float4 *>(&ms.c_head[h0 + 4 * j4]);
-                    const float4 r4 = *reinterpret_cast<const float4 *>(mref + 4 * j4);
-                    d[4 * j4 + 0] = fmaf(sc_[4 * j4 + 0], c4.x * sc_t, -r4.x);
-                    d[4 * j4 + 1] = fmaf(sc_[4 * j4 + 1], c4.y * sc_t, -r4.y);
-                    d[4 * j4 + 2] = fmaf(sc_[4 * j4 + 2], c4.z * sc_t, -r4.z);
-                    d[4 * j4 + 3] = fmaf(sc_[4 * j4 + 3], c4.w * sc_t, -r4.w);
-                    dmax = fmaxf(dmax, fmaxf(fmaxf(d[4 * j4 + 0], d[4 * j4 + 1]), fmaxf(d[4 * j4 + 2], d[4 * j4 + 3])));
+                    for (int j4 = 0; j4 < kV4; ++j4) {
+                        const float4 c4 = *reinterpret_cast<const float4 *>(&ms.c_head[h0 + 4 * j4]);
+                        const float4 r4 = *reinterpret_cast<const float4 *>(mref + 4 * j4);
+                        d2[2 * j4] = f2_fma(s2[2 * j4], f2_mul(f2_pack(c4.x, c4.y), st2), f2_pack(-r4.x, -r4.y));
+                        d2[2 * j4 + 1] = f2_fma(s2[2 * j4 + 1], f2_mul(f2_pack(c4.z, c4.w), st2), f2_pack(-r4.z, -r4.w));
+                        float a, b, c, e;
+                        f2_unpack(d2[2 * j4], a, b);
+                        f2_unpack(d2[2 * j4 + 1], c, e);
+                        dmax = fmaxf(dmax, fmaxf(fmaxf(a, b), fmaxf(c, e)));
+                    }
                 }
                 if (!valid) {
 #pragma unroll
-                    for (int j = 0; j < kHG; ++j) d[j] = -INFINITY;
+                    for (int j = 0; j < kP; ++j) d2[j] = f2_pack(-INFINITY, -INFINITY);
                     dmax = -INFINITY;
                 }
                 // lazy rescale: the group takes the slow path when some score exceeds its head's running
@@ -584,13 +593,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool slow = bar_red_or(bar_id, 128, dmax > kTau || !seen);
                 bool any_alpha = false;
                 if (slow) {
-                    float v[kHG];
+                    // per-head maxima over this warp's 32 rows (one warp reduction per head), then over the
+                    // group's four lane quadrants through shared memory
+                    float hm[kHG];
 #pragma unroll
-                    for (int j = 0; j < kHG; ++j) v[j] = d[j];
-                    const float vmax = warp_reduce_heads(v, true);  // this warp's 32 rows, head lane % kHG
+                    for (int j = 0; j < kP; ++j) {
+                        float a, b;
+                        f2_unpack(d2[j], a, b);
+                        hm[2 * j] = warp_redux_max(a);
+                        hm[2 * j + 1] = warp_redux_max(b);
+                    }
+                    if (lane == 0) {
+#pragma unroll
+                        for (int j4 = 0; j4 < kV4; ++j4)
+                            *reinterpret_cast<float4 *>(&ms.red[q][h0 + 4 * j4]) =
+                                make_float4(hm[4 * j4], hm[4 * j4 + 1], hm[4 * j4 + 2], hm[4 * j4 + 3]);
+                    }
                     const int hl = lane & (kHG - 1);
                     const int hj = h0 + hl;
-                    if (lane < kHG) ms.red[q][hj] = vmax;
                     named_sync(bar_id, 128);
                     const float ref_o = ms.m_ref[cur][hj], mo = ms.m_run[cur][hj];
                     const float tmax = fmaxf(fmaxf(ms.red[0][hj], ms.red[1][hj]), fmaxf(ms.red[2][hj], ms.red[3][hj])) + ref_o;
@@ -611,31 +631,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j4 = 0; j4 < kV4; ++j4) {
                         const float4 a4 = *reinterpret_cast<const float4 *>(&ms.ph.tile.alpha[grp][4 * j4]);
                         const float4 e4 = *reinterpret_cast<const float4 *>(&ms.ph.tile.delta[grp][4 * j4]);
-                        d[4 * j4 + 0] += e4.x;
-                        d[4 * j4 + 1] += e4.y;
-                        d[4 * j4 + 2] += e4.z;
-                        d[4 * j4 + 3] += e4.w;
-                        z[4 * j4 + 0] *= a4.x;
-                        z[4 * j4 + 1] *= a4.y;
-                        z[4 * j4 + 2] *= a4.z;
-                        z[4 * j4 + 3] *= a4.w;
+                        d2[2 * j4] = f2_add(d2[2 * j4], f2_pack(e4.x, e4.y));
+                        d2[2 * j4 + 1] = f2_add(d2[2 * j4 + 1], f2_pack(e4.z, e4.w));
+                        z2[2 * j4] = f2_mul(z2[2 * j4], f2_pack(a4.x, a4.y));
+                        z2[2 * j4 + 1] = f2_mul(z2[2 * j4 + 1], f2_pack(a4.z, a4.w));
                     }
                     cur ^= 1;
                 }
                 // weights: p = 2^d (row sum z), w = p * s_t * kWScale / s_ref, split e4m3 hi + lo
                 const float g = valid ? sc_t * w_mul : 0.f;
+                const uint64_t g2 = f2_pack(g, g);
                 uint32_t whi[kV4], wlo[kV4];
 #pragma unroll
                 for (int j4 = 0; j4 < kV4; ++j4) {
-                    const float p0 = ex2_approx(d[4 * j4 + 0]), p1 = ex2_approx(d[4 * j4 + 1]);
-                    const float p2 = ex2_approx(d[4 * j4 + 2]), p3 = ex2_approx(d[4 * j4 + 3]);
-                    z[4 * j4 + 0] += p0;
-                    z[4 * j4 + 1] += p1;
-                    z[4 * j4 + 2] += p2;
-                    z[4 * j4 + 3] += p3;
+                    float d0, d1, e0, e1;
+                    f2_unpack(d2[2 * j4], d0, d1);
+                    f2_unpack(d2[2 * j4 + 1], e0, e1);
+                    const uint64_t p01 = f2_pack(ex2_approx(d0), ex2_approx(d1));
+                    const uint64_t p23 = f2_pack(ex2_approx(e0), ex2_approx(e1));
+                    z2[2 * j4] = f2_add(z2[2 * j4], p01);
+                    z2[2 * j4 + 1] = f2_add(z2[2 * j4 + 1], p23);
+                    float w0, w1, w2, w3;
+                    f2_unpack(f2_mul(p01, g2), w0, w1);
+                    f2_unpack(f2_mul(p23, g2), w2, w3);
                     uint32_t h01, l01, h23, l23;
-                    split_pair_h(p0 * g, p1 * g, h01, l01);
-                    split_pair_h(p2 * g, p3 * g, h23, l23);
+                    split_pair_h(w0, w1, h01, l01);
+                    split_pair_h(w2, w3, h23, l23);
                     whi[j4] = h01 | (h23 << 16);
                     wlo[j4] = l01 | (l23 << 16);
                 }
@@ -667,12 +688,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int j4 = 0; j4 < kV4; ++j4) {
                                 const float4 a4 = *reinterpret_cast<const float4 *>(al + 4 * j4);
-                                const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+                                const uint64_t a01 = f2_pack(a4.x, a4.y), a23 = f2_pack(a4.z, a4.w);
 #pragma unroll
-                                for (int c = 0; c < kPerTrip; ++c)
-#pragma unroll
-                                    for (int u4 = 0; u4 < 4; ++u4)
-                                        o[c][4 * j4 + u4] = __float_as_uint(__uint_as_float(o[c][4 * j4 + u4]) * av[u4]);
+                                for (int c = 0; c < kPerTrip; ++c) {
+                                    uint32_t *oc = &o[c][4 * j4];
+                                    float x0, x1, x2, x3;
+                                    f2_unpack(f2_mul(f2_pack(__uint_as_float(oc[0]), __uint_as_float(oc[1])), a01), x0, x1);
+                                    f2_unpack(f2_mul(f2_pack(__uint_as_float(oc[2]), __uint_as_float(oc[3])), a23), x2, x3);
+                                    oc[0] = __float_as_uint(x0);
+                                    oc[1] = __float_as_uint(x1);
+                                    oc[2] = __float_as_uint(x2);
+                                    oc[3] = __float_as_uint(x3);
+                                }
                             }
 #pragma unroll
                             for (int c = 0; c < kPerTrip; ++c)
@@ -702,6 +729,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
             // row sums per head: over the warp's 32 rows (the butterfly), then over the 4 quadrants
             {
+                float z[kHG];
+#pragma unroll
+                for (int j = 0; j < kP; ++j) f2_unpack(z2[j], z[2 * j], z[2 * j + 1]);
                 const float zw = warp_reduce_heads(z, false);
                 if (lane < kHG) ms.red[q][h0 + lane] = zw;
             }

@@ -6,29 +6,22 @@
 // requests whose partials do not fit are refused.  Calls that overlap on the GPU race on the array.
 #include "internal.h"
 
-#include <mutex>
-
 namespace {
 
 // One copy per device, resident from module load until the process exits.  Host code must not use
 // this name as a pointer: its device address comes from cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[KV8_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 128;
-std::mutex g_mu;
-void *g_scratch_addr[kMaxDevices];  // device address of g_noalloc_scratch per device; null until looked up
-
-// Device address of the array on the current device.  The first call on a device looks it up.
+// Device address of the array in the current device's context, looked up on every call: a context
+// that was destroyed and created again (cudaDeviceReset) reloads the module, possibly at another
+// address, so no address is kept between calls.  The first lookup in a context loads the module.
 int scratch_address(void **out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KV8_ECUDA;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (g_scratch_addr[dev] == nullptr) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return KV8_ECUDA;
-        g_scratch_addr[dev] = p;
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+        (void)cudaGetLastError();
+        return KV8_ECUDA;
     }
-    *out = g_scratch_addr[dev];
+    *out = p;
     return KV8_OK;
 }
 

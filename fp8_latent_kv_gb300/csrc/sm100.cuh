@@ -267,6 +267,40 @@ __device__ __forceinline__ bool bar_red_or(int id, int count, bool v) {
     return r != 0;
 }
 
+// Packed pairs of f32 (two lanes of one 64-bit register pair) and the sm_100-family f32x2 arithmetic:
+// each instruction rounds both halves exactly as the scalar instruction would.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Maximum of v over the 32 lanes of the warp, returned to every lane (exact; a NaN input is ignored
+// unless every input is NaN).
+__device__ __forceinline__ float warp_redux_max(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
 // 2^x by the hardware approximation (MUFU.EX2; subnormal results flush to 0, 2^-inf = 0)
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;

@@ -195,16 +195,20 @@ KV8_API int mla_absorb_prefill8(const void *q_lat, const void *q_rope, int q_dty
  * or a latency-critical loop that must not take cudaMalloc's implicit device synchronisation.
  * This entry point keeps the partials in a fixed array of KV8_NOALLOC_SCRATCH_BYTES that is part of
  * the library's device image: every GPU that loads the library holds it until the process exits.
- * Neither this call nor anything it calls allocates memory.
+ * Apart from that module load (below), neither this call nor anything it calls allocates memory.
  *
  * Arguments as mla_absorb_decode8, without workspace / ws_bytes.  P_req == 0 picks the automatic
  * partition count, lowered if needed until the partials fit the array; an explicit P_req whose
  * partials do not fit returns KV8_EWORKSPACE (nothing is enqueued).
- * The first call on each device (with that device current) looks up the array's device address;
- * make that first call before any stream capture.  All calls share the one array and it keeps the
- * last call's contents (each call writes every partial it reads, so nothing needs clearing):
- * calls whose kernels overlap on the GPU (two streams, or two host threads) race on it and must be
- * ordered by the caller.
+ * Every call looks up the array's address in the current device's context (a cheap host query; no
+ * address is kept between calls, so a context that was reset and created again is handled).  The
+ * first call in a context also loads the library's device module, which places the array: that step
+ * can allocate device memory and synchronise, and it fails with KV8_ECUDA if the device has no room
+ * left.  A caller whose memory pool takes the whole GPU should therefore make one warm-up call per
+ * device at set-up time, before the pool grows and before any stream capture.
+ * All calls share the one array and it keeps the last call's contents (each call writes every
+ * partial it reads, so nothing needs clearing): calls whose kernels overlap on the GPU (two streams,
+ * or two host threads) race on it and must be ordered by the caller.
  * --------------------------------------------------------------------------------------------- */
 #define KV8_NOALLOC_SCRATCH_BYTES (16u << 20) /* 16 MiB per device */
 KV8_API int mla_absorb_decode8_noalloc(const void *q_lat, const void *q_rope, int q_dtype, int H,
