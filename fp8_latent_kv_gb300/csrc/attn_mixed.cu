@@ -677,11 +677,12 @@ __global__ void __launch_bounds__(kMxPrepThreads) mixed_prep_kernel(MxPrepArgs a
 }  // namespace
 
 int mixed_partitions(int H, int64_t T) {
-    // one wave of tensor-core CTAs (one per SM of a 152-SM part: a CTA per partition and 64-head half),
-    // at least 128 rows per partition
-    const int64_t cap = H > kHeads ? 76 : 152;
+    // one wave of tensor-core CTAs on the current device (one per SM: a CTA per partition and 64-head
+    // half), at least 128 rows per partition
+    const int64_t sms = device_sm_count();
+    const int64_t cap = H > kHeads ? sms / 2 : sms;
     const int64_t p = (T + kTile - 1) / kTile;
-    return (int)(p < cap ? p : cap);
+    return (int)(p < cap ? p : (cap < 1 ? 1 : cap));
 }
 
 size_t mixed_scratch_bytes(int H, int P) {

@@ -18,8 +18,12 @@
 //   softmax one thread per tile row (TMEM lane); online max with a lazy rescale (only when a head's
 //           max grows by more than kTau); weights w = 2^(s - m) * s_t / s_ref * 2^(8-kTau), split into
 //           e4m3 hi + lo the same way.
-//   context O^T[d][h]  += sum_t  V8[t][d] * W^T[t][h]        M = 128 dims (x4 chunks), N = 64, K = 128 rows
-//           A = the same cache bytes read MN-major (V^T), B = the weights MN-major.
+//   context O^T[d][n]  += sum_t  V8[t][d] * W^T[t][n]        M = 128 dims (x4 chunks), K = 128 rows
+//           A = the same cache bytes read MN-major (V^T), B = the weights MN-major.  Dims 0..255 take
+//           the hi and lo weights side by side (N = 128, one accumulator column per head and piece,
+//           summed at the end); dims 256..511 add both pieces into one accumulator (two N = 64 passes).
+//           An MMA reading A MN-major costs about the same at N = 64 as at N = 128, so the wide passes
+//           halve the first two chunks' tensor time; TMEM has room for two of them.
 //
 // Rows reach shared memory by TMA: dense (and causal) ranges as 128-row tiles, selected rows (DSA) four
 // at a time with tile::gather4 from a tensor map over all items' caches.
@@ -28,8 +32,8 @@
 // four warps (one per TMEM lane quadrant), each group owning 16 of the CTA's 64 heads.
 // Shared memory (231 KB): query image 72 KB, two 72 KB row stages (the weights' hi piece reuses the
 // stage's rope block once the score has read it), weights' lo piece 8 KB, barriers and scratch.
-// TMEM (512 columns): two 128-column score buffers (hi / lo query pieces side by side), four 64-column
-// context accumulators.
+// TMEM (512 columns): one 128-column score buffer (hi / lo query pieces side by side), then six 64-column
+// context accumulators: dims 0..127 hi, lo; dims 128..255 hi, lo; dims 256..383; dims 384..511.
 // Every mbarrier wait is bounded in time; a timeout sets KV8_ERR_TIMEOUT.  The softmax warps then skip
 // their remaining waits but still pass every named barrier of every tile, so the CTA winds down without
 // hanging.
@@ -61,6 +65,9 @@ constexpr uint32_t kRcOff = 65536;     // rope block inside an image / stage
 constexpr uint32_t OFF_Q = 0, OFF_ST0 = kImg, OFF_ST1 = 2 * kImg, OFF_PLO = 3 * kImg, OFF_MISC = 3 * kImg + 8192;
 constexpr float kTau = 2.0f;           // lazy-rescale threshold (log2 units): p <= 2^kTau
 constexpr float kWScale = 64.0f;       // 2^(8 - kTau): keeps w <= 256 < 448 (e4m3 max)
+constexpr uint32_t TM_S = 0;           // score: columns 0..63 hi piece, 64..127 lo piece
+constexpr uint32_t TM_O = 128;         // context piece k (0..5) at TM_O + 64k, see the header
+constexpr int kOPieces = 6;
 
 struct Misc {
     // per-head arrays first: they are read with 16-byte vector loads.  m_run / m_ref have two copies;
@@ -83,7 +90,8 @@ struct Misc {
             float zinv[kHeadsPerCta];          // and the direct output's factors s_ref / kWScale / zsum
         } fin;
     } ph;
-    uint64_t kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, pv_done, final_bar, q_full;
+    uint64_t kv_full[2], kv_empty[2], s_full, s_free, p_full, lo_free, final_bar, q_full;
+    uint64_t pv_done[2];    // context product of a tile of that parity done (one phase per two tiles)
     uint64_t kv_blk[2][4];  // latent block kb of a stage has been read by the context product
     uint32_t tmem_base;
     int abort_flag;
@@ -170,11 +178,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&ms.kv_full[s], 1);
             mbar_init(&ms.kv_empty[s], 1);
             for (int kb = 0; kb < 4; ++kb) mbar_init(&ms.kv_blk[s][kb], 1);
-            mbar_init(&ms.s_full[s], 1);
-            mbar_init(&ms.s_free[s], kSoftmaxThreads);
+            mbar_init(&ms.pv_done[s], 1);
         }
+        mbar_init(&ms.s_full, 1);
+        mbar_init(&ms.s_free, kSoftmaxThreads);
         mbar_init(&ms.p_full, kSoftmaxThreads);
-        mbar_init(&ms.pv_done, 1);
+        mbar_init(&ms.lo_free, 1);
         mbar_init(&ms.final_bar, 1);
         mbar_init(&ms.q_full, 1);
         ms.abort_flag = 0;
@@ -398,6 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 const uint32_t id_s = idesc_e4m3_f32(128, 128, false, false);
                 const uint32_t id_pv = idesc_e4m3_f32(128, 64, true, true);
+                const uint32_t id_pw = idesc_e4m3_f32(128, 128, true, true);
                 const uint32_t qb = sbase + OFF_Q;
                 auto issue_score = [&](int i) {
                     const int s = i & 1;
@@ -405,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // S^T = K8 [Q_hi; Q_lo]^T in one N = 128 pass: columns 0..63 hold the hi piece's
                     // scores, 64..127 the lo piece's (one pass reads the rows once; two N = 64 passes
                     // into one accumulator take about 60% longer on the tensor cores)
-                    const uint32_t d = tmem + (uint32_t)s * 128u;
+                    const uint32_t d = tmem + TM_S;
 #pragma unroll
                     for (int kb = 0; kb < 4; ++kb)
 #pragma unroll
@@ -416,29 +426,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int kk = 0; kk < 2; ++kk)
                         mma_f8f6f4(d, smem_desc(st + kRcOff + kk * 32, 0, 512, kSw64),
                                    smem_desc(qb + kRcOff + kk * 32, 0, 512, kSw64), id_s, 1);
-                    mma_commit(&ms.s_full[s]);
+                    mma_commit(&ms.s_full);
                 };
                 auto issue_pv = [&](int j) {
                     const int s = j & 1;
                     const uint32_t st = sbase + (s ? OFF_ST1 : OFF_ST0);
                     const uint32_t phi = st + kRcOff, plo = sbase + OFF_PLO;
+                    // dims 0..255: B = 128 columns, the hi piece's 64 heads then the lo piece's (MN-major,
+                    // 64-byte swizzle atoms; the second atom along N sits at the leading-byte offset)
+                    const uint32_t lbo = plo - phi;
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        const uint32_t d = tmem + 256u + (uint32_t)ch * 64u;
+                    for (int ch = 0; ch < 2; ++ch) {
+                        const uint32_t d = tmem + TM_O + 128u * (uint32_t)ch;
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t ad = smem_desc(st + ch * 16384 + kk * 4096, 0, 1024, kSw128);
-                            mma_f8f6f4(d, ad, smem_desc(phi + kk * 2048, 0, 512, kSw64), id_pv, (j | kk) != 0);
-                            mma_f8f6f4(d, ad, smem_desc(plo + kk * 2048, 0, 512, kSw64), id_pv, 1);
-                        }
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_f8f6f4(d, smem_desc(st + ch * 16384 + kk * 4096, 0, 1024, kSw128),
+                                       smem_desc(phi + kk * 2048, lbo, 512, kSw64), id_pw, (j | kk) != 0);
                         mma_commit(&ms.kv_blk[s][ch]);  // latent block ch may be refilled
                     }
+                    // dims 256..511: the lo piece's passes first, so that the next tile's softmax may
+                    // overwrite the lo buffer while the hi passes run
+#pragma unroll
+                    for (int ch = 2; ch < 4; ++ch)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_f8f6f4(tmem + TM_O + 64u * (uint32_t)(ch + 2),
+                                       smem_desc(st + ch * 16384 + kk * 4096, 0, 1024, kSw128),
+                                       smem_desc(plo + kk * 2048, 0, 512, kSw64), id_pv, (j | kk) != 0);
+                    mma_commit(&ms.lo_free);
+#pragma unroll
+                    for (int ch = 2; ch < 4; ++ch) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_f8f6f4(tmem + TM_O + 64u * (uint32_t)(ch + 2),
+                                       smem_desc(st + ch * 16384 + kk * 4096, 0, 1024, kSw128),
+                                       smem_desc(phi + kk * 2048, 0, 512, kSw64), id_pv, 1);
+                        mma_commit(&ms.kv_blk[s][ch]);
+                    }
                     mma_commit(&ms.kv_empty[s]);
-                    mma_commit(&ms.pv_done);
+                    mma_commit(&ms.pv_done[s]);
                 };
                 // Issue whichever is ready, the context product first: it releases the row stage for
-                // the next load.  Score i needs tile i loaded and score buffer i%2 read by the softmax
-                // (tile i-2); PV j needs the weights of tile j.
+                // the next load.  Score i needs tile i loaded and the score buffer read by the softmax
+                // of tile i-1; PV j needs the weights of tile j.
                 int ns = 0, np = 0;
                 if (a.qimg && n_tiles > 0 && !mbar_wait(&ms.q_full, 0, &ms.abort_flag, a.err_word)) np = n_tiles;
                 const uint64_t t_start = globaltimer_ns();
@@ -452,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         continue;
                     }
                     if (ns < n_tiles && mbar_test_wait(&ms.kv_full[ns & 1], (ns >> 1) & 1) &&
-                        (ns < 2 || mbar_test_wait(&ms.s_free[ns & 1], ((ns >> 1) - 1) & 1))) {
+                        (ns == 0 || mbar_test_wait(&ms.s_free, (ns - 1) & 1))) {
                         tc_fence_after_sync();
                         issue_score(ns++);
                         spins = 0;
@@ -542,12 +572,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool valid = sc_t >= 0.f;
                 sc_next = i + 1 < n_tiles ? row_scale(t + kTile) : -1.f;
 
-                if (ok) ok = mbar_wait(&ms.s_full[bb], (i >> 1) & 1, &ms.abort_flag, a.err_word);
+                if (ok) ok = mbar_wait(&ms.s_full, i & 1, &ms.abort_flag, a.err_word);
                 tc_fence_after_sync();
                 uint64_t s2[kP];  // S = hi piece + lo piece (one TMEM round trip), head pairs packed
                 {
                     uint32_t shi[kLd][16], slo[kLd][16];
-                    const uint32_t ta = tmem + lane_addr + (uint32_t)bb * 128u + (uint32_t)h0;
+                    const uint32_t ta = tmem + lane_addr + TM_S + (uint32_t)h0;
 #pragma unroll
                     for (int u = 0; u < kLd; ++u) {
                         tmem_ld_32x32b_x16(ta + 16u * u, shi[u]);
@@ -562,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 tc_fence_before_sync();
-                mbar_arrive(&ms.s_free[bb]);
+                mbar_arrive(&ms.s_free);
 
                 // d = s - ref with s = S * sm_scale*log2(e)*2^-e_h * s_t (the factor is rounded once, then
                 // one fused multiply-add per score); ref is the running max, or 0 before any valid row
@@ -666,22 +696,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<uint4 *>(phi + sw64_offset(r, h0 + 16 * u)) =
                         make_uint4(whi[4 * u], whi[4 * u + 1], whi[4 * u + 2], whi[4 * u + 3]);
                 if (i >= 1) {
-                    // the previous context product must be done before its weights' lo buffer is reused
-                    // and before its accumulators are rescaled
-                    if (ok) ok = mbar_wait(&ms.pv_done, (i - 1) & 1, &ms.abort_flag, a.err_word);
+                    // the previous context product must have read its weights' lo buffer before it is
+                    // reused, and be done before its accumulators are rescaled.  lo_free is waited on every
+                    // tile; pv_done only on a rescale, so it has one barrier per tile parity: the phase
+                    // before the awaited one (tile i-3) is complete, which keeps the parity unambiguous.
+                    if (ok) ok = mbar_wait(&ms.lo_free, (i - 1) & 1, &ms.abort_flag, a.err_word);
                     if (any_alpha) {
-                        // rescale this group's columns of the four context accumulators, 32 columns per
+                        if (ok) ok = mbar_wait(&ms.pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, &ms.abort_flag, a.err_word);
+                        // rescale this group's columns of the six context accumulators, 32 columns per
                         // TMEM round trip
                         tc_fence_after_sync();
                         constexpr int kPerTrip = 32 / kHG;  // accumulators per round trip
 #pragma unroll 1
-                        for (int c0 = 0; c0 < 4; c0 += kPerTrip) {
+                        for (int c0 = 0; c0 < kOPieces; c0 += kPerTrip) {
                             uint32_t o[kPerTrip][kHG];
 #pragma unroll
                             for (int c = 0; c < kPerTrip; ++c)
 #pragma unroll
                                 for (int u = 0; u < kLd; ++u)
-                                    tmem_ld_32x32b_x16(tmem + lane_addr + 256u + 64u * (c0 + c) + (uint32_t)h0 + 16u * u,
+                                    tmem_ld_32x32b_x16(tmem + lane_addr + TM_O + 64u * (c0 + c) + (uint32_t)h0 + 16u * u,
                                                        *reinterpret_cast<uint32_t(*)[16]>(&o[c][16 * u]));
                             tmem_wait_ld();
                             const float *al = ms.ph.tile.alpha[grp];
@@ -705,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int c = 0; c < kPerTrip; ++c)
 #pragma unroll
                                 for (int u = 0; u < kLd; ++u)
-                                    tmem_st_32x32b_x16(tmem + lane_addr + 256u + 64u * (c0 + c) + (uint32_t)h0 + 16u * u,
+                                    tmem_st_32x32b_x16(tmem + lane_addr + TM_O + 64u * (c0 + c) + (uint32_t)h0 + 16u * u,
                                                        *reinterpret_cast<const uint32_t(*)[16]>(&o[c][16 * u]));
                         }
                         tmem_wait_st();
@@ -725,7 +758,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             grid_launch_dependents();
             if (grp == 0 && __any_sync(0xffffffffu, bad_index) && lane == 0 && a.err_word)
                 atomicOr(a.err_word, (int)KV8_ERR_INDEX);
-            if (ok && n_tiles > 0) ok = mbar_wait(&ms.pv_done, (n_tiles - 1) & 1, &ms.abort_flag, a.err_word);
+            if (ok && n_tiles > 0)
+                ok = mbar_wait(&ms.pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, &ms.abort_flag, a.err_word);
             tc_fence_after_sync();
             // row sums per head: over the warp's 32 rows (the butterfly), then over the 4 quadrants
             {
@@ -746,36 +780,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) {
                 const float out_mul = ms.out_mul;
                 PartialView pv(a.ws, a.B, a.P, a.H);
-                // this thread's row (dims 128c + r) of the four accumulators, 32 columns per TMEM round
-                // trip; partial sets (relative to the running max) or the normalised output
+                // this thread's row (dims 128c + r) of the accumulators (dims 0..255: the hi and lo
+                // pieces' accumulators, summed); partial sets (relative to the running max) or the
+                // normalised output
                 float *const dst = a.ws ? pv.cl + ((int64_t)b * a.P + part) * a.H * kKL : a.out + (int64_t)b * a.H * kKL;
-                constexpr int kPerTrip = 32 / kHG;
 #pragma unroll 1
-                for (int c0 = 0; c0 < 4; c0 += kPerTrip) {
-                    uint32_t o[kPerTrip][kHG];
+                for (int c = 0; c < 4; ++c) {
+                    // chunk c: pieces 2c and 2c+1 for dims 0..255, piece c+2 for the rest
+                    uint32_t o[kHG];
                     if (n_tiles > 0) {
+                        if (c < 2) {
+                            uint32_t e[kHG];
 #pragma unroll
-                        for (int c = 0; c < kPerTrip; ++c)
+                            for (int u = 0; u < kLd; ++u) {
+                                tmem_ld_32x32b_x16(tmem + lane_addr + TM_O + 128u * c + (uint32_t)h0 + 16u * u,
+                                                   *reinterpret_cast<uint32_t(*)[16]>(&o[16 * u]));
+                                tmem_ld_32x32b_x16(tmem + lane_addr + TM_O + 128u * c + 64u + (uint32_t)h0 + 16u * u,
+                                                   *reinterpret_cast<uint32_t(*)[16]>(&e[16 * u]));
+                            }
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int j = 0; j < kHG; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) + __uint_as_float(e[j]));
+                        } else {
 #pragma unroll
                             for (int u = 0; u < kLd; ++u)
-                                tmem_ld_32x32b_x16(tmem + lane_addr + 256u + 64u * (c0 + c) + (uint32_t)h0 + 16u * u,
-                                                   *reinterpret_cast<uint32_t(*)[16]>(&o[c][16 * u]));
-                        tmem_wait_ld();
+                                tmem_ld_32x32b_x16(tmem + lane_addr + TM_O + 64u * (c + 2) + (uint32_t)h0 + 16u * u,
+                                                   *reinterpret_cast<uint32_t(*)[16]>(&o[16 * u]));
+                            tmem_wait_ld();
+                        }
                     } else {
 #pragma unroll
-                        for (int c = 0; c < kPerTrip; ++c)
-#pragma unroll
-                            for (int j = 0; j < kHG; ++j) o[c][j] = 0u;
+                        for (int j = 0; j < kHG; ++j) o[j] = 0u;
                     }
+                    float *const col = dst + 128 * c + r;
 #pragma unroll
-                    for (int c = 0; c < kPerTrip; ++c) {
-                        float *const col = dst + 128 * (c0 + c) + r;
-#pragma unroll
-                        for (int j = 0; j < kHG; ++j) {
-                            const int hl = h0 + j;  // head within the CTA
-                            const int hg = half * kHeadsPerCta + hl;
-                            if (hg < a.H) col[(int64_t)hg * kKL] = __uint_as_float(o[c][j]) * (a.ws ? out_mul : ms.ph.fin.zinv[hl]);
-                        }
+                    for (int j = 0; j < kHG; ++j) {
+                        const int hl = h0 + j;  // head within the CTA
+                        const int hg = half * kHeadsPerCta + hl;
+                        if (hg < a.H) col[(int64_t)hg * kKL] = __uint_as_float(o[j]) * (a.ws ? out_mul : ms.ph.fin.zinv[hl]);
                     }
                 }
                 if (a.ws && q == 0 && lane < kHG) {

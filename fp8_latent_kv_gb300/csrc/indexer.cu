@@ -469,7 +469,8 @@ cudaError_t launch_index_scores(const void *q, int q_bf16, const float *w, int B
     a.k_scale = k_scale;
     a.T = T;
     a.seq_stride_rows = seq_stride_rows;
-    a.ctas_per_item = B >= 152 ? 1 : 152 / B;  // one wave of CTAs (one per SM of a 152-SM part)
+    const int sms = device_sm_count();
+    a.ctas_per_item = B >= sms ? 1 : sms / B;  // one wave of CTAs (one per SM of the current device)
     a.scores = scores;
     a.hist0 = static_cast<uint32_t *>(topk_ws);
     a.err_word = err_word;
@@ -489,7 +490,8 @@ cudaError_t reset_topk_workspace(void *ws, int B, cudaStream_t st) {
 cudaError_t launch_topk(const float *scores, int B, int64_t T, int NS, int32_t *idx, void *ws, int *err_word,
                         cudaStream_t st) {
     cudaError_t e;
-    const int C = B >= kKMaxC ? 1 : kKMaxC / B;
+    const int cmax = min(kKMaxC, device_sm_count());  // one CTA per SM: the grid barriers need them all resident
+    const int C = B >= cmax ? 1 : cmax / B;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(B * C));
     cfg.blockDim = dim3(kKThreads);

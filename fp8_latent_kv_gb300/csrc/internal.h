@@ -71,7 +71,9 @@ size_t mixed_scratch_bytes(int H, int P);
 cudaError_t launch_copy(void *dst, const void *src, size_t bytes, cudaStream_t st);
 cudaError_t launch_lse_merge(const float *ws, int B, int P, int H, float *out, cudaStream_t st);
 
-// Partition policy shared by the workspace queries and the launchers.
+// Partition policy shared by the workspace queries and the launchers: one wave of CTAs on the current
+// device, from its multiprocessor count (152 when no device is visible).
+int device_sm_count();
 int decode_partitions(int H, int64_t T, int P_req);
 int select_partitions(int B, int H, int NS);
 int batch_partitions(int B, int H, int64_t T_max);

@@ -51,24 +51,45 @@ size_t sel_partial_bytes(int B, int P, int H) {
     return ((PartialView::floats(B, P, H) * sizeof(float)) + 255) & ~(size_t)255;
 }
 
+int device_sm_count() {
+    // a property of the GPU, so it may be kept per device id; with no visible device (host-only size
+    // queries) the answer is GB300's 152
+    constexpr int kMaxDev = 64;
+    static int cache[kMaxDev] = {0};
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+        (void)cudaGetLastError();
+        return 152;
+    }
+    if (dev < kMaxDev && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        return 152;
+    }
+    if (dev < kMaxDev) cache[dev] = n;
+    return n;
+}
+
 int decode_partitions(int H, int64_t T, int P_req) {
     if (T < 1) return 1;
     if (P_req > 0) {
         int64_t p = P_req < T ? P_req : T;
         return (int)(p > 65535 ? 65535 : p);
     }
-    // automatic: one wave of tensor-core CTAs (one per SM of a 152-SM part, a CTA per partition and
-    // 64-head half), at least 128 rows per partition
-    const int64_t cap = H > 64 ? 76 : 152;
+    // automatic: one wave of tensor-core CTAs on the current device (one per SM: a CTA per partition
+    // and 64-head half), at least 128 rows per partition
+    const int64_t sms = device_sm_count();
+    const int64_t cap = H > 64 ? sms / 2 : sms;
     const int64_t p = (T + 127) / 128;
-    return (int)(p < cap ? p : cap);
+    return (int)(p < cap ? p : (cap < 1 ? 1 : cap));
 }
 
 int batch_partitions(int B, int H, int64_t T_max) {
-    // one wave of tensor-core CTAs (one per SM of a 152-SM part): B items x P partitions x head halves,
-    // at least 128 rows per partition
+    // one wave of tensor-core CTAs on the current device (one per SM): B items x P partitions x head
+    // halves, at least 128 rows per partition
     const int64_t n_half = H > 64 ? 2 : 1;
-    int64_t cap = 152 / ((int64_t)B * n_half);
+    int64_t cap = device_sm_count() / ((int64_t)B * n_half);
     if (cap < 1) cap = 1;
     const int64_t p = (T_max + 127) / 128;
     return (int)(p < cap ? p : cap);
@@ -79,11 +100,11 @@ size_t decode_partial_bytes_b(int B, int P, int H) {
 }
 
 int select_partitions(int B, int H, int NS) {
-    // one wave of tensor-core CTAs (one per SM of a 152-SM part): B items x P partitions x head
+    // one wave of tensor-core CTAs on the current device (one per SM): B items x P partitions x head
     // halves, with the list's 128-row tiles spread evenly over the partitions
     const int64_t n_half = H > 64 ? 2 : 1;
     const int64_t tiles = (NS + 127) / 128;
-    int64_t cap = 152 / ((int64_t)B * n_half);
+    int64_t cap = device_sm_count() / ((int64_t)B * n_half);
     if (cap < 1) cap = 1;
     const int64_t per = (tiles + cap - 1) / cap;
     const int64_t p = (tiles + per - 1) / per;

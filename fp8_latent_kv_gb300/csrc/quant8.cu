@@ -112,7 +112,8 @@ cudaError_t launch_encode(const float *y, int64_t n, uint8_t *out, cudaStream_t 
     if (n == 0) return cudaSuccess;
     int64_t n4 = (n + 3) / 4;
     int64_t blocks = (n4 + 255) / 256;
-    if (blocks > 152 * 16) blocks = 152 * 16;
+    const int64_t cap = (int64_t)device_sm_count() * 16;  // a grid-stride loop: a few waves suffice
+    if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     encode_kernel<<<(unsigned)blocks, 256, 0, st>>>(y, n, out);
     return cudaGetLastError();

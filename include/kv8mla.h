@@ -125,8 +125,10 @@ KV8_API int kv8_quant_rows_w(const float *x, int64_t n, int width, uint8_t *q, f
  * The decode workspace continues with the library's own staging (the prepared queries); its size
  * is included in mla_decode8_workspace_bytes.
  * mla_decode8_partitions:      the partition count P the library uses for (H, T, P_req):
- *                              P_req = 0 picks automatically (one CTA per SM of a 152-SM GPU:
- *                              min(ceil(T/128), 76 for H > 64, else 152)), P_req > 0 is clamped to [1, T].
+ *                              P_req = 0 picks automatically (one CTA per SM of the current device,
+ *                              N SMs (152 on GB300; 152 when no device is visible): min(ceil(T/128),
+ *                              N/2 for H > 64, else N)), P_req > 0 is clamped to [1, T].  The count
+ *                              depends on the device current at the call: size and launch on one device.
  * mla_decode8_workspace_bytes: workspace bytes for (H, T, P_req).
  * --------------------------------------------------------------------------------------------- */
 KV8_API int mla_decode8_partitions(int H, int64_t T, int P_req, int *P_out);
@@ -163,7 +165,7 @@ KV8_API int mla_absorb_decode8(const void *q_lat, const void *q_rope, int q_dtyp
  *   skipped and sets KV8_ERR_INDEX in *err_word.  out [B][H][512] f32.
  *   NS in [1, KV8_MAX_SELECT]; T in [1, KV8_MAX_ROWS]; H in [1, 128]; B >= 1.
  *   workspace >= mla_sel8_workspace_bytes(B, H, NS): the B x P partial sets, then staging for the
- *   prepared bf16 queries.  P spreads the list's 128-row tiles over one wave of 152 CTAs (B items x
+ *   prepared bf16 queries.  P spreads the list's 128-row tiles over one wave of CTAs, one per SM (B items x
  *   P x ceil(H/64)).  bf16 queries run on the tensor cores, which gather the selected rows from all
  *   items' caches with 32-bit row coordinates; f32 queries, and caches with
  *   (B-1)*seq_stride_rows + T >= 2^31 rows, run on the CUDA cores.
