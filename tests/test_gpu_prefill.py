@@ -1,16 +1,16 @@
 """GPU causal prefill vs the oracle.
 
 Small chunk: every query and head.  Full workload (S = 1024 queries at 64512..65535 over T = 65536
-rows, H = 128): the 1024 fresh rows are quantized on the GPU in-run (checked bit-exact), then
-sampled (query, head) pairs -- including the first and last query -- are compared with the oracle;
-the last query also equals a full-T decode on the GPU.
+rows, H = 128): the 1024 fresh rows are quantized on the GPU in-run (checked bit-exact), then 64
+queries -- the first, the last and 62 spread between -- are compared with the oracle on every head
+(each head on its own scale); the last query also equals a full-T decode on the GPU.
 """
 import numpy as np
 import pytest
 import torch
 
 import synth
-from helpers import oracle_cache, parity
+from helpers import oracle_cache, parity, parity_per_head
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda")
@@ -73,10 +73,11 @@ def test_prefill_full_workload_sampled(lib, oracle):
     tql, tqr = bf(ql), bf(qr)
     got = _prefill(lib, tql, tqr, w.pos0, kv8, sc, w.T)
     assert np.all(np.isfinite(got))
-    qs = [0, 1, 511, 1023]
-    heads = [0, 77, 127]
-    ref = oracle.attn_prefill(ql[qs][:, heads], qr[qs][:, heads], w.pos0 + np.array(qs), q_o, s_o, synth.SM_SCALE)
-    parity(got[qs][:, heads], ref, "prefill sampled")
+    # 64 queries (the first, the last and 62 spread between) x every head, each head on its own scale
+    qs = sorted({0, w.S - 1} | set(np.linspace(1, w.S - 2, 62).astype(int).tolist()))
+    assert len(qs) == 64
+    ref = oracle.attn_prefill(ql[qs], qr[qs], w.pos0 + np.array(qs), q_o, s_o, synth.SM_SCALE)
+    parity_per_head(got[qs], ref, "prefill 64 queries every head")
     # the last query attends the whole cache: equal to decode over all T rows
     ws = torch.empty(lib.mla_decode8_workspace_bytes(w.H, w.T) // 4, dtype=torch.float32, device=DEV)
     dec = torch.empty((w.H, 512), dtype=torch.float32, device=DEV)

@@ -1,7 +1,8 @@
 """GPU selected-row (DSA gather) decode vs the oracle.
 
 Full workload: B = 8 sequences, each with its own T = 131072-row cache, NS = 2048 sorted unique
-indices; sampled heads of every sequence compared with the oracle.  Edge cases: a full index list
+indices; every head of the first and the last sequence (each head on its own scale) and sampled heads
+of every sequence compared with the oracle.  Edge cases: a full index list
 equals dense decode, NS = 1, duplicate indices, out-of-range indices (skipped and flagged).
 """
 import numpy as np
@@ -9,7 +10,7 @@ import pytest
 import torch
 
 import synth
-from helpers import oracle_cache, parity
+from helpers import oracle_cache, parity, parity_per_head
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda")
@@ -43,6 +44,13 @@ def test_select_full_workload_sampled_heads(lib, oracle):
     got = _sel(lib, torch.from_numpy(ql).to(DEV).to(torch.bfloat16), torch.from_numpy(qr).to(DEV).to(torch.bfloat16),
                kv8, sc, w.T, w.T, torch.from_numpy(idx).to(DEV), err)
     assert err.item() == 0
+    # every head of the first and the last sequence, each head on its own scale
+    for b in (0, w.B - 1):
+        ref, bad = oracle.attn_select(ql[b:b + 1], qr[b:b + 1], q_all[b * w.T:(b + 1) * w.T],
+                                      s_all[b * w.T:(b + 1) * w.T], w.T, w.T, idx[b:b + 1], synth.SM_SCALE)
+        assert bad == 0
+        parity_per_head(got[b], ref[0], f"dsa sequence {b} every head")
+    # sampled heads of all sequences
     heads = [0, 5, 64, 127]
     ref, bad = oracle.attn_select(ql[:, heads], qr[:, heads], q_all, s_all, w.T, w.T, idx, synth.SM_SCALE)
     assert bad == 0
