@@ -25,8 +25,9 @@
 //           An MMA reading A MN-major costs about the same at N = 64 as at N = 128, so the wide passes
 //           halve the first two chunks' tensor time; TMEM has room for two of them.
 //
-// Rows reach shared memory by TMA: dense (and causal) ranges as 128-row tiles, selected rows (DSA) four
-// at a time with tile::gather4 from a tensor map over all items' caches.
+// Rows reach shared memory by TMA as 128-row tiles (dense and causal ranges); selected rows (DSA) by
+// cp.async, one row per warp instruction (32 lanes x 16 bytes), written into the same swizzled image --
+// the copy engine works through tile::gather4 copies (four rows per copy) several times slower.
 //
 // Warps: 0 = TMA producer, 1 = MMA issuer (and TMEM owner), 2..17 = softmax / epilogue in four groups of
 // four warps (one per TMEM lane quadrant), each group owning 16 of the CTA's 64 heads.
@@ -109,6 +110,7 @@ struct TcArgs {
     const __nv_bfloat16 *q_lat;  // [B][H][512]
     const __nv_bfloat16 *q_rope; // [B][H][64]
     int B, H, P, n_half;
+    const uint8_t *kv8;          // cache rows [..][576] (selected rows are copied from here directly)
     const float *kv_scale;
     int64_t T;
     int64_t pos0;                // causal: item b attends rows [0, pos0 + b]; -1: rows [0, T)
@@ -175,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&ms.kv_full[s], 1);
+            mbar_init(&ms.kv_full[s], idx_b ? 32 : 1);  // selected rows: one cp.async arrival per producer lane
             mbar_init(&ms.kv_empty[s], 1);
             for (int kb = 0; kb < 4; ++kb) mbar_init(&ms.kv_blk[s][kb], 1);
             mbar_init(&ms.pv_done[s], 1);
@@ -210,10 +212,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 prefetch_tensormap(&map_rc);
             }
             int issued = 0, armed = 0;
+            // the query image (which depends on the query prep) goes out after the first tile's rows (which
+            // do not), so that the first score waits for one tile and the image only
+            const int q_at = n_tiles > 1 ? 1 : 0;
             for (int i = 0; i < n_tiles; ++i) {
                 const int s = i & 1;
-                if (lane == 0 && (i == 2 || (i == n_tiles - 1 && i < 2)) && a.qimg) {
-                    // the rows do not depend on the query prep; the query image does
+                if (lane == 0 && i == q_at && a.qimg) {
                     grid_dependency_wait();
                     mbar_arrive_expect_tx(&ms.q_full, kImg);
                     const uint8_t *src = a.qimg + ((size_t)b * a.n_half + half) * kImg;
@@ -256,18 +260,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0 && i >= 2) ok_p = mbar_wait(&ms.kv_empty[s], ph, &ms.abort_flag, a.err_word);
                     ok_p = __shfl_sync(0xffffffffu, ok_p, 0);
                     if (ok_p) {
-                        if (lane == 0) {
-                            mbar_arrive_expect_tx(&ms.kv_full[s], kImg);
-                            armed = i + 1;
-                        }
-                        __syncwarp();
-                        // lane l fetches tile rows 4l..4l+3: 512 bytes of each latent block, 256 of the rope block
+                        // the context product's reads of this stage are complete; order them before the
+                        // copies' writes (another proxy)
+                        fence_proxy_async_smem();
+                        armed = i + 1;
+                        // latent rows one per instruction: lane l copies bytes 16l..16l+15 (latent block l/8)
+                        // into the 128-byte-swizzled image the tile copies would make
+                        const uint8_t *kv = a.kv8;
+#pragma unroll 1
+                        for (int r4 = 0; r4 < 32; ++r4) {
 #pragma unroll
-                        for (int kb = 0; kb < 4; ++kb)
-                            tma_gather4(st + kb * 16384 + lane * 512, &map_lc, kb * 128, rows[0], rows[1], rows[2],
-                                        rows[3], &ms.kv_full[s]);
-                        tma_gather4(st + kRcOff + lane * 256, &map_rc, 512, rows[0], rows[1], rows[2], rows[3],
-                                    &ms.kv_full[s]);
+                            for (int k = 0; k < 4; ++k) {
+                                const int r = 4 * r4 + k;
+                                const int row = __shfl_sync(0xffffffffu, rows[k], r4);
+                                cp_async_16(st + (lane >> 3) * 16384 + sw128_offset((uint32_t)r, (uint32_t)(lane & 7) * 16u),
+                                            kv + (int64_t)row * kRow + lane * 16);
+                            }
+                        }
+                        // rope bytes: 64 per row, eight rows per instruction (lane l: row r0 + l/4, chunk l%4)
+#pragma unroll 1
+                        for (int r0 = 0; r0 < kTile; r0 += 8) {
+                            const int r = r0 + (lane >> 2), src_lane = r >> 2, k = r & 3;
+                            const int c0 = __shfl_sync(0xffffffffu, rows[0], src_lane);
+                            const int c1 = __shfl_sync(0xffffffffu, rows[1], src_lane);
+                            const int c2 = __shfl_sync(0xffffffffu, rows[2], src_lane);
+                            const int c3 = __shfl_sync(0xffffffffu, rows[3], src_lane);
+                            const int row = k == 0 ? c0 : k == 1 ? c1 : k == 2 ? c2 : c3;
+                            cp_async_16(st + kRcOff + sw64_offset((uint32_t)r, (uint32_t)(lane & 3) * 16u),
+                                        kv + (int64_t)row * kRow + kKL + (lane & 3) * 16);
+                        }
+                        // one arrival per lane (the barrier expects 32 for selected rows) when its copies land
+                        cp_async_mbar_arrive(&ms.kv_full[s]);
                     }
                 }
                 ok_p = __shfl_sync(0xffffffffu, ok_p, 0);
@@ -484,6 +507,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (ns < n_tiles && mbar_test_wait(&ms.kv_full[ns & 1], (ns >> 1) & 1) &&
                         (ns == 0 || mbar_test_wait(&ms.s_free, (ns - 1) & 1))) {
                         tc_fence_after_sync();
+                        // selected rows arrive by cp.async (generic proxy): make them visible to the MMAs
+                        if (idx_b) fence_proxy_async_smem();
                         issue_score(ns++);
                         spins = 0;
                         continue;
@@ -995,6 +1020,7 @@ cudaError_t launch_attn_tc(const AttnArgs &x, cudaStream_t st) {
     a.H = x.H;
     a.P = x.P;
     a.n_half = x.H > kHeadsPerCta ? 2 : 1;
+    a.kv8 = x.kv8;
     a.kv_scale = x.kv_scale;
     a.T = x.T;
     a.pos0 = x.pos0;

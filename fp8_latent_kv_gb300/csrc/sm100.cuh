@@ -119,6 +119,18 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint
                  : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared through L2 (sm_80 cp.async; both addresses 16-byte aligned).
+// The bytes land in the generic proxy: a reader in the async proxy (tcgen05.mma) needs
+// fence_proxy_async_smem() after it has seen them complete.
+__device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+// An arrival on `bar` once every cp.async this thread issued before has completed; the barrier's expected
+// count includes it (no increment of the pending count).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
