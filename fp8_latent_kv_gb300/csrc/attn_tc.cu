@@ -26,8 +26,8 @@
 //           halve the first two chunks' tensor time; TMEM has room for two of them.
 //
 // Rows reach shared memory by TMA as 128-row tiles (dense and causal ranges); selected rows (DSA) by
-// cp.async, one row per warp instruction (32 lanes x 16 bytes), written into the same swizzled image --
-// the copy engine works through tile::gather4 copies (four rows per copy) several times slower.
+// cp.async, one row per warp instruction (32 lanes x 16 bytes), written into the same swizzled image
+// (as fast as four-row TMA gathers, and it leaves the copy engine to the query image).
 //
 // Warps: 0 = TMA producer, 1 = MMA issuer (and TMEM owner), 2..17 = softmax / epilogue in four groups of
 // four warps (one per TMEM lane quadrant), each group owning 16 of the CTA's 64 heads.
@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ================================ TMA producer ================================
         // Dense rows: lane 0 issues the tile copies and does the waits.  Selection: the whole warp reads
-        // the tile's 128 row indices (4 per lane) and every lane gathers its own 4 rows.
+        // the tile's 128 row indices (4 per lane) and copies the rows, one row per instruction.
         if (n_tiles > 0) {
             if (lane == 0) {
                 prefetch_tensormap(&map_lc);
@@ -991,8 +991,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // Launch the tensor-core kernel.  The grid covers B items x P partitions x the head halves.  Dense
-// rows are loaded as 128-row tiles; selected rows are gathered 4 at a time from a tensor map over all
-// items' caches.  Returns cudaErrorNotSupported if the tensor-map encoder is unavailable.
+// rows are loaded as 128-row tiles through tensor maps over all items' caches; selected rows are
+// copied by the kernel's producer warp.  Returns cudaErrorNotSupported if the tensor-map encoder is
+// unavailable.
 cudaError_t launch_attn_tc(const AttnArgs &x, cudaStream_t st) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
@@ -1003,7 +1004,7 @@ cudaError_t launch_attn_tc(const AttnArgs &x, cudaStream_t st) {
     CUtensorMap m_lc, m_rc;
     const cuuint64_t dims[2] = {(cuuint64_t)kRow, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)kRow};
-    const cuuint32_t box_h = sel ? 1u : (cuuint32_t)kTile;
+    const cuuint32_t box_h = sel ? 1u : (cuuint32_t)kTile;  // selection does not use the maps
     const cuuint32_t box_lc[2] = {128, box_h}, box_rc[2] = {64, box_h}, es[2] = {1, 1};
     void *base = const_cast<uint8_t *>(x.kv8);
     if (encode(&m_lc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box_lc, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
