@@ -13,6 +13,9 @@
 // cache through shared memory (16-byte loads), computes the 64x32 score tile, updates the online
 // softmax per head and accumulates the 32x512 context in registers (2 latent columns per thread).
 #include "internal.h"
+#include "sm100.cuh"
+
+#include <cudaTypedefs.h>
 
 #include <math.h>
 
@@ -221,10 +224,90 @@ __global__ void __launch_bounds__(kThreads, 1) attn_simt_kernel(AttnArgs a) {
 
 // Log-sum-exp merge: block (h, quarter, b) -- 128 threads, one latent column each.
 //
-// Small P (<= kMergeFast): every load the block needs is issued before any result is used -- each
-// thread's P partial columns, and each warp's own copy of the P maxima and row sums -- so the
-// partials' latency is paid about once.  Each warp turns the maxima into weights 2^(m_p - M) itself
-// (lane p % 32 holds partition p's) and every thread sums its column.
+// P <= kMergeTma: one 3-D TMA box brings the block's 128 columns of all P partitions' cl rows of head h
+// into shared memory (a tensor map over cl viewed as [B*P][H][512]), while warp 0 loads every maximum and
+// row sum at once (up to four per lane, one round trip) and turns them into weights 2^(m_p - M); every
+// thread then sums its column.  Per-thread loads of the columns (the kernels below) keep far more lines
+// in flight per SM than the load units track, so they wait on memory-level parallelism, not bandwidth.
+constexpr int kMergeTma = 128;
+// byte offset of the merge block's mbarrier: after the P x 128 columns and the P + 1 weights
+__host__ __device__ constexpr size_t merge_tma_bar_offset(int P) {
+    return ((size_t)P * 129 * sizeof(float) + sizeof(float) + 15) & ~(size_t)15;
+}
+
+__global__ void __launch_bounds__(128) lse_merge_tma_kernel(const __grid_constant__ CUtensorMap map,
+                                                            const float *__restrict__ ws, int B, int P, int H,
+                                                            float *__restrict__ out) {
+    extern __shared__ __align__(1024) uint8_t msm[];
+    float *cs = reinterpret_cast<float *>(msm);  // [P][128]
+    float *wsh = cs + (size_t)P * 128;           // [P] weights, then Z
+    uint64_t *full = reinterpret_cast<uint64_t *>(msm + merge_tma_bar_offset(P));
+    const int h = blockIdx.x, quarter = blockIdx.y, b = blockIdx.z, tid = threadIdx.x, lane = tid & 31;
+    PartialView pv(const_cast<float *>(ws), B, P, H);
+    const int64_t base = (int64_t)b * P * H + h;
+    float *o = out + ((int64_t)b * H + h) * kKL + quarter * 128 + tid;
+    if ((sm100::smem_u32(msm) & 127u) != 0) {  // a tensor copy needs a 128-byte aligned destination
+        *o = NAN;
+        return;
+    }
+    if (tid == 0) {
+        sm100::prefetch_tensormap(&map);
+        sm100::mbar_init(full, 1);
+        sm100::fence_barrier_init();
+    }
+    __syncthreads();
+    // launched as a programmatic dependent of the partial kernel: wait until its partials are written
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (tid == 0) {
+        sm100::mbar_arrive_expect_tx(full, (uint32_t)P * 512u);
+        sm100::tma_load_3d(cs, &map, quarter * 128, h, b * P, full);
+    }
+    if (tid < 32) {
+        float mv[kMergeTma / 32], zv[kMergeTma / 32];
+#pragma unroll
+        for (int k = 0; k < kMergeTma / 32; ++k) {
+            const int p = lane + 32 * k;
+            mv[k] = p < P ? pv.m[base + (int64_t)p * H] : -INFINITY;
+            zv[k] = p < P ? pv.z[base + (int64_t)p * H] : 0.f;
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kMergeTma / 32; ++k) M = fmaxf(M, mv[k]);
+        M = warp_max(M);
+        float Z = 0.f;
+#pragma unroll
+        for (int k = 0; k < kMergeTma / 32; ++k) {
+            const int p = lane + 32 * k;
+            const float w = (mv[k] == -INFINITY || M == -INFINITY) ? 0.f : exp2f(mv[k] - M);
+            if (p < P) wsh[p] = w;
+            Z = fmaf(w, zv[k], Z);
+        }
+        Z = warp_sum(Z);
+        if (tid == 0) wsh[P] = Z;
+    }
+    __syncthreads();
+    // the copy lands long before the limit; if it did not, the block reports NaN and still waits for it
+    // before it ends (its destination is this block's shared memory)
+    const bool ok = sm100::mbar_wait(full, 0, nullptr, nullptr, 200000000ull);
+    if (!ok) (void)sm100::mbar_wait(full, 0, nullptr, nullptr, 200000000ull);
+    float acc0 = 0.f, acc1 = 0.f;
+    for (int p = 0; p < P; ++p) {
+        const float w = wsh[p];
+        // a partition with weight 0 may hold anything (it attended no row): do not touch its values
+        if (w != 0.f) {
+            if (p & 1) acc1 = fmaf(w, cs[p * 128 + tid], acc1);
+            else acc0 = fmaf(w, cs[p * 128 + tid], acc0);
+        }
+    }
+    const float Z = wsh[P];
+    *o = !ok ? NAN : Z > 0.f ? (acc0 + acc1) / Z : 0.f;
+}
+
+// Without a tensor-map encoder, or for P > kMergeTma.  Small P (<= kMergeFast): every load the block
+// needs is issued before any result is used -- each thread's P partial columns, and each warp's own copy
+// of the P maxima and row sums -- so the partials' latency is paid about once.  Each warp turns the
+// maxima into weights 2^(m_p - M) itself (lane p % 32 holds partition p's) and every thread sums its
+// column.
 constexpr int kMergeFast = 128;
 constexpr int kMergeMaxP = 1024;  // larger P: weights kept in shared memory, loops over slices
 
@@ -357,6 +440,25 @@ cudaError_t launch_lse_merge(const float *ws, int B, int P, int H, float *out, c
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (encode && P <= kMergeTma) {
+        // cl viewed as [B*P][H][512] f32: one box = 128 columns x 1 head x the item's P partitions
+        CUtensorMap map;
+        const cuuint64_t dims[3] = {(cuuint64_t)kKL, (cuuint64_t)H, (cuuint64_t)B * (cuuint64_t)P};
+        const cuuint64_t strides[2] = {(cuuint64_t)kKL * sizeof(float), (cuuint64_t)H * kKL * sizeof(float)};
+        const cuuint32_t box[3] = {128u, 1u, (cuuint32_t)P}, es[3] = {1u, 1u, 1u};
+        if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(ws), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
+            cudaError_t e = cudaFuncSetAttribute(lse_merge_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)(merge_tma_bar_offset(kMergeTma) + sizeof(uint64_t)));
+            if (e != cudaSuccess) return e;
+            cfg.dynamicSmemBytes = merge_tma_bar_offset(P) + sizeof(uint64_t);
+            e = cudaLaunchKernelEx(&cfg, lse_merge_tma_kernel, map, ws, B, P, H, out);
+            if (e != cudaSuccess) return e;
+            return cudaGetLastError();
+        }
+    }
     cudaError_t e = P <= 16   ? cudaLaunchKernelEx(&cfg, lse_merge_kernel<16>, ws, B, P, H, out)
                     : P <= 32 ? cudaLaunchKernelEx(&cfg, lse_merge_kernel<32>, ws, B, P, H, out)
                     : P <= 64 ? cudaLaunchKernelEx(&cfg, lse_merge_kernel<64>, ws, B, P, H, out)
