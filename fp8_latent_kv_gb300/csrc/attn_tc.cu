@@ -60,6 +60,7 @@ constexpr int kThreads = 64 + 128 * kNG; // warp 0 TMA, warp 1 MMA, then the sof
 constexpr int kSoftmaxThreads = 128 * kNG;
 constexpr int kPrepThreads = 288;      // warps 1..9: the in-kernel query prep's workers
 constexpr int kPrepAll = kThreads - 32;  // warps 1..: every thread that waits for the prologue
+static_assert(kPrepAll / 32 <= 32, "one prologue maximum slot per warp");
 static_assert(kHG == 16 || kHG == 32, "a softmax thread's heads: one or two 16-column TMEM loads");
 constexpr uint32_t kImg = 73728;       // 4 x 16 KB (SW128, 128 B per row) + 8 KB (SW64, 64 B per row)
 constexpr uint32_t kRcOff = 65536;     // rope block inside an image / stage
@@ -80,7 +81,7 @@ struct Misc {
     union alignas(16) Phase {                  // storage that is never live in two phases at once
         struct {
             int qmax_bits[kHeadsPerCta];       // prologue: per-head max |q| (bits of a non-negative float)
-            float wred[2][16];                 // prologue: per-warp maxima
+            float wred[2][16];                 // prologue: per-warp maxima (flat: one slot per warp 1..17)
         } pro;
         struct {
             float alpha[kNG][kHG];             // tile loop, per softmax group: rescale factors 2^(m_old - m_new)
@@ -315,7 +316,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             // decode: the prep kernel wrote the query image (loaded by the producer) and the factors
             grid_dependency_wait();
             if (pt < kHeadsPerCta) ms.c_head[pt] = a.c_head[(b * a.n_half + half) * kHeadsPerCta + pt];
-            smax = a.smax[b * a.P + part];
+            if (idx_b) {
+                smax = a.smax[b * a.P + part];
+            } else {
+                // dense rows: the largest row scale of this CTA's rows, read here (one round of loads,
+                // beside the query image's copy) rather than by the prep kernel, whose grid -- and with it
+                // the query image -- then completes sooner.  After the grid dependency: the step's append
+                // may just have written the last row's scale.
+                const float *sc = a.kv_scale + seq_base;
+                for (int64_t t = t0 + pt; t < t1; t += 8 * kPrepAll) {
+                    float v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int64_t tu = t + (int64_t)u * kPrepAll;
+                        v[u] = tu < t1 ? __ldg(sc + tu) : 0.f;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) smax = fmaxf(smax, fabsf(v[u]));
+                }
+                smax = warp_max(smax);
+                float *wr = &ms.ph.pro.wred[0][0];  // 32 slots for the prologue's 17 warps
+                if (lane == 0) wr[warp - 1] = smax;
+                named_sync(1, kPrepAll);
+                smax = 0.f;
+                for (int k = 0; k < kPrepAll / 32; ++k) smax = fmaxf(smax, wr[k]);
+            }
         } else {
             // prefill: each CTA prepares its own 64 heads (the image is reused for all its tiles)
             constexpr int kItems = kHeadsPerCta * 36 / kPrepThreads;  // 8 chunks of 16 query elements
@@ -864,8 +889,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Query prep, run once before the partial kernel (decode and selection).  Block b * n_heads_pad/8 + g
 // splits heads 8g..8g+7 of item b (each scaled by 2^e_h so that max|q| * 2^e_h lies in [128, 256)) into
 // e4m3 hi + lo rows of that item's head-group image and writes their score factors
-// sm_scale*log2(e)*2^-e_h (0 for a padding head); block B * n_heads_pad/8 + b * P + p takes the largest
-// scale among the rows that partition p of item b attends.
+// sm_scale*log2(e)*2^-e_h (0 for a padding head); for selected rows, block B * n_heads_pad/8 + b * P + p
+// takes the largest scale among the rows that partition p of item b attends (dense rows: the partial
+// kernel takes it itself).
 struct PrepArgs {
     const __nv_bfloat16 *q_lat, *q_rope;
     int B, H, n_heads_pad, P;
@@ -1061,7 +1087,9 @@ cudaError_t launch_attn_tc(const AttnArgs &x, cudaStream_t st) {
         a.c_head = pa.c_head;
         a.smax = pa.smax;
         cudaLaunchConfig_t pcfg = {};
-        pcfg.gridDim = dim3((unsigned)((int64_t)a.B * (n_heads_pad / kPrepHeads + a.P)));
+        // partition blocks (largest row scale per partition) only for selected rows; dense rows take the
+        // maximum inside the partial kernel
+        pcfg.gridDim = dim3((unsigned)((int64_t)a.B * (n_heads_pad / kPrepHeads + (sel ? a.P : 0))));
         pcfg.blockDim = dim3(kPrepBlock);
         pcfg.stream = st;
         cudaLaunchAttribute pattr[1];
