@@ -421,11 +421,31 @@ __global__ void __launch_bounds__(kKThreads) topk_kernel(const float *__restrict
         gcnt[2 * c + 1] = cta_eq;
     }
     if (!query_barrier(gbar, 3u * (uint32_t)C, err_word, &abort_sh)) return;
-    uint32_t gt_prev = 0, eq_prev = 0;  // over the query's earlier CTAs
-    for (int cc = 0; cc < c; ++cc) {
-        gt_prev += __ldcg(&gcnt[2 * cc]);
-        eq_prev += __ldcg(&gcnt[2 * cc + 1]);
+    // over the query's earlier CTAs: every count loaded at once (a lane per CTA, all in flight), then a
+    // warp sum -- a loop of dependent adds would wait for one round trip per earlier CTA
+    if (tid < 32) {
+        uint32_t g = 0, e = 0;
+#pragma unroll
+        for (int u = 0; u < (kKMaxC + 31) / 32; ++u) {
+            const int cc = tid + 32 * u;
+            const bool in = cc < c;
+            const uint32_t gv = in ? __ldcg(&gcnt[2 * cc]) : 0u, ev = in ? __ldcg(&gcnt[2 * cc + 1]) : 0u;
+            g += gv;
+            e += ev;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            g += __shfl_xor_sync(0xffffffffu, g, o);
+            e += __shfl_xor_sync(0xffffffffu, e, o);
+        }
+        if (tid == 0) {
+            warp_sums[0] = g;
+            warp_sums[1] = e;
+        }
     }
+    __syncthreads();
+    const uint32_t gt_prev = warp_sums[0], eq_prev = warp_sums[1];
+    __syncthreads();  // warp_sums is reused by the next scan
     const uint32_t eq_all_before = eq_prev + eq_before;
     const uint32_t eq_take = eq_all_before >= need ? 0u : (need - eq_all_before < n_eq ? need - eq_all_before : n_eq);
     const uint32_t eq_taken_prev = eq_prev < need ? eq_prev : need;  // equals taken by earlier CTAs
