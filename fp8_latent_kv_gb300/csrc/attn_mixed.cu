@@ -29,10 +29,10 @@
 // 128-byte-swizzled block), the query image (e4m3 rows, bf16 RoPE rows and their lo piece), the
 // weights (e4m3 hi and lo, bf16).  TMEM (512 columns): one score buffer (S_n | S_r), five 64-column
 // context accumulators.
-// Warps: 0 = TMA producer, 1 = MMA issuer (and TMEM owner), 2..9 = softmax / epilogue.  The query image,
-// the per-head score factors and the per-partition row-scale maxima come from mixed_prep_kernel, run just
-// before as the programmatic predecessor: the producer starts the first two tiles' loads before it waits
-// for that grid.  Every mbarrier wait is bounded in time; a timeout sets KV8_ERR_TIMEOUT, and the
+// Warps: 0 = TMA producer, 1 = MMA issuer (and TMEM owner), 2..9 = softmax / epilogue.  The query image
+// and the per-head score factors come from mixed_prep_kernel, run just before as the programmatic
+// predecessor: the producer starts the first tile's loads before it waits for that grid; the prologue
+// takes the largest row scale of the CTA's rows itself.  Every mbarrier wait is bounded in time; a timeout sets KV8_ERR_TIMEOUT, and the
 // softmax warps then skip their remaining waits but pass every named barrier.
 #include "internal.h"
 #include "quant_row.cuh"
@@ -116,10 +116,9 @@ struct MxArgs {
     float *ws;                   // partial sets [P][H]
     int *err_word;
     // written by mixed_prep_kernel: query images [n_half][kQImg], score factors [n_half * 64] (0 for a
-    // padding head), row-scale maxima [P]
+    // padding head)
     const uint8_t *qimg;
     const float *c_head;
-    const float *smax;
 };
 
 __device__ __forceinline__ uint32_t bf16x2_bits(float a, float b) {  // a in the low half
@@ -207,8 +206,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_2d(st + kB3, &map_k8b3, 384, y, &ms.kv_full[s]);
                 tma_load_2d(st + kRope, &map_kr, 0, y, &ms.kv_full[s]);
                 issued = i + 1;
-                if (i == (n_tiles < 2 ? n_tiles : 2) - 1) {
-                    // the rows do not depend on the query prep; the query image does
+                if (i == 0) {
+                    // the rows do not depend on the query prep; the query image does: it goes out after
+                    // the first tile, so that the first score waits for one tile and the image only
                     grid_dependency_wait();
                     mbar_arrive_expect_tx(&ms.q_full, kQImg);
                     const uint8_t *src = a.qimg + (size_t)half * kQImg;
@@ -221,20 +221,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = (armed > 2 ? armed - 2 : 0); i < armed; ++i)
                 mbar_wait(&ms.kv_full[i & 1], (i >> 1) & 1, nullptr, a.err_word,
                           i < issued ? 200000000ull : 20000000ull);
-            if (issued >= (n_tiles < 2 ? n_tiles : 2)) mbar_wait(&ms.q_full, 0, nullptr, a.err_word, 200000000ull);
+            if (issued >= 1) mbar_wait(&ms.q_full, 0, nullptr, a.err_word, 200000000ull);
         }
         __syncwarp();
     } else {
-        // ============ prologue: the prep kernel's score factors and row-scale maximum ============
+        // ============ prologue: the prep kernel's score factors, the rows' largest scale ============
         const int pt = tid - 32;  // 0..287
         grid_dependency_wait();
+        // the largest row scale of this CTA's rows, read here (one round of loads beside the query image's
+        // copy) rather than by the prep kernel, whose grid -- and with it the image -- then completes
+        // sooner.  After the grid dependency: the step's append may just have written the last row.
+        float mx = 0.f;
+        for (int64_t t = t0 + pt; t < t1; t += 8 * kPrepThreads) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int64_t tu = t + (int64_t)u * kPrepThreads;
+                v[u] = tu < t1 ? __ldg(a.k_scale + tu) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) mx = fmaxf(mx, fabsf(v[u]));
+        }
+        mx = warp_max(mx);
+        if (lane == 0) ms.red[0][warp - 1] = mx;  // scratch until the tile loop
         if (pt < kHeads) {
             ms.c_head[pt] = a.c_head[half * kHeads + pt];
             ms.m_run[0][pt] = ms.m_run[1][pt] = -INFINITY;
             ms.m_ref[0][pt] = ms.m_ref[1][pt] = 0.f;
         }
+        named_sync(1, kPrepThreads);
         if (pt == 0) {
-            const float s_ref = fmaxf(a.smax[part], 1e-30f);
+            float m = 0.f;
+            for (int k = 0; k < kPrepThreads / 32; ++k) m = fmaxf(m, ms.red[0][k]);
+            const float s_ref = fmaxf(m, 1e-30f);
             ms.w_mul = kWScale / s_ref;
             ms.out_mul = s_ref / kWScale;
         }
@@ -583,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // 8g + w: its no-position part goes through the row quantizer's f32 steps (the bytes the cache quantizer
 // would give) into K-major e4m3 rows of its head half's image, its RoPE part into bf16 rows (an f32 query
 // also gets the lo piece x - bf16(x)), and its score factor sm_scale*log2(e)*q_scale (a padding head gets
-// zeros).  Block n_groups + p takes the largest row scale of partition p.
+// zeros).
 struct MxPrepArgs {
     const void *q_nope, *q_rope;
     int q_bf16, H, n_groups, P;
@@ -592,7 +611,6 @@ struct MxPrepArgs {
     int64_t T;
     uint8_t *img;     // [n_half][kQImg]
     float *c_head;    // [n_half * 64]
-    float *smax;      // [P]
 };
 constexpr int kMxPrepThreads = 256;  // 8 warps, one head each
 
@@ -602,7 +620,7 @@ __global__ void __launch_bounds__(kMxPrepThreads) mixed_prep_kernel(MxPrepArgs a
     grid_dependency_wait();
     grid_launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if ((int)blockIdx.x < a.n_groups) {
+    {
         const int hg = (int)blockIdx.x * (kMxPrepThreads / 32) + warp;
         const int half = hg / kHeads, h = hg - half * kHeads;
         uint8_t *img = a.img + (size_t)half * kQImg;
@@ -648,29 +666,6 @@ __global__ void __launch_bounds__(kMxPrepThreads) mixed_prep_kernel(MxPrepArgs a
         *reinterpret_cast<uint32_t *>(img + kQR + sw128_offset(h, 4u * lane)) = hi;
         if (!a.q_bf16) *reinterpret_cast<uint32_t *>(img + kQRLo + sw128_offset(h, 4u * lane)) = bf16x2_bits(rp.x - back.x, rp.y - back.y);
         if (lane == 0) a.c_head[hg] = hg < a.H ? a.sm_scale_log2 * qs : 0.f;
-    } else {
-        __shared__ float red[kMxPrepThreads / 32];
-        const int p = (int)blockIdx.x - a.n_groups;
-        const int64_t t0 = a.T * p / a.P, t1 = a.T * (p + 1) / a.P;
-        float mx = 0.f;
-        for (int64_t t = t0 + tid; t < t1; t += 4 * kMxPrepThreads) {
-            float v[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int64_t tu = t + (int64_t)u * kMxPrepThreads;
-                v[u] = tu < t1 ? __ldg(a.k_scale + tu) : 0.f;
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) mx = fmaxf(mx, fabsf(v[u]));
-        }
-        mx = warp_max(mx);
-        if (lane == 0) red[warp] = mx;
-        __syncthreads();
-        if (tid == 0) {
-            float m = 0.f;
-            for (int k = 0; k < kMxPrepThreads / 32; ++k) m = fmaxf(m, red[k]);
-            a.smax[p] = m;
-        }
     }
 }
 
@@ -686,7 +681,8 @@ int mixed_partitions(int H, int64_t T) {
 }
 
 size_t mixed_scratch_bytes(int H, int P) {
-    // query images, score factors, row-scale maxima (each 256-byte aligned)
+    // query images and score factors (each 256-byte aligned), then P floats that nothing writes any more
+    // (kept so that the workspace size stays what earlier callers sized)
     const size_t n_half = H > kHeads ? 2 : 1;
     return n_half * kQImg + ((n_half * kHeads * sizeof(float) + 255) & ~(size_t)255) +
            (((size_t)P * sizeof(float) + 255) & ~(size_t)255);
@@ -742,15 +738,13 @@ cudaError_t launch_attn_mixed(const void *q_nope, const void *q_rope, int q_bf16
     pa.T = T;
     pa.img = static_cast<uint8_t *>(scratch);
     pa.c_head = reinterpret_cast<float *>(pa.img + (size_t)a.n_half * kQImg);
-    pa.smax = pa.c_head + (((size_t)a.n_half * kHeads * sizeof(float) + 255) & ~(size_t)255) / sizeof(float);
     a.qimg = pa.img;
     a.c_head = pa.c_head;
-    a.smax = pa.smax;
     cudaError_t e =
         cudaFuncSetAttribute(attn_mixed_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t pcfg = {};
-    pcfg.gridDim = dim3((unsigned)(pa.n_groups + P));
+    pcfg.gridDim = dim3((unsigned)pa.n_groups);
     pcfg.blockDim = dim3(kMxPrepThreads);
     pcfg.stream = st;
     cudaLaunchAttribute pattr[1];
