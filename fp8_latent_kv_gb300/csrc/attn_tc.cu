@@ -191,6 +191,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&ms.q_full, 1);
         ms.abort_flag = 0;
         fence_barrier_init();
+        if (!idx_b && n_tiles > 0) {
+            // dense rows: tile 0's copies go out now (this is the producer lane), before the CTA-wide
+            // barrier -- they depend on nothing the other warps set up
+            const int y = (int)(seq_base + t0);
+            mbar_arrive_expect_tx(&ms.kv_full[0], kImg);
+            for (int kb = 0; kb < 4; ++kb) tma_load_2d(smem + OFF_ST0 + kb * 16384, &map_lc, kb * 128, y, &ms.kv_full[0]);
+            tma_load_2d(smem + OFF_ST0 + kRcOff, &map_rc, 512, y, &ms.kv_full[0]);
+        }
     }
     if (warp == 1) {
         tmem_alloc(&ms.tmem_base, 512);
@@ -212,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 prefetch_tensormap(&map_lc);
                 prefetch_tensormap(&map_rc);
             }
-            int issued = 0, armed = 0;
+            int issued = 0, armed = (!idx_b && n_tiles > 0) ? 1 : 0;  // dense tile 0: issued at the start
             // the query image (which depends on the query prep) goes out after the first tile's rows (which
             // do not), so that the first score waits for one tile and the image only
             const int q_at = n_tiles > 1 ? 1 : 0;
@@ -234,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // it; the rope block also holds tile i-2's weights and is refilled after the whole
                     // product.  The stage's full barrier is re-armed only after the first release: that
                     // implies tile i-2's phase of it has completed (one arrival per phase).
-                    if (lane == 0) {
+                    if (lane == 0 && i > 0) {
                         const int y = (int)(seq_base + p0);
                         for (int kb = 0; kb < 4 && ok_p; ++kb) {
                             if (i >= 2 && !(ok_p = mbar_wait(&ms.kv_blk[s][kb], ph, &ms.abort_flag, a.err_word))) break;
