@@ -758,15 +758,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // reused, and be done before its accumulators are rescaled.  lo_free is waited on every
                     // tile; pv_done only on a rescale, so it has one barrier per tile parity: the phase
                     // before the awaited one (tile i-3) is complete, which keeps the parity unambiguous.
+                    // lo_free also covers every MMA issued before the lo passes (the dims 0..255 passes):
+                    // pieces 0..3 are rescaled right away, pieces 4, 5 once the hi passes are done too.
                     if (ok) ok = mbar_wait(&ms.lo_free, (i - 1) & 1, &ms.abort_flag, a.err_word);
                     if (any_alpha) {
-                        if (ok) ok = mbar_wait(&ms.pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, &ms.abort_flag, a.err_word);
                         // rescale this group's columns of the six context accumulators, 32 columns per
                         // TMEM round trip
-                        tc_fence_after_sync();
                         constexpr int kPerTrip = 32 / kHG;  // accumulators per round trip
-#pragma unroll 1
-                        for (int c0 = 0; c0 < kOPieces; c0 += kPerTrip) {
+                        static_assert(4 % kPerTrip == 0, "pieces 0..3 and 4..5 in whole round trips");
+                        auto rescale_trip = [&](int c0) {
                             uint32_t o[kPerTrip][kHG];
 #pragma unroll
                             for (int c = 0; c < kPerTrip; ++c)
@@ -798,7 +798,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 for (int u = 0; u < kLd; ++u)
                                     tmem_st_32x32b_x16(tmem + lane_addr + TM_O + 64u * (c0 + c) + (uint32_t)h0 + 16u * u,
                                                        *reinterpret_cast<const uint32_t(*)[16]>(&o[c][16 * u]));
-                        }
+                        };
+                        tc_fence_after_sync();
+#pragma unroll 1
+                        for (int c0 = 0; c0 < 4; c0 += kPerTrip) rescale_trip(c0);
+                        if (ok) ok = mbar_wait(&ms.pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, &ms.abort_flag, a.err_word);
+                        tc_fence_after_sync();
+#pragma unroll 1
+                        for (int c0 = 4; c0 < kOPieces; c0 += kPerTrip) rescale_trip(c0);
                         tmem_wait_st();
                     }
                 }

@@ -41,6 +41,9 @@ constexpr int kKThreads = 512;
 constexpr int kKBins = 2048;
 constexpr int kKMaxC = 152;
 constexpr int kKCache = 8192;  // a CTA's scores staged in shared memory when its range is this short
+// unused dynamic shared memory that keeps the top-k at one CTA per SM: launched early behind the score
+// kernel, its CTAs would otherwise pack four to each of the first SMs that score CTAs leave
+constexpr int kKPadSmem = 80 * 1024;
 // per-query workspace (u32): three pass histograms, per-CTA (above, equal) counts, barrier counter
 constexpr int kKWsHist = 3 * kKBins;
 constexpr int kKWsPerItem = kKWsHist + 2 * kKMaxC + 32;
@@ -143,6 +146,8 @@ __global__ void __launch_bounds__(kIThreads, 1) index_score_kernel(const __grid_
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = sm.tmem_base;
+    // the top-k kernel may be launched now: it waits for this grid to complete before it reads anything
+    grid_launch_dependents();
 
     if (warp == 0) {
         // ================================ TMA producer ================================
@@ -349,6 +354,9 @@ __global__ void __launch_bounds__(kKThreads) topk_kernel(const float *__restrict
     const uint32_t k = (uint32_t)((int64_t)NS < T ? NS : T);
     const int64_t c0 = T * c / C, c1 = T * (c + 1) / C;
     if (tid == 0) abort_sh = 0;
+    // launched as a programmatic dependent of the score kernel: its scores and pass-0 histogram are
+    // complete and visible once this returns
+    grid_dependency_wait();
     // the CTA's keys, staged once when they fit (every pass below reads them again)
     const bool cached = c1 - c0 <= kKCache;
     if (cached)
@@ -515,12 +523,18 @@ cudaError_t launch_topk(const float *scores, int B, int64_t T, int NS, int32_t *
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(B * C));
     cfg.blockDim = dim3(kKThreads);
+    cfg.dynamicSmemBytes = kKPadSmem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kKPadSmem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;  // the CTAs of a query wait for one another
     attr[0].val.cooperative = C > 1 ? 1 : 0;
+    // a programmatic dependent of the score kernel: its launch overlaps that kernel's tail
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, topk_kernel, scores, T, NS, C, idx, static_cast<uint32_t *>(ws), err_word);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
