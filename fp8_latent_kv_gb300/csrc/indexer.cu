@@ -94,10 +94,12 @@ __global__ void __launch_bounds__(kIThreads, 1) index_score_kernel(const __grid_
 
     // The first epilogue group's warps load the query head rows and weights first, before any key tile
     // is requested: issued behind the key stream they would wait for it.  Lane j holds the weight of the
-    // warp's j-th head row; lane l holds elements 4l..4l+3 of each row.
+    // warp's j-th head row; lane l holds elements 4l..4l+3 of each row, as raw bits (f32: 16 bytes, bf16:
+    // 8 bytes in .x and .y) converted only where they are quantized, so that every load is in flight at
+    // once -- converting each row as it arrives took one memory round trip per row.
     constexpr int kRowsPerWarp = KV8_MAX_IDX_HEADS / 4;
     static_assert(kRowsPerWarp <= 32, "one head weight per lane");
-    float4 v[kRowsPerWarp];
+    uint4 qraw[kRowsPerWarp];
     float w_lane = 0.f;
     if (warp >= 2 && warp < 6) {
         const int hw = warp - 2 + 4 * lane;
@@ -105,16 +107,14 @@ __global__ void __launch_bounds__(kIThreads, 1) index_score_kernel(const __grid_
 #pragma unroll
         for (int j = 0; j < kRowsPerWarp; ++j) {
             const int h = warp - 2 + 4 * j;
-            v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            qraw[j] = make_uint4(0u, 0u, 0u, 0u);
             if (h < a.HI) {
                 const int64_t e = ((int64_t)b * a.HI + h) * kIdxD + 4 * lane;
                 if (a.q_bf16) {
-                    const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(a.q) + e));
-                    const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.x));
-                    const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.y));
-                    v[j] = make_float4(f0.x, f0.y, f1.x, f1.y);
+                    const uint2 r2 = __ldg(reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(a.q) + e));
+                    qraw[j] = make_uint4(r2.x, r2.y, 0u, 0u);
                 } else {
-                    v[j] = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(a.q) + e));
+                    qraw[j] = __ldg(reinterpret_cast<const uint4 *>(static_cast<const float *>(a.q) + e));
                 }
             }
         }
@@ -206,15 +206,24 @@ __global__ void __launch_bounds__(kIThreads, 1) index_score_kernel(const __grid_
             for (int j = 0; j < kRowsPerWarp; ++j) {
                 const int h = warp - 2 + 4 * j;
                 if (h >= HI) break;
+                float4 vj;
+                if (a.q_bf16) {
+                    const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qraw[j].x));
+                    const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qraw[j].y));
+                    vj = make_float4(f0.x, f0.y, f1.x, f1.y);
+                } else {
+                    vj = make_float4(__uint_as_float(qraw[j].x), __uint_as_float(qraw[j].y), __uint_as_float(qraw[j].z),
+                                     __uint_as_float(qraw[j].w));
+                }
                 float amax = 0.f;
-                amax = finite_abs_max(amax, v[j].x);
-                amax = finite_abs_max(amax, v[j].y);
-                amax = finite_abs_max(amax, v[j].z);
-                amax = finite_abs_max(amax, v[j].w);
+                amax = finite_abs_max(amax, vj.x);
+                amax = finite_abs_max(amax, vj.y);
+                amax = finite_abs_max(amax, vj.z);
+                amax = finite_abs_max(amax, vj.w);
                 amax = warp_max(amax);
                 float pre, mul, qs;
                 row_quant_factors(amax, pre, mul, qs);
-                *reinterpret_cast<uint32_t *>(sm.qimg + sw128_offset(h, 4 * lane)) = enc4(scale4(v[j], pre, mul));
+                *reinterpret_cast<uint32_t *>(sm.qimg + sw128_offset(h, 4 * lane)) = enc4(scale4(vj, pre, mul));
                 const float wj = __shfl_sync(0xffffffffu, w_lane, j);
                 if (lane == 0) sm.wq[h] = wj * qs;
             }
