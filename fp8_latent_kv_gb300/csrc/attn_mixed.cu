@@ -127,16 +127,6 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float a, float b) {  // a in the
 }
 
 // four consecutive query values as f32 (bf16 or f32 storage; 8- or 16-byte aligned)
-__device__ __forceinline__ float4 load4(const void *base, int64_t i, int bf16) {
-    if (bf16) {
-        const uint2 u = __ldg(reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(base) + i));
-        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
-        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
-        return make_float4(a.x, a.y, b.x, b.y);
-    }
-    return __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(base) + i));
-}
-
 // 10 warps, one CTA per SM (220 KB of shared memory).
 __global__ void __launch_bounds__(kThreads, 1)
     attn_mixed_tc_kernel(const __grid_constant__ CUtensorMap map_k8, const __grid_constant__ CUtensorMap map_k8b3,
@@ -625,21 +615,45 @@ __global__ void __launch_bounds__(kMxPrepThreads) mixed_prep_kernel(MxPrepArgs a
         const int half = hg / kHeads, h = hg - half * kHeads;
         uint8_t *img = a.img + (size_t)half * kQImg;
         constexpr int kF4 = kMxNope / 4;  // 112 groups of four, up to 4 per lane
-        float4 v[4];
+        // every load is issued before any is converted (raw bits: f32 16 bytes, bf16 8 bytes in .x and
+        // .y), so the five loads share one memory round trip
+        uint4 raw[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int f = j * 32 + lane;
-            v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (hg < a.H && f < kF4) v[j] = load4(a.q_nope, (int64_t)hg * kMxNope + 4 * f, a.q_bf16);
+            raw[j] = make_uint4(0u, 0u, 0u, 0u);
+            if (hg < a.H && f < kF4) {
+                const int64_t i = (int64_t)hg * kMxNope + 4 * f;
+                if (a.q_bf16) {
+                    const uint2 u = __ldg(reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(a.q_nope) + i));
+                    raw[j] = make_uint4(u.x, u.y, 0u, 0u);
+                } else {
+                    raw[j] = __ldg(reinterpret_cast<const uint4 *>(static_cast<const float *>(a.q_nope) + i));
+                }
+            }
         }
-        float2 rp = make_float2(0.f, 0.f);  // RoPE values 2*lane, 2*lane + 1
+        uint2 rraw = make_uint2(0u, 0u);  // RoPE values 2*lane, 2*lane + 1
         if (hg < a.H) {
             const int64_t e = (int64_t)hg * kMxRope + 2 * lane;
             if (a.q_bf16)
-                rp = __bfloat1622float2(__ldg(reinterpret_cast<const __nv_bfloat162 *>(a.q_rope) + e / 2));
+                rraw.x = __ldg(reinterpret_cast<const uint32_t *>(static_cast<const __nv_bfloat16 *>(a.q_rope) + e));
             else
-                rp = __ldg(reinterpret_cast<const float2 *>(a.q_rope) + e / 2);
+                rraw = __ldg(reinterpret_cast<const uint2 *>(static_cast<const float *>(a.q_rope) + e));
         }
+        float4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (a.q_bf16) {
+                const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw[j].x));
+                const float2 hi2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw[j].y));
+                v[j] = make_float4(lo.x, lo.y, hi2.x, hi2.y);
+            } else {
+                v[j] = make_float4(__uint_as_float(raw[j].x), __uint_as_float(raw[j].y), __uint_as_float(raw[j].z),
+                                   __uint_as_float(raw[j].w));
+            }
+        }
+        const float2 rp = a.q_bf16 ? __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&rraw.x))
+                                   : make_float2(__uint_as_float(rraw.x), __uint_as_float(rraw.y));
         float amax = 0.f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
