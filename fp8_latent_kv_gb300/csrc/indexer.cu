@@ -10,14 +10,16 @@
 // score kernel: the scores are a dense e4m3 contraction (HI heads x 128 x T rows), so they run on the
 // tensor cores: per 128-row key tile, S^T = K8 [Q8]^T with M = 128 rows, N = HI heads, K = 128 (four
 // kind::f8f6f4 MMAs of K = 32) into one of four TMEM accumulators.  Warp 0 streams key tiles through
-// six shared-memory stages with TMA, warp 1 issues the MMAs, warps 2..5 (one TMEM lane quadrant each)
-// read a row's HI scores, apply the ReLU and weights and store the row's score.  The CTA quantizes its
-// query's HI heads itself (same f32 steps as the row quantizer).  Every wait is bounded in time.
+// twelve shared-memory stages with TMA, warp 1 issues the MMAs, warps 2..9 (two groups of four, one TMEM
+// lane quadrant per warp, taking alternate tiles) read a row's HI scores, apply the ReLU and weights and
+// store the row's score.  The CTA quantizes its query's HI heads itself (same f32 steps as the row
+// quantizer).  Every wait is bounded in time.
 //
 // top-k kernel: a radix select over the scores' order-preserving 32-bit keys (11 + 11 + 10 bits) finds
 // the k-th largest key, then an index-ordered pass keeps every larger score and, among scores equal to
 // the k-th, the smallest positions -- written in ascending position order.  Each query's positions are
-// split over several CTAs of one cooperative launch that meet at bounded barriers.
+// split over several CTAs of one cooperative launch that meet at bounded barriers; the launch is a
+// programmatic dependent of the score kernel.
 #include "internal.h"
 #include "quant_row.cuh"
 #include "sm100.cuh"
