@@ -177,3 +177,24 @@ def test_workspace_reused_and_dirty(lib, oracle):
         assert np.array_equal(s_, outs[0][0]) and np.array_equal(i_, outs[0][1])
     for b in range(B):
         assert np.array_equal(outs[0][1][b], oracle.topk(outs[0][0][b], NS))
+
+
+def test_more_queries_than_ctas_per_wave(lib, oracle):
+    """B = 160 queries: more than the GPU's SMs, so each query gets one CTA (no barrier between CTAs, not
+    a cooperative launch) and the grid runs in more than one wave; short ragged key lists.  Every
+    query's selection = the oracle's top-k of the GPU scores; scores of two queries against the oracle."""
+    rng = np.random.default_rng(36)
+    B, HI, T, NS = 160, 16, 300, 64
+    rows = (rng.standard_normal((B * T, 128)) * 10.0 ** rng.uniform(-0.5, 0.5, (B * T, 1))).astype(np.float32)
+    k8, ks, tk8, tks = _keys(oracle, rows)
+    q = synth.to_bf16_values(rng.standard_normal((B, HI, 128)).astype(np.float32))
+    w = (rng.standard_normal((B, HI)) / 8).astype(np.float32)
+    scores, idx = _run(lib, _qtensor(q, True), torch.from_numpy(w).to(DEV), tk8, tks, B, T, T, NS)
+    q8, qs = oracle.quant_rows_w(q.reshape(B * HI, 128), 128)
+    q8, qs = q8.reshape(B, HI, 128), qs.reshape(B, HI)
+    for b in (0, B - 1):
+        ref = oracle.index_scores(q8[b:b + 1], qs[b:b + 1], w[b:b + 1], k8[b * T:(b + 1) * T], ks[b * T:(b + 1) * T], T, 0)[0]
+        err = np.abs(scores[b] - ref).max() / np.abs(ref).max()
+        assert err <= SCORE_TOL, f"query {b}: max error {err:.2e}"
+    for b in range(B):
+        assert np.array_equal(idx[b], oracle.topk(scores[b].astype(np.float64), NS)), f"query {b}"
