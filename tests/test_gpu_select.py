@@ -173,3 +173,17 @@ def test_select_repeated_calls_identical(lib, oracle):
         heads = [0, 77, 127]
         parity(first[:, heads], oracle.attn_select(ql[:, heads], qr[:, heads], q_o, s_o, T, T, idx,
                                                    synth.SM_SCALE)[0], f"NS={NS}")
+
+
+def test_select_more_sequences_than_one_wave(lib, oracle):
+    """B = 90 sequences x 2 head halves: more CTAs than SMs (one partition per sequence, the grid in two
+    waves behind the query prep); ragged lists of 200 positions; sampled heads of every sequence."""
+    B, T, H, NS = 90, 500, 128, 200
+    q_o, s_o, ql, qr, rng = _small(oracle, B, T, H, 9)
+    kv8, sc = torch.from_numpy(q_o).to(DEV), torch.from_numpy(s_o).to(DEV)
+    idx = np.stack([np.sort(rng.choice(T, NS, replace=False)) for _ in range(B)]).astype(np.int32)
+    got = _sel(lib, _bf(ql), _bf(qr), kv8, sc, T, T, torch.from_numpy(idx).to(DEV))
+    heads = [0, 64, 127]
+    ref, n_bad = oracle.attn_select(ql[:, heads], qr[:, heads], q_o, s_o, T, T, idx, synth.SM_SCALE)
+    assert n_bad == 0
+    parity(got[:, heads], ref, "90 sequences, sampled heads")
