@@ -14,6 +14,7 @@
 // and used for all rows, on the CUDA cores); more rows (prefill chunks) go to the tensor-core kernels of
 // proj8_tc.cu.
 #include "internal.h"
+#include "sm100.cuh"
 
 namespace kv8 {
 namespace {
@@ -50,14 +51,18 @@ __global__ void __launch_bounds__(256) q_absorb_small(const void *__restrict__ q
     __shared__ float qs[NS][kNope];
     __shared__ float4 red[8][NS][32];
     const int h = blockIdx.x, cb = blockIdx.y, tid = threadIdx.x, g = tid >> 5, lane = tid & 31;
-    for (int i = tid; i < NS * kNope; i += 256) {
-        const int s = i / kNope, j = i - s * kNope;
-        qs[s][j] = s < S ? load_act(q_nope, ((int64_t)s * H + h) * kNope + j, q_bf16) : 0.f;
-    }
+    // launched as a programmatic dependent: the weights (never written by the kernel before this one on the
+    // stream) stream in while that kernel finishes; the activations only after it has completed
+    sm100::grid_launch_dependents();
     const uint8_t *wb = w8 + ((int64_t)h * kKvbRows + 16 * g) * kKL + cb * kBlk + 4 * lane;
     uint32_t wv[16];
 #pragma unroll
     for (int r = 0; r < 16; ++r) wv[r] = __ldg(reinterpret_cast<const uint32_t *>(wb + (int64_t)r * kKL));
+    sm100::grid_dependency_wait();
+    for (int i = tid; i < NS * kNope; i += 256) {
+        const int s = i / kNope, j = i - s * kNope;
+        qs[s][j] = s < S ? load_act(q_nope, ((int64_t)s * H + h) * kNope + j, q_bf16) : 0.f;
+    }
     __syncthreads();
     float4 acc[NS];
 #pragma unroll
@@ -113,12 +118,9 @@ __global__ void __launch_bounds__(256) out_project_small(const float *__restrict
                                                          const float *__restrict__ w_scale, float *__restrict__ out) {
     __shared__ __align__(16) float xs[NS][kKL];
     const int h = blockIdx.x, v0 = blockIdx.y * 32, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    for (int i = tid; i < NS * kKL / 4; i += 256) {
-        const int s = i / (kKL / 4), c4 = i - s * (kKL / 4);
-        *reinterpret_cast<float4 *>(&xs[s][4 * c4]) =
-            s < S ? __ldg(reinterpret_cast<const float4 *>(ctx + ((int64_t)s * H + h) * kKL) + c4)
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    // launched as a programmatic dependent: the weights (never written by the kernel before this one on the
+    // stream) stream in while that kernel finishes; the context rows only after it has completed
+    sm100::grid_launch_dependents();
     uint32_t wv[4][kNbc];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -129,6 +131,13 @@ __global__ void __launch_bounds__(256) out_project_small(const float *__restrict
     float sc[kNbc];
 #pragma unroll
     for (int k = 0; k < kNbc; ++k) sc[k] = __ldg(w_scale + (int64_t)(2 * h + 1) * kNbc + k);
+    sm100::grid_dependency_wait();
+    for (int i = tid; i < NS * kKL / 4; i += 256) {
+        const int s = i / (kKL / 4), c4 = i - s * (kKL / 4);
+        *reinterpret_cast<float4 *>(&xs[s][4 * c4]) =
+            s < S ? __ldg(reinterpret_cast<const float4 *>(ctx + ((int64_t)s * H + h) * kKL) + c4)
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     __syncthreads();
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -159,26 +168,39 @@ __global__ void __launch_bounds__(256) out_project_small(const float *__restrict
 cudaError_t launch_q_absorb(const void *q_nope, int q_bf16, int S, int H, const uint8_t *w8, const float *w_scale,
                             void *q_lat, int out_bf16, int *err_word, cudaStream_t st) {
     if (S > kSmallS) return launch_q_absorb_tc(q_nope, q_bf16, S, H, w8, w_scale, q_lat, out_bf16, err_word, st);
-    const dim3 grid((unsigned)H, (unsigned)kNbc);
-    if (S <= 1)
-        q_absorb_small<1><<<grid, 256, 0, st>>>(q_nope, q_bf16, S, H, w8, w_scale, q_lat, out_bf16);
-    else if (S <= 4)
-        q_absorb_small<4><<<grid, 256, 0, st>>>(q_nope, q_bf16, S, H, w8, w_scale, q_lat, out_bf16);
-    else
-        q_absorb_small<kSmallS><<<grid, 256, 0, st>>>(q_nope, q_bf16, S, H, w8, w_scale, q_lat, out_bf16);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)H, (unsigned)kNbc);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e =
+        S <= 1   ? cudaLaunchKernelEx(&cfg, q_absorb_small<1>, q_nope, q_bf16, S, H, w8, w_scale, q_lat, out_bf16)
+        : S <= 4 ? cudaLaunchKernelEx(&cfg, q_absorb_small<4>, q_nope, q_bf16, S, H, w8, w_scale, q_lat, out_bf16)
+                 : cudaLaunchKernelEx(&cfg, q_absorb_small<kSmallS>, q_nope, q_bf16, S, H, w8, w_scale, q_lat, out_bf16);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 cudaError_t launch_out_project(const float *ctx, int S, int H, const uint8_t *w8, const float *w_scale, float *out,
                                int *err_word, cudaStream_t st) {
     if (S > kSmallS) return launch_out_project_tc(ctx, S, H, w8, w_scale, out, err_word, st);
-    const dim3 grid((unsigned)H, (unsigned)(kVH / 32));
-    if (S <= 1)
-        out_project_small<1><<<grid, 256, 0, st>>>(ctx, S, H, w8, w_scale, out);
-    else if (S <= 4)
-        out_project_small<4><<<grid, 256, 0, st>>>(ctx, S, H, w8, w_scale, out);
-    else
-        out_project_small<kSmallS><<<grid, 256, 0, st>>>(ctx, S, H, w8, w_scale, out);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)H, (unsigned)(kVH / 32));
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = S <= 1   ? cudaLaunchKernelEx(&cfg, out_project_small<1>, ctx, S, H, w8, w_scale, out)
+                          : S <= 4 ? cudaLaunchKernelEx(&cfg, out_project_small<4>, ctx, S, H, w8, w_scale, out)
+                                   : cudaLaunchKernelEx(&cfg, out_project_small<kSmallS>, ctx, S, H, w8, w_scale, out);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
