@@ -80,6 +80,9 @@ __global__ void __launch_bounds__(kPThreads, 1) q_absorb_tc_kernel(const void *_
         tmem_alloc(&sm.tmem_base, 512);
         tmem_relinquish();
     }
+    // a programmatic dependent: the weights (never written by the kernel before this one on the stream)
+    // are decoded while that kernel finishes; the activations are read only after it has completed
+    grid_launch_dependents();
     // W_UK[h] (e4m3 [128 j][512 c]) -> b[j / 64][c][j % 64] as bf16: item (j, c4) = 4 consecutive c;
     // each thread's loads go out 16 at a time
     static_assert(kNope * (kKL / 4) % (16 * kPThreads) == 0, "weight items split evenly");
@@ -133,6 +136,7 @@ __global__ void __launch_bounds__(kPThreads, 1) q_absorb_tc_kernel(const void *_
             }
         }
     };
+    grid_dependency_wait();
     load_tile(0);
     bool ok = true;
     for (int ti = 0; ti < n_tiles && ok; ++ti) {
@@ -264,6 +268,9 @@ __global__ void __launch_bounds__(kPThreads, 1) out_project_tc_kernel(const floa
         tmem_alloc(&sm.tmem_base, 512);
         tmem_relinquish();
     }
+    // a programmatic dependent: the weights (never written by the kernel before this one on the stream)
+    // are decoded while that kernel finishes; the context rows are read only after it has completed
+    grid_launch_dependents();
     // W_UV[h] (e4m3 [128 v][512 c]) -> b[c / 64][v][c % 64] as bf16: item (v, c8) = 8 consecutive c; each
     // thread's loads go out 16 at a time
     static_assert(kVH * (kKL / 8) % (16 * kPThreads) == 0, "weight items split evenly");
@@ -311,6 +318,7 @@ __global__ void __launch_bounds__(kPThreads, 1) out_project_tc_kernel(const floa
             }
         }
     };
+    grid_dependency_wait();
     load_stage(0, 0);
     bool ok = true;
     uint32_t phase = 0;
@@ -398,8 +406,18 @@ cudaError_t launch_q_absorb_tc(const void *q_nope, int q_bf16, int S, int H, con
     const size_t smem = sizeof(QTcSmem);
     cudaError_t e = cudaFuncSetAttribute(q_absorb_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    q_absorb_tc_kernel<<<(unsigned)H, kPThreads, smem, st>>>(q_nope, q_bf16, S, H, w8, w_scale, q_lat, out_bf16,
-                                                             err_word);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)H);
+    cfg.blockDim = dim3(kPThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, q_absorb_tc_kernel, q_nope, q_bf16, S, H, w8, w_scale, q_lat, out_bf16, err_word);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -408,7 +426,18 @@ cudaError_t launch_out_project_tc(const float *ctx, int S, int H, const uint8_t 
     const size_t smem = sizeof(OTcSmem);
     cudaError_t e = cudaFuncSetAttribute(out_project_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    out_project_tc_kernel<<<(unsigned)H, kPThreads, smem, st>>>(ctx, S, H, w8, w_scale, out, err_word);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)H);
+    cfg.blockDim = dim3(kPThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, out_project_tc_kernel, ctx, S, H, w8, w_scale, out, err_word);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
