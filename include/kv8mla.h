@@ -277,9 +277,9 @@ KV8_API int kv8_quant_rows_scatter(const float *x, int64_t n, const int64_t *dst
  * rows run on the CUDA cores (the weights read once); more on the tensor cores (kind::f16: every e4m3
  * weight is a bf16; f32 activations as bf16 hi + lo pieces).  err_word: optional (KV8_ERR_TIMEOUT).
  * S in [1, KV8_MAX_ROWS]; H in [1, 128]; all buffers 16-byte aligned; outputs must not overlap inputs.
- * Up to 8 rows the kernel is a programmatic dependent of the kernel launched before it on the stream: it
- * starts reading w8 and w_scale while that kernel finishes, and q_nope / ctx only after it has completed.
- * So w8 and w_scale must not be written by the kernel launched just before this call on the same stream.
+ * The kernels are programmatic dependents of the kernel launched before them on the stream: they start
+ * reading w8 and w_scale while that kernel finishes, and q_nope / ctx only after it has completed.  So
+ * w8 and w_scale must not be written by the kernel launched just before this call on the same stream.
  * --------------------------------------------------------------------------------------------- */
 KV8_API int mla_q_absorb8(const void *q_nope, int q_dtype, int S, int H, const uint8_t *w8, const float *w_scale,
                           void *q_lat, int out_dtype, int *err_word, void *stream);
