@@ -102,6 +102,29 @@ def test_topk_ties_and_short_lists(lib, oracle):
                 assert np.array_equal(got, np.arange(T)) and np.all(idx[b][T:] == -7)  # nothing past min(NS, T)
 
 
+@pytest.mark.parametrize("B,T,zero_frac", [(2, 20000, 0.9), (76, 10000, 0.9), (8, 40000, 0.95)])
+def test_topk_heavy_ties_across_ctas(lib, oracle, B, T, zero_frac):
+    """Most rows score exactly 0 and the k-th score is 0, so the selection ends inside a tie thousands of
+    keys long that spans every CTA of a query.  All B queries read the same key rows (stride 0) with their
+    own query.  On a 152-SM GPU a query has 76 CTAs (B=2), 2 CTAs of 5000 positions, ~4500 of them tied
+    (B=76), or 19 CTAs over 38,000 tied keys (B=8).  The selection must equal the oracle's top-k of the
+    GPU scores: every positive score, then the tied zeros from the smallest position on."""
+    HI = 16
+    rng = np.random.default_rng(T + B)
+    rows = rng.standard_normal((T, 128)).astype(np.float32)
+    rows[rng.random(T) < zero_frac] = 0.0
+    k8, ks, tk8, tks = _keys(oracle, rows)
+    q = synth.to_bf16_values(rng.standard_normal((B, HI, 128)).astype(np.float32))
+    w = np.abs(rng.standard_normal((B, HI))).astype(np.float32)
+    NS = 3000
+    scores, idx = _run(lib, _qtensor(q, True), torch.from_numpy(w).to(DEV), tk8, tks, B, T, 0, NS)
+    zero = ks == 0.0
+    assert np.all(scores[:, zero] == 0.0)
+    for b in range(B):
+        assert np.count_nonzero(scores[b] > 0) < NS  # the k-th score is 0
+        assert np.array_equal(idx[b], oracle.topk(scores[b].astype(np.float64), NS)), f"query {b}"
+
+
 def test_indexer_workload_sampled(lib, oracle):
     """The indexer workload (B=8 x T=131072, HI=64, NS=2048): scores of sequences 0 and 7 against the
     oracle; every sequence's selection = the oracle's top-k of the GPU scores."""
