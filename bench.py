@@ -996,11 +996,22 @@ def run_ours(args, rank, world, local_rank):
     w = synth.WORKLOADS[key]
     case = CASES[key](kv, torch, dev, w)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    # The L2 flush writes a buffer twice the L2's size, then reads a second one as large.  The write evicts
+    # every line of the step's data; the read evicts the write's dirty lines in turn.  So a timed step
+    # starts with none of its data in L2 and nothing to write back.  After the write alone, ~129 MB of
+    # dirty lines would be written back during the step, sharing the DRAM with its reads.
+    flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def l2_flush():
+        flush.zero_()
+        torch.sum(flush_rd, dim=0, out=flush_sink)
+
     stream = torch.cuda.Stream(device=dev)
 
     with torch.cuda.stream(stream):
         for _ in range(max(args.warmup, 3)):
-            flush.zero_()
+            l2_flush()
             case.step(stream)
             case.e2e_step(stream)
     torch.cuda.synchronize(dev)
@@ -1023,7 +1034,7 @@ def run_ours(args, rank, world, local_rank):
         case.e2e_step(stream)
     with torch.cuda.stream(stream):
         for _ in range(3):
-            flush.zero_()
+            l2_flush()
             g_step.replay()
             g_kern.replay()
             g_e2e.replay()
@@ -1040,11 +1051,11 @@ def run_ours(args, rank, world, local_rank):
     for k in range(args.steps):
         e0, e1 = E(), E()
         with torch.cuda.stream(stream):
-            flush.zero_()
+            l2_flush()
             e0.record(stream)
             g_step.replay()
             e1.record(stream)
-            flush.zero_()
+            l2_flush()
             k0.record(stream)
             g_kern.replay()
             k1.record(stream)
@@ -1070,6 +1081,19 @@ def run_ours(args, rank, world, local_rank):
         e1.synchronize()
         warm_ms.append(e0.elapsed_time(e1))
     warm_ms_mean = reduce_max(statistics.mean(warm_ms), dev)
+
+    # ---- the same steps after the write alone (the flush's dirty lines written back during the step)
+    wflush_ms = []
+    for k in range(args.steps):
+        e0, e1 = E(), E()
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            e0.record(stream)
+            g_step.replay()
+            e1.record(stream)
+        e1.synchronize()
+        wflush_ms.append(e0.elapsed_time(e1))
+    wflush_ms_mean = reduce_max(statistics.mean(wflush_ms), dev)
 
     # ---- clock soak: >= 1 s of back-to-back step replays with the clocks sampled throughout
     soak = None
@@ -1108,7 +1132,7 @@ def run_ours(args, rank, world, local_rank):
         ev = [(E(), E()) for _ in range(args.steps)]
         with torch.cuda.stream(stream):
             for k in range(args.steps):
-                flush.zero_()
+                l2_flush()
                 ev[k][0].record(stream)
                 fn()
                 ev[k][1].record(stream)
@@ -1131,7 +1155,8 @@ def run_ours(args, rank, world, local_rank):
     cfg = {"workload": synth.DESCRIPTIONS[key]}
     cfg.update(case.config())
     cfg.update({"step": case.step_desc,
-                "l2": f"flushed ({L2_FLUSH_BYTES >> 20} MiB write) before every timed step, outside the events",
+                "l2": (f"flushed before every timed step, outside the events: a {L2_FLUSH_BYTES >> 20} MiB write, then a "
+                       f"{L2_FLUSH_BYTES >> 20} MiB read of a second buffer (none of the step's data and no dirty line left in L2)"),
                 "timing": "each step is one replay of a CUDA graph of the step's library calls (captured once)",
                 "parallelism": f"replicas x{world}"})
     line = {
@@ -1148,6 +1173,9 @@ def run_ours(args, rank, world, local_rank):
         "clocks": {k: clk.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples", "power_w_max")},
         "warm_l2": {"value": whole_job_us_per_step(warm_ms_mean, world), "unit": case.unit,
                     "how": "the same step replays without the L2 flush before each step"},
+        "l2_write_flush": {"value": whole_job_us_per_step(wflush_ms_mean, world), "unit": case.unit,
+                           "how": (f"the same step after the {L2_FLUSH_BYTES >> 20} MiB write alone: the write's "
+                                   "dirty lines are written back during the step")},
         "clock_soak": soak,
         "wall_s_timed_region": wall_s,
     }
